@@ -1,0 +1,90 @@
+"""Seeded synthetic inputs and the named workloads.
+
+This module holds no attention arithmetic: it only draws random tensors.  It
+is the one module that both the CUDA path's callers (tests, bench, smoke) and
+the oracle-side checks use, so both see identical input bits.
+
+Recipe: a CPU ``torch.Generator`` seeded with the workload's seed draws q, k,
+v and dO, in that order, as float32 ``randn * std``; each is then rounded to
+the workload's 16-bit dtype (round to nearest even).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import numpy as np
+import torch
+
+_TORCH_DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Lq: int
+    Lk: int
+    D: int
+    dtype: str = "bf16"
+    std: float = 1.0
+    causal: bool = True
+    seed: int = 1000
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(D) rounded to float32 (the value the C ABI receives)."""
+        return float(np.float32(1.0 / math.sqrt(self.D)))
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPES[self.dtype]
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads, shaped like the ones the pages measure or describe.
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_gqa_l128_d64", B=1, Hq=2, Hkv=1, Lq=128, Lk=128, D=64, seed=1000),
+        Workload("llama_gqa_l2048_d128", B=2, Hq=32, Hkv=8, Lq=2048, Lk=2048, D=128, seed=1001),
+        Workload("qwen3_8b_gqa_l8192_d128", B=1, Hq=32, Hkv=8, Lq=8192, Lk=8192, D=128, seed=1002),
+        Workload("gqa_l8192_d256", B=1, Hq=16, Hkv=2, Lq=8192, Lk=8192, D=256, seed=1003),
+        Workload(
+            "ragged_mha_q4064_k4112_d96",
+            B=4, Hq=16, Hkv=16, Lq=4064, Lk=4112, D=96, dtype="fp16", std=0.5, seed=1004,
+        ),
+    ]
+}
+
+# Long-context memory check shape (same heads as the 8192 workload).
+MEMORY_CHECK = WORKLOADS["qwen3_8b_gqa_l8192_d128"].with_(
+    name="qwen3_8b_gqa_l23040_d128_memcheck", Lq=23040, Lk=23040, seed=1005
+)
+
+
+def make_inputs(w: Workload, device: str | torch.device = "cpu"):
+    """q, k, v, dO as contiguous [B, H, L, D] tensors of the workload's dtype."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    shapes = [
+        (w.B, w.Hq, w.Lq, w.D),
+        (w.B, w.Hkv, w.Lk, w.D),
+        (w.B, w.Hkv, w.Lk, w.D),
+        (w.B, w.Hq, w.Lq, w.D),
+    ]
+    out = []
+    for s in shapes:
+        t = torch.randn(s, generator=gen, dtype=torch.float32) * w.std
+        out.append(t.to(w.torch_dtype).to(device).contiguous())
+    return tuple(out)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    """Exact decode of a 16-bit (or fp32) tensor to a float64 numpy array."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
