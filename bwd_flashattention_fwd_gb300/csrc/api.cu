@@ -1,0 +1,214 @@
+// C ABI of libgbattn.so (declared in include/gbattn.h): argument validation,
+// the per-device status word, and dispatch to the per-head-dimension
+// launchers.  Validation is synchronous and touches no device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/gbattn.h"
+#include "launch.h"
+
+namespace gbattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+int* g_status[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+uint64_t wait_limit_ns() {
+  static const uint64_t v = [] {
+    const char* s = std::getenv("GBATTN_WAIT_LIMIT_NS");
+    if (s && *s) {
+      const unsigned long long x = std::strtoull(s, nullptr, 10);
+      if (x > 0) return static_cast<uint64_t>(x);
+    }
+    return static_cast<uint64_t>(2000000000ull);
+  }();
+  return v;
+}
+
+// Per-device state created on first use: the tensor-map encoder (a driver
+// entry point), the device status word (one int, zeroed) and the SM count.
+attn_status_t device_state(int* dev_out, EncodeTiledFn* enc, int** status, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if (!g_status[dev]) {
+    int* p = nullptr;
+    if (cudaMalloc(&p, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_num_sms[dev] = sms;
+    g_status[dev] = p;
+  }
+  *dev_out = dev;
+  *enc = g_encode;
+  *status = g_status[dev];
+  *num_sms = g_num_sms[dev];
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_d(int D) { return D == 64 || D == 96 || D == 128 || D == 256; }
+
+attn_status_t check_common(int B, int Hq, int Lq, int D, attn_dtype_t dtype) {
+  if (B <= 0 || Hq <= 0 || Lq <= 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_FP16 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!supported_d(D)) return ATTN_ERR_UNSUPPORTED;
+  // grid limits: B*H CTAs along x, 64-row tiles along y
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if ((Lq + 63) / 64 > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status_t check_attention(int B, int Hq, int Hkv, int Lq, int Lk, int D, float scale, int causal,
+                              attn_dtype_t dtype) {
+  const attn_status_t s = check_common(B, Hq, Lq, D, dtype);
+  if (s == ATTN_ERR_INVALID_ARG) return s;
+  if (Hkv <= 0 || Lk <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (causal && Lq > Lk) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (s != ATTN_OK) return s;
+  if ((Lk + 63) / 64 > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status_t finish(int r) {
+  if (r == kLaunchOk) return ATTN_OK;
+  if (r == kLaunchBadMap) return ATTN_ERR_INVALID_ARG;
+  return ATTN_ERR_CUDA;
+}
+
+int dispatch_fwd(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_fwd_d64(a);
+    case 96: return launch_fwd_d96(a);
+    case 128: return launch_fwd_d128(a);
+    default: return launch_fwd_d256(a);
+  }
+}
+int dispatch_bwd(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_bwd_d64(a);
+    case 96: return launch_bwd_d96(a);
+    case 128: return launch_bwd_d128(a);
+    default: return launch_bwd_d256(a);
+  }
+}
+int dispatch_delta(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_delta_d64(a);
+    case 96: return launch_delta_d96(a);
+    case 128: return launch_delta_d128(a);
+    default: return launch_delta_d256(a);
+  }
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                  cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dispatch_fwd(a));
+}
+
+extern "C" attn_status_t attn_bwd_delta(const void* o, const void* dO, float* delta, int B, int Hq, int Lq, int D,
+                                        attn_dtype_t dtype, cudaStream_t stream) {
+  if (!o || !dO || !delta) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(delta)) return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_common(B, Hq, Lq, D, dtype);
+  if (s != ATTN_OK) return s;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.o = o, a.dO = dO, a.delta_out = delta;
+  a.B = B, a.Hq = Hq, a.Hkv = Hq, a.Lq = Lq, a.Lk = Lq, a.D = D;
+  a.bf16 = dtype == ATTN_DTYPE_BF16, a.stream = stream;
+  return finish(dispatch_delta(a));
+}
+
+extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                  const float* lse, const float* delta, void* dq, void* dk, void* dv, int B, int Hq,
+                                  int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                  cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !delta || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta;
+  a.dq = dq, a.dk = dk, a.dv = dv;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dispatch_bwd(a));
+}
+
+extern "C" attn_status_t attn_last_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  int* p;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    p = g_status[dev];
+  }
+  if (!p) return ATTN_OK;
+  int h = 0;
+  if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h != 0) {
+    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+extern "C" const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}

@@ -1,0 +1,266 @@
+// Forward attention with saved base-2 log-sum-exp.
+//
+// One CTA owns a tile of BQ = 128 query rows of one (batch, query head) and
+// walks the visible key tiles with an online softmax ("When the Bottleneck
+// Moved", section 3: m_new = max(m_old, rowmax S), alpha = exp(m_old - m_new),
+// l_new = alpha l_old + rowsum p, acc_new = alpha acc_old + p V, then
+// O = acc / l and L = m + log l), kept in the log2 domain ("feat(attention):
+// complete Flash Attention VJP implementation", section "Background":
+// P = exp2(S * scale_log2 - LSE)).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread t of warp w owns query row 32w+t, which is TMEM
+//              lane 32w+t of every accumulator;
+//   warp 4     TMA producer: Q once, then K/V tiles into a STAGES-deep ring;
+//   warp 5     MMA issuer (one thread) and TMEM owner.
+// Tensor memory (512 columns): O (D columns, fp32), two S buffers (BK columns
+// each, fp32) and two P buffers (BK/2 columns, bf16/fp16 pairs).  S_j = Q K_j^T
+// runs on the tensor cores while the softmax warps turn S_{j-1} into P_{j-1};
+// O += P_j V_j reads P straight from tensor memory.
+#pragma once
+
+#include "kernel_common.cuh"
+
+namespace gbattn {
+
+template <int D>
+struct FwdGeom {
+  static constexpr int BQ = 128;
+  static constexpr int BK = (D == 256) ? 64 : 128;
+  static constexpr int NCH = n_chunks(D);
+  static constexpr int Q_BYTES = NCH * BQ * 128;
+  static constexpr int KV_BYTES = NCH * BK * 128;
+  static constexpr int STAGES_FIT = (kMaxDynSmem - kSmemReserve - 1024 - Q_BYTES) / (2 * KV_BYTES);
+  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * 2 * KV_BYTES;
+  static constexpr int O_COL = 0;
+  static constexpr int S_COL0 = (D <= 128) ? 128 : 256;
+  static constexpr int S_COL1 = S_COL0 + BK;
+  static constexpr int P_COL0 = S_COL1 + BK;
+  static constexpr int P_COL1 = P_COL0 + BK / 2;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_THREADS = 192;
+  static_assert(STAGES >= 2, "need a double-buffered K/V ring");
+  static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using Gm = FwdGeom<D>;
+  using E = Elem<BF16>;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kfull[ST], bar_vfull[ST], bar_kvempty[ST], bar_sfull[2],
+      bar_pready[2], bar_odone, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = sbase;
+  const uint32_t sK0 = sQ + Gm::Q_BYTES;
+  const uint32_t sV0 = sK0 + ST * Gm::KV_BYTES;
+
+  const int bh = blockIdx.x;  // b * Hq + hq
+  const int b = bh / p.Hq, hq = bh - b * p.Hq;
+  const int hk = hq / p.G;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
+  const int q0 = qt * BQ;
+  const int q_hi = min(q0 + BQ, p.Lq);
+  const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
+  const int n_kv = (kv_end + BK - 1) / BK;
+  const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(smem_u32(&bar_kfull[s]), 1);
+      mbar_init(smem_u32(&bar_vfull[s]), 1);
+      mbar_init(smem_u32(&bar_kvempty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_sfull[i]), 1);
+      mbar_init(smem_u32(&bar_pready[i]), 128);
+    }
+    mbar_init(smem_u32(&bar_odone), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int zkv = b * p.Hkv + hk;
+      mbar_arrive_expect_tx(smem_u32(&bar_q), Gm::Q_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % ST, u = j / ST;
+        if (u > 0) mbar_wait(smem_u32(&bar_kvempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 1);
+        mbar_arrive_expect_tx(smem_u32(&bar_kfull[s]), Gm::KV_BYTES);
+        for (int c = 0; c < NCH; ++c)
+          tma_load_3d(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64,
+                      j * BK, zkv);
+        mbar_arrive_expect_tx(smem_u32(&bar_vfull[s]), Gm::KV_BYTES);
+        for (int c = 0; c < NCH; ++c)
+          tma_load_3d(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64,
+                      j * BK, zkv);
+      }
+      // Do not leave the CTA while a copy may still be landing.
+      for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
+        mbar_wait_drain(smem_u32(&bar_vfull[j % ST]), (j / ST) & 1, p.limit_ns);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
+      constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
+      mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 2);
+      tc_fence_after_sync();
+      for (int j = 0; j <= n_kv; ++j) {
+        if (j < n_kv) {
+          const int s = j % ST;
+          mbar_wait(smem_u32(&bar_kfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 3);
+          tc_fence_after_sync();
+          const uint32_t d = tmem + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
+          const uint32_t kbase = sK0 + s * Gm::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = make_sdesc_sw128(sQ + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = make_sdesc_sw128(kbase + (kk >> 2) * (BK * 128) + (kk & 3) * 32, 16, 1024);
+            mma_ss(d, a, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bar_sfull[j & 1]));
+        }
+        if (j >= 1) {
+          const int jp = j - 1, sp = jp % ST;
+          mbar_wait(smem_u32(&bar_pready[jp & 1]), (jp >> 1) & 1, g, kDevTimeoutBase + 4);
+          mbar_wait(smem_u32(&bar_vfull[sp]), (jp / ST) & 1, g, kDevTimeoutBase + 5);
+          tc_fence_after_sync();
+          const uint32_t pcol = tmem + ((jp & 1) ? Gm::P_COL1 : Gm::P_COL0);
+          const uint32_t vbase = sV0 + sp * Gm::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bd = make_sdesc_sw128(vbase + kk * 2048, BK * 128, 1024);
+            mma_ts(tmem + Gm::O_COL, pcol + kk * 8, bd, IDESC_PV, (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bar_kvempty[sp]));
+          mma_commit(smem_u32(&bar_odone));
+        }
+      }
+      // Wait for every MMA of this CTA before tensor memory is released.
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait_drain(smem_u32(&bar_drain), 0, p.limit_ns);
+    }
+  } else {
+    // ---------------- softmax warps ----------------
+    const int r = warp * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    // last visible key of this row (inclusive)
+    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_kv; ++j) {
+      mbar_wait(smem_u32(&bar_sfull[j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 6);
+      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t scol = tmem + lrow + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
+      float x[BK];
+#pragma unroll
+      for (int c = 0; c < BK / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(scol + c * 32, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]) * sl2;
+      }
+      const int k0 = j * BK;
+      const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < BK; ++i)
+          if (k0 + i > lim) x[i] = -INFINITY;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int i = 1; i < BK; ++i) mt = fmaxf(mt, x[i]);
+      const float m_new = fmaxf(m, mt);
+      const float alpha = ex2_approx(m - m_new);
+      float sum = 0.f;
+      const uint32_t pcol = tmem + lrow + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
+#pragma unroll
+      for (int c = 0; c < BK / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(x[c * 32 + 2 * i] - m_new);
+          const float p1 = ex2_approx(x[c * 32 + 2 * i + 1] - m_new);
+          sum += p0 + p1;
+          pk[i] = E::pack(p0, p1);
+        }
+        tmem_st16(pcol + c * 16, pk);
+      }
+      l = l * alpha + sum;
+      if (j > 0) {
+        // O holds P_{j-1} V_{j-1} only once that MMA is done; rescale after it.
+        mbar_wait(smem_u32(&bar_odone), (j - 1) & 1, g, kDevTimeoutBase + 7);
+        __syncwarp();
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(tmem + lrow + Gm::O_COL + c * 32, rr);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_pready[j & 1]));
+      m = m_new;
+    }
+    // ---------------- epilogue ----------------
+    mbar_wait(smem_u32(&bar_odone), (n_kv - 1) & 1, g, kDevTimeoutBase + 8);
+    __syncwarp();
+    tc_fence_after_sync();
+    const float inv_l = 1.f / l;
+    typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
+      tmem_ld_wait(rr);
+      if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
+    }
+    if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+}
+
+}  // namespace gbattn

@@ -1,0 +1,171 @@
+// Kernel instantiations and launchers for one head dimension.  The build
+// compiles this file once per supported D with -DGBATTN_HEAD_DIM=<D>, so the
+// four translation units compile in parallel.
+#include "launch.h"
+
+#include "bwd_dkv_kernel.cuh"
+#include "bwd_dq_kernel.cuh"
+#include "delta_kernel.cuh"
+#include "fwd_kernel.cuh"
+
+#ifndef GBATTN_HEAD_DIM
+#error "compile with -DGBATTN_HEAD_DIM=<64|96|128|256>"
+#endif
+
+#define GBATTN_CAT2(a, b) a##b
+#define GBATTN_CAT(a, b) GBATTN_CAT2(a, b)
+
+namespace gbattn {
+// A namespace per head dimension: the four objects are built from this one
+// file and are linked together.
+namespace GBATTN_CAT(inst_d, GBATTN_HEAD_DIM) {
+
+constexpr int kD = GBATTN_HEAD_DIM;
+
+// Rank-3 view [B*H, L, D] of a contiguous [B, H, L, D] tensor; boxes of
+// 64 columns x box_rows rows with the 128-byte swizzle the MMA descriptors
+// expect.  Rows past L (and columns past D) read as zeros.
+bool make_map(const AttnArgs& a, CUtensorMap* m, const void* base, int L, int BH, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(kD) * 2 * static_cast<cuuint64_t>(L)};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+  const CUresult r = a.encode(m, a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                              3, const_cast<void*>(base), dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename Kern>
+int launch(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, const CUtensorMap& a0,
+           const CUtensorMap& a1, const CUtensorMap& a2, const FwdParams& p) {
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kLaunchCudaError;
+  kern<<<grid, threads, smem, stream>>>(a0, a1, a2, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
+template <typename Kern>
+int launch(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, const CUtensorMap& a0,
+           const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& a3, const BwdParams& p) {
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kLaunchCudaError;
+  kern<<<grid, threads, smem, stream>>>(a0, a1, a2, a3, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
+template <bool BF16, bool CAUSAL>
+int fwd_impl(const AttnArgs& a) {
+  using Gm = FwdGeom<kD>;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+    return kLaunchBadMap;
+  FwdParams p{};
+  p.o = a.o_out;
+  p.lse = a.lse_out;
+  p.status = a.status;
+  p.B = a.B, p.Hq = a.Hq, p.Hkv = a.Hkv, p.Lq = a.Lq, p.Lk = a.Lk, p.G = a.Hq / a.Hkv;
+  p.off = a.Lk - a.Lq;
+  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.limit_ns = a.limit_ns;
+  const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  return launch(attn_fwd_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
+                tv, p);
+}
+
+BwdParams bwd_params(const AttnArgs& a) {
+  BwdParams p{};
+  p.dq = a.dq;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.status = a.status;
+  p.B = a.B, p.Hq = a.Hq, p.Hkv = a.Hkv, p.Lq = a.Lq, p.Lk = a.Lk, p.G = a.Hq / a.Hkv;
+  p.off = a.Lk - a.Lq;
+  p.scale = a.scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.limit_ns = a.limit_ns;
+  return p;
+}
+
+template <bool BF16, bool CAUSAL, int MODE>
+int dkv_impl(const AttnArgs& a) {
+  using Gm = DkvGeom<kD, MODE>;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+    return kLaunchBadMap;
+  BwdParams p = bwd_params(a);
+  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+  p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
+  const dim3 grid(a.B * a.Hkv, p.n_ktiles);
+  return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL, MODE>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
+                tq, tk, tv, tdo, p);
+}
+
+template <bool BF16, bool CAUSAL>
+int dq_impl(const AttnArgs& a) {
+  using Gm = DqGeom<kD>;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+    return kLaunchBadMap;
+  BwdParams p = bwd_params(a);
+  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+  p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
+  const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
+                tv, tdo, p);
+}
+
+template <bool BF16, bool CAUSAL>
+int bwd_impl(const AttnArgs& a) {
+  int r;
+  if constexpr (kD <= 128) {
+    r = dkv_impl<BF16, CAUSAL, kDkvBoth>(a);
+  } else {
+    r = dkv_impl<BF16, CAUSAL, kDkvDvOnly>(a);
+    if (r == kLaunchOk) r = dkv_impl<BF16, CAUSAL, kDkvDkOnly>(a);
+  }
+  if (r != kLaunchOk) return r;
+  return dq_impl<BF16, CAUSAL>(a);
+}
+
+template <bool BF16>
+int delta_impl(const AttnArgs& a) {
+  using Gm = DeltaGeom<kD>;
+  const long long rows = static_cast<long long>(a.B) * a.Hq * a.Lq;
+  const long long rows_per_block = static_cast<long long>(Gm::THREADS / 32) * Gm::ROWS_PER_WARP * Gm::UNROLL;
+  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  const long long cap = static_cast<long long>(a.num_sms > 0 ? a.num_sms : 152) * 8;
+  if (blocks > cap) blocks = cap;
+  attn_delta_kernel<kD, BF16><<<static_cast<unsigned>(blocks), Gm::THREADS, 0, a.stream>>>(a.o, a.dO, a.delta_out,
+                                                                                            rows);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
+}  // namespace inst_d<D>
+
+using namespace GBATTN_CAT(inst_d, GBATTN_HEAD_DIM);
+
+int GBATTN_CAT(launch_fwd_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? fwd_impl<true, true>(a) : fwd_impl<true, false>(a);
+  return a.causal ? fwd_impl<false, true>(a) : fwd_impl<false, false>(a);
+}
+
+int GBATTN_CAT(launch_bwd_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? bwd_impl<true, true>(a) : bwd_impl<true, false>(a);
+  return a.causal ? bwd_impl<false, true>(a) : bwd_impl<false, false>(a);
+}
+
+int GBATTN_CAT(launch_delta_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  return a.bf16 ? delta_impl<true>(a) : delta_impl<false>(a);
+}
+
+}  // namespace gbattn

@@ -1,0 +1,152 @@
+"""Thin Python binding of libgbattn.so (declared in include/gbattn.h).
+
+Argument marshalling only: torch tensors supply device pointers, shapes and
+the stream; every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgbattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_DTYPE_FP16 = 0
+ATTN_DTYPE_BF16 = 1
+
+EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_last_device_status", "attn_status_string")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} failed: {status_string(status)} ({status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgbattn.so once and declare its C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is not built; run bwd_flashattention_fwd_gb300.build.build() (or __graft_entry__.build())"
+        )
+    lib = ctypes.CDLL(path)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_fwd.restype = ci
+    lib.attn_bwd_delta.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp]
+    lib.attn_bwd_delta.restype = ci
+    lib.attn_bwd.argtypes = [vp] * 10 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd.restype = ci
+    lib.attn_last_device_status.argtypes = [vp]
+    lib.attn_last_device_status.restype = ci
+    lib.attn_status_string.argtypes = [ci]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_DTYPE_BF16
+    if t.dtype == torch.float16:
+        return ATTN_DTYPE_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16 or float16")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(status: int, call: str, check: bool) -> int:
+    if check and status != ATTN_OK:
+        raise AttnError(status, call)
+    return status
+
+
+def attn_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None, check: bool = True) -> int:
+    """O and base-2 LSE of causal/non-causal GQA attention (writes o, lse)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Lq, Lk, D,
+                                 float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_fwd", check)
+
+
+def attn_bwd_delta(o, dO, delta, stream=None, check: bool = True) -> int:
+    """delta = rowsum(dO * O) in float32 (writes delta)."""
+    B, Hq, Lq, D = o.shape
+    st = load_library().attn_bwd_delta(_ptr(o), _ptr(dO), _ptr(delta), B, Hq, Lq, D, _dtype_code(o),
+                                       _stream_handle(stream))
+    return _check(st, "attn_bwd_delta", check)
+
+
+def attn_bwd(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bool, stream=None,
+             check: bool = True) -> int:
+    """dQ, dK, dV of the attention (writes dq, dk, dv)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D, float(scale),
+                                 int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_bwd", check)
+
+
+def attn_last_device_status(stream=None) -> int:
+    return load_library().attn_last_device_status(_stream_handle(stream))
+
+
+def attn_status_string(status: int) -> str:
+    return status_string(status)
+
+
+# ---------------------------------------------------------------------------
+# Conveniences that allocate the outputs with torch and call the ABI.
+# ---------------------------------------------------------------------------
+
+
+def forward(q, k, v, scale: float, causal: bool = True, stream=None):
+    B, Hq, Lq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def delta(o, dO, stream=None):
+    B, Hq, Lq, _ = o.shape
+    d = torch.empty((B, Hq, Lq), dtype=torch.float32, device=o.device)
+    attn_bwd_delta(o, dO, d, stream)
+    return d
+
+
+def backward(q, k, v, o, dO, lse, dlt, scale: float, causal: bool = True, stream=None):
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    attn_bwd(q, k, v, o, dO, lse, dlt, dq, dk, dv, scale, causal, stream)
+    return dq, dk, dv

@@ -1,0 +1,112 @@
+/*
+ * gbattn -- exact causal grouped-query attention (forward with saved
+ * log-sum-exp, delta precompute, fused two-kernel backward) for NVIDIA GB300
+ * (sm_103a).  C ABI of libgbattn.so.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every tensor pointer is a DEVICE pointer owned by the caller.
+ *   The library never allocates per-call device memory and never frees caller
+ *   memory.  Each pointer must be 16-byte aligned.
+ * Layout.  Contiguous row-major [B, H, L, D]: D is the fastest axis, then the
+ *   sequence position, then the head, then the batch.  q, o, dO, dq use
+ *   H = Hq and L = Lq; k, v, dk, dv use H = Hkv and L = Lk.  lse and delta are
+ *   float32 [B, Hq, Lq].  dq/dk/dv/o are written in the input dtype.
+ * GQA.  Query head hq reads KV head hq / (Hq / Hkv): consecutive query heads
+ *   share a KV head.
+ * Causal alignment.  Bottom-right: key j is visible to query i iff
+ *   j <= i + (Lk - Lq).  The offset comes from the true lengths ("Add a fused
+ *   full-attention path for head_dim 256 on NAX devices", section "Ragged
+ *   causal inputs").  Causal calls need Lk >= Lq, so every row sees a key.
+ * Shapes.  B, Hq, Hkv, Lq, Lk >= 1; Hq % Hkv == 0; D in {64, 96, 128, 256}.
+ *   Lq and Lk are arbitrary (ragged tails are masked inside the kernels).
+ * Streams and errors.  Every call validates its arguments on the host first,
+ *   without touching device memory, and returns ATTN_ERR_INVALID_ARG or
+ *   ATTN_ERR_UNSUPPORTED before launching anything.  Otherwise it enqueues its
+ *   kernels on `stream` and returns without synchronising; a launch failure
+ *   returns ATTN_ERR_CUDA.  There is no fallback path: an unsupported shape is
+ *   an error, never a silent change of implementation.  Device-side waits are
+ *   bounded; a wait that runs out records ATTN_ERR_TIMEOUT in a device status
+ *   word that attn_last_device_status() reports.
+ */
+#ifndef GBATTN_H_
+#define GBATTN_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,
+  ATTN_ERR_UNSUPPORTED = 2,
+  ATTN_ERR_CUDA = 3,
+  ATTN_ERR_TIMEOUT = 4
+} attn_status_t;
+
+typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
+
+/*
+ * Forward with saved log-sum-exp.
+ *   O = softmax(scale * Q K^T + mask) V, and per query row the base-2
+ *   log-sum-exp lse_i = log2 sum_{j visible} exp2(scale * log2(e) * q_i.k_j).
+ * Computed by an online softmax over key tiles ("When the Bottleneck Moved",
+ * section 3, the running m / l / acc update and O = acc / l, L = m + log l),
+ * in the log2 domain ("feat(attention): complete Flash Attention VJP
+ * implementation", section "Background": P = exp2(S * scale_log2 - LSE)).
+ *   q [B,Hq,Lq,D], k and v [B,Hkv,Lk,D]: inputs (dtype).
+ *   o [B,Hq,Lq,D]: output (dtype).  lse [B,Hq,Lq]: output, float32, base 2.
+ *   scale: finite and > 0 (usually 1/sqrt(D)).  causal: 0 or 1.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int D, float scale, int causal,
+                       attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * delta_i = sum_d float(dO_id) * float(O_id), float32 accumulation
+ * ("feat(attention): complete Flash Attention VJP implementation", sections
+ * "Reference implementation" and "Two-Kernel Design": delta = rowsum(dO * O)
+ * computed once, before the two gradient kernels).
+ *   o, dO [B,Hq,Lq,D]: inputs (dtype); o is the forward's stored output.
+ *   delta [B,Hq,Lq]: output, float32.
+ */
+attn_status_t attn_bwd_delta(const void* o, const void* dO, float* delta, int B, int Hq, int Lq,
+                             int D, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Fused backward: one dQ kernel (owns query rows, loops over key tiles) and
+ * one dK/dV kernel (owns key rows, loops over the GQA group then query tiles),
+ * so no output is shared and no atomics are needed ("feat(attention):
+ * complete Flash Attention VJP implementation", sections "Background" and
+ * "Two-Kernel Design").  Both recompute
+ *   S = Q K^T,  P = exp2(S * scale * log2(e) - lse),  dP = dO V^T,
+ *   dS = P * (dP - delta),
+ * and accumulate dQ = scale * dS K, dK = scale * dS^T Q, dV = P^T dO.
+ *   q, k, v, o, dO: inputs (dtype; o is accepted for interface symmetry and is
+ *   only read through delta).  lse from attn_fwd and delta from attn_bwd_delta
+ *   of the same (q, k, v, scale, causal): float32 [B,Hq,Lq].
+ *   dq [B,Hq,Lq,D], dk and dv [B,Hkv,Lk,D]: outputs (dtype), fully overwritten.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, const float* delta, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int D, float scale, int causal,
+                       attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the device status word of the
+ * current device: ATTN_ERR_TIMEOUT if a bounded device-side wait ran out in a
+ * kernel since the last call, ATTN_ERR_CUDA if the stream reported an error,
+ * ATTN_OK otherwise.
+ */
+attn_status_t attn_last_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H_ */

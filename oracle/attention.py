@@ -155,6 +155,68 @@ def forward_rows(q, k, v, scale: float, causal: bool, b: int, hq: int, rows):
     return O, (m + np.log(l))[:, 0] * LOG2E
 
 
+def lse_all_rows(q, k, scale: float, causal: bool, b: int, hq: int, block: int = 1024):
+    """Natural-log LSE of every query row of head (b, hq), one row block at a
+    time (same definition as head_forward, without holding all of S)."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    hk = hq // _group(Hq, Hkv)
+    Lq, Lk = q.shape[2], k.shape[2]
+    out = np.empty(Lq)
+    kh = k[b, hk]
+    for r0 in range(0, Lq, block):
+        rows = np.arange(r0, min(Lq, r0 + block))
+        S = scale * (q[b, hq, rows] @ kh.T)
+        mask = visible(Lq, Lk, causal)[rows] if causal else np.ones((len(rows), Lk), dtype=bool)
+        S = np.where(mask, S, -np.inf)
+        m = S.max(axis=1, keepdims=True)
+        l = np.where(mask, np.exp(S - m), 0.0).sum(axis=1, keepdims=True)
+        out[rows] = (m + np.log(l))[:, 0]
+    return out
+
+
+def backward_query_rows(q, k, v, o, do, scale: float, causal: bool, b: int, hq: int, rows):
+    """dQ for selected query rows of head (b, hq): each row needs only its own
+    softmax row, dP row and delta (dQ_i = scale * sum_j dS_ij K_j)."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    hk = hq // _group(Hq, Hkv)
+    Lq, Lk = q.shape[2], k.shape[2]
+    rows = np.asarray(rows)
+    S = scale * (q[b, hq, rows] @ k[b, hk].T)
+    mask = visible(Lq, Lk, causal)[rows]
+    S = np.where(mask, S, -np.inf)
+    m = S.max(axis=1, keepdims=True)
+    E = np.where(mask, np.exp(S - m), 0.0)
+    P = E / E.sum(axis=1, keepdims=True)
+    dP = do[b, hq, rows] @ v[b, hk].T
+    dlt = delta(o[b, hq, rows], do[b, hq, rows])[:, None]
+    dS = P * (dP - dlt)
+    return scale * (dS @ k[b, hk])
+
+
+def backward_key_rows(q, k, v, o, do, scale: float, causal: bool, b: int, hk: int, keys):
+    """dK and dV for selected key rows of KV head (b, hk): column j of P needs
+    the LSE of every query row (dK_j = scale * sum_{g,i} dS_ij Q_i,
+    dV_j = sum_{g,i} P_ij dO_i)."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    G = _group(Hq, Hkv)
+    Lq, Lk = q.shape[2], k.shape[2]
+    keys = np.asarray(keys)
+    dk = np.zeros((len(keys), k.shape[3]))
+    dv = np.zeros((len(keys), v.shape[3]))
+    mask = visible(Lq, Lk, causal)[:, keys]  # [Lq, n_keys]
+    for g in range(G):
+        hq = hk * G + g
+        lse = lse_all_rows(q, k, scale, causal, b, hq)
+        S = scale * (q[b, hq] @ k[b, hk, keys].T)  # [Lq, n_keys]
+        P = np.where(mask, np.exp(np.where(mask, S, 0.0) - lse[:, None]), 0.0)
+        dP = do[b, hq] @ v[b, hk, keys].T
+        dlt = delta(o[b, hq], do[b, hq])[:, None]
+        dS = P * (dP - dlt)
+        dk += scale * (dS.T @ q[b, hq])
+        dv += P.T @ do[b, hq]
+    return dk, dv
+
+
 def backward_kv_head(q, k, v, o, do, scale: float, causal: bool, b: int, hk: int):
     """dQ for the G query heads of KV head (b, hk), and that head's dK, dV."""
     Hq, Hkv = q.shape[1], k.shape[1]

@@ -1,0 +1,101 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/gbattn.h declares, and rejects bad arguments on the host
+before touching any device memory."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from bwd_flashattention_fwd_gb300 import build, gbattn
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gbattn.h")
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gbattn.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert set(names) == set(gbattn.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=4, Hkv=2, Lq=64, Lk=64, D=128, scale=0.1,
+        causal=1, dtype=1):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, ctypes.c_float(scale), causal, dtype, None)
+
+
+def bwd(lib, ptrs=None, B=1, Hq=4, Hkv=2, Lq=64, Lk=64, D=128, scale=0.1, causal=1, dtype=1):
+    ptrs = ptrs or [FAKE] * 10
+    return lib.attn_bwd(*ptrs, B, Hq, Hkv, Lq, Lk, D, ctypes.c_float(scale), causal, dtype, None)
+
+
+@pytest.mark.parametrize(
+    "kw,expected",
+    [
+        (dict(q=None), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(lse=None), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(q=FAKE + 8), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(B=0), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(Lq=0), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(Lk=-3, causal=0), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(Hkv=3), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(Hkv=0), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(Lq=65, Lk=64), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(scale=0.0), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(scale=-1.0), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(scale=math.nan), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(scale=math.inf), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(causal=2), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(dtype=5), gbattn.ATTN_ERR_INVALID_ARG),
+        (dict(D=80), gbattn.ATTN_ERR_UNSUPPORTED),
+        (dict(D=32), gbattn.ATTN_ERR_UNSUPPORTED),
+        (dict(D=512), gbattn.ATTN_ERR_UNSUPPORTED),
+    ],
+)
+def test_fwd_rejects_on_host(lib, kw, expected):
+    assert fwd(lib, **kw) == expected
+
+
+def test_bwd_rejects_on_host(lib):
+    for i in range(10):
+        ptrs = [FAKE] * 10
+        ptrs[i] = None
+        assert bwd(lib, ptrs) == gbattn.ATTN_ERR_INVALID_ARG
+    assert bwd(lib, Lq=100, Lk=99) == gbattn.ATTN_ERR_INVALID_ARG
+    assert bwd(lib, D=48) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert bwd(lib, Hq=5, Hkv=2) == gbattn.ATTN_ERR_INVALID_ARG
+
+
+def test_delta_rejects_on_host(lib):
+    assert lib.attn_bwd_delta(None, FAKE, FAKE, 1, 2, 3, 64, 1, None) == gbattn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_delta(FAKE, FAKE, FAKE + 4, 1, 2, 3, 64, 1, None) == gbattn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_delta(FAKE, FAKE, FAKE, 0, 2, 3, 64, 1, None) == gbattn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_delta(FAKE, FAKE, FAKE, 1, 2, 3, 100, 1, None) == gbattn.ATTN_ERR_UNSUPPORTED
+
+
+def test_status_strings(lib):
+    names = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+             4: "ATTN_ERR_TIMEOUT"}
+    for code, name in names.items():
+        assert gbattn.status_string(code) == name
+    assert gbattn.status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(gbattn.AttnError):
+        gbattn._check(gbattn.ATTN_ERR_UNSUPPORTED, "attn_fwd", True)

@@ -224,6 +224,16 @@ def pin_sampled_helpers(o):
     dqs, dkh, dvh = o.backward_kv_head(q, k, v, out, do, 0.5, True, 1, 1)
     assert np.allclose(dqs, dq[1, 2:4], atol=1e-13)
     assert np.allclose(dkh, dk[1, 1], atol=1e-13) and np.allclose(dvh, dv[1, 1], atol=1e-13)
+    for causal in (True, False):
+        out, lse2, lse_nat = o.forward(q, k, v, 0.5, causal)
+        dq, dk, dv = o.backward(q, k, v, out, do, 0.5, causal)
+        assert np.allclose(o.lse_all_rows(q, k, 0.5, causal, 1, 2, block=4), lse_nat[1, 2], atol=1e-13)
+        assert np.allclose(o.backward_query_rows(q, k, v, out, do, 0.5, causal, 0, 3, rows),
+                           dq[0, 3, rows], atol=1e-13)
+        keys = [0, 5, 10]
+        dks, dvs = o.backward_key_rows(q, k, v, out, do, 0.5, causal, 1, 0, keys)
+        assert np.allclose(dks, dk[1, 0, keys], atol=1e-13)
+        assert np.allclose(dvs, dv[1, 0, keys], atol=1e-13)
 
 
 PINS = [pin_rows_sum_to_one, pin_zero_query, pin_causal_diagonal, pin_delta_identity,
