@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark: causal GQA attention forward + delta + backward on GB300.
+
+One step = attn_fwd -> attn_bwd_delta -> attn_bwd (dK/dV kernel, then dQ
+kernel) over one batch of the workload, inputs resident in HBM.  The metric
+is credited TFLOP/s: 3.5 x the forward FLOPs (4*B*Hq*Lq*Lk*D, halved for
+causal) over the summed device time of the step's kernels.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload on its own GPU (weak scaling); the value is all ranks' work
+over the slowest rank's time.  `--impl reference` times the fp64 CPU oracle on
+the host cores instead, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from bwd_flashattention_fwd_gb300 import flops as F  # noqa: E402
+from bwd_flashattention_fwd_gb300 import replicas  # noqa: E402
+from bwd_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+METRIC = "fwd+bwd attention TFLOP/s, causal GQA L=8192 D=128 bf16; % of BF16 TC peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "qwen3_8b_gqa_l8192_d128"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "bwd_flashattention_fwd_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None).  Line format:
+    `<kernel> <workload> <bytes_per_launch> <source_hash>`."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    cur = kernel_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+                return float(parts[2]) if parts[3] == cur else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        for line in out.splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+                power.append(float(p[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def physical_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if local_rank < len(ids) and ids[local_rank].isdigit():
+        return int(ids[local_rank])
+    return local_rank
+
+
+def workload_config(w: Workload, extra: dict) -> dict:
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk, "D": w.D,
+           "causal": w.causal, "dtype": w.dtype, "input_std": w.std, "seed": w.seed}
+    cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+
+def oracle_sample_problem(w: Workload, rows: int):
+    """The last `rows` query rows of head (b=0, hq=0) with the keys they can
+    see: with bottom-right causal alignment that row block is itself a causal
+    problem (Lq' = rows, Lk' = visible keys), so the oracle runs on it as is."""
+    q, k, v, do = make_inputs(w, "cpu")
+    from bwd_flashattention_fwd_gb300.inputs import to_f64
+
+    r0 = w.Lq - rows
+    qs = to_f64(q[:1, :1, r0:])
+    dos = to_f64(do[:1, :1, r0:])
+    ks = to_f64(k[:1, :1])  # the last query row sees every key
+    vs = to_f64(v[:1, :1])
+    # credit 3.5 x 4*D FLOPs per visible (query, key) pair of the sample; over a
+    # whole causal problem that is the half-rectangle count of the metric
+    credited = 3.5 * 4.0 * w.D * F.visible_pairs(rows, w.Lk, w.causal)
+    return (qs, ks, vs, dos), credited
+
+
+def run_oracle_sample(arrays, w: Workload):
+    import oracle.attention as A
+
+    qs, ks, vs, dos = arrays
+    o, lse2, _ = A.forward(qs, ks, vs, w.scale, w.causal)
+    A.delta(o, dos)
+    A.backward(qs, ks, vs, o, dos, w.scale, w.causal)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w: Workload, rows: int) -> dict:
+    arrays, credited = oracle_sample_problem(w, rows)
+    run_oracle_sample(arrays, w)  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run_oracle_sample(arrays, w)
+        n += 1
+        if time.perf_counter() - t0 > 5.0:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": credited / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+delta+bwd on the last {rows} query rows of head (b=0,hq=0) and the "
+                      f"keys they see ({credited:.3g} credited FLOP per run, {n} runs, {dt:.3f} s each)"}
+
+
+def run_reference(args):
+    rank, local_rank, ws = replicas.world()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    rows = args.ref_rows
+    arrays, credited = oracle_sample_problem(w, rows)
+    for _ in range(args.warmup):
+        run_oracle_sample(arrays, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_sample(arrays, w)
+    dt = time.perf_counter() - t0
+    value = credited * args.steps / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, {"sample_rows": rows, "parallelism": "host cores"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"each step: fp64 oracle fwd+delta+bwd on the last {rows} query rows of "
+                                   f"head (b=0,hq=0) and the keys they see"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args):
+    from bwd_flashattention_fwd_gb300 import build, gbattn
+
+    rank, local_rank, ws = replicas.world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    replicas.init("nccl")
+    build.build()
+    gbattn.load_library()
+
+    w = WORKLOADS[args.workload]
+    q, k, v, do = make_inputs(w, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Lq), dtype=torch.float32, device=dev)
+    dlt = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sc, causal = w.scale, w.causal
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        gbattn.attn_fwd(q, k, v, o, lse, sc, causal, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        gbattn.attn_bwd_delta(o, do, dlt, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        gbattn.attn_bwd_dkv(q, k, v, do, lse, dlt, dk, dv, sc, causal, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        gbattn.attn_bwd_dq(q, k, v, do, lse, dlt, dq, sc, causal, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize(dev)
+    if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(physical_gpu_index(local_rank))
+    replicas.barrier(dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)  # L2 flush between steps, outside the step's events
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    replicas.barrier(dev)
+    clk = clocks.stop()
+    if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
+        raise RuntimeError("device-side wait timed out during the timed steps")
+
+    phase_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
+    per_phase = {n: [] for n in phase_names}
+    step_ms = []
+    for ev in events:
+        for j, n in enumerate(phase_names):
+            per_phase[n].append(ev[j].elapsed_time(ev[j + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[4]))
+    local_s = sum(step_ms) / 1e3
+    credited = F.credited_fwd_bwd(w.B, w.Hq, w.Lq, w.Lk, w.D, w.causal)
+    value_flops, _, max_s = replicas.aggregate_throughput(credited * args.steps, local_s, dev)
+    value = value_flops / 1e12
+    peaks = load_peaks()
+    avg = {n: statistics.mean(v) for n, v in per_phase.items()}
+
+    # roofline per kernel (algorithmic work / average launch time)
+    kernels = {}
+    for n in ("fwd", "bwd_dkv", "bwd_dq"):
+        fl = F.kernel_flops(n, w.B, w.Hq, w.Lq, w.Lk, w.D, w.causal)
+        ach = fl / (avg[n] * 1e-3) / 1e12
+        kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
+                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
+                      "avg_ms": avg[n], "algorithmic": fl, "traffic": recorded_traffic(n, w.name)}
+    db = F.delta_bytes(w.B, w.Hq, w.Lq, w.D)
+    ach = db / (avg["delta"] * 1e-3) / 1e9
+    kernels["delta"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "avg_ms": avg["delta"], "algorithmic": db,
+                        "traffic": recorded_traffic("delta", w.name)}
+    dominant = max(("fwd", "bwd_dkv", "bwd_dq"), key=lambda n: avg[n])
+    roof = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = dominant
+    roof["peak_kind"] = f"bf16 dense, sustained ({peaks['source']})"
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, dev, stream, gbattn, credited)
+
+    n_dkv = 1 if w.D <= 128 else 2
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(w, {
+            "l2": "flushed between steps (256 MiB write outside the step events); inputs 384 MiB",
+            "parallelism": "replicas" if ws > 1 else "single GPU",
+            "timing": "CUDA events on the launching stream, sum over steps",
+        }),
+        "pct_of_bf16_peak": 100.0 * value / ws / peaks["bf16_tflops"],
+        "pct_of_bf16_peak_sustained": 100.0 * value / ws / peaks["bf16_tflops_sustained"],
+        "peaks": peaks,
+        "phase_ms": avg,
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (1 + 1 + n_dkv + 1),
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    replicas.shutdown()
+    return 0
+
+
+def run_e2e(args, w, dev, stream, gbattn, credited):
+    """Same metric through attn_fwd / attn_bwd_delta / attn_bwd with pinned
+    host buffers: every step copies q, k, v, dO in and o, lse, dq, dk, dv out."""
+    qh, kh, vh, doh = (t.pin_memory() for t in make_inputs(w, "cpu"))
+    q, k, v, do = (torch.empty_like(t, device=dev) for t in (qh, kh, vh, doh))
+    o, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((w.B, w.Hq, w.Lq), dtype=torch.float32, device=dev)
+    dlt = torch.empty_like(lse)
+    outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, doh))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+    def e2e_step():
+        for dst, src in zip((q, k, v, do), (qh, kh, vh, doh)):
+            dst.copy_(src, non_blocking=True)
+        gbattn.attn_fwd(q, k, v, o, lse, w.scale, w.causal, stream)
+        gbattn.attn_bwd_delta(o, do, dlt, stream)
+        gbattn.attn_bwd(q, k, v, o, do, lse, dlt, dq, dk, dv, w.scale, w.causal, stream)
+        for dst, src in zip(outs_h, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    replicas.barrier(dev)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    local_s = e0.elapsed_time(e1) / 1e3
+    value, _, _ = replicas.aggregate_throughput(credited * n, local_s, dev)
+    return {"value": value / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "ms_per_step": local_s * 1e3 / n}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=128, help="query rows per reference-arm step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -112,6 +112,22 @@ int dispatch_bwd(const AttnArgs& a) {
     default: return launch_bwd_d256(a);
   }
 }
+int dispatch_bwd_dq(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_bwd_dq_d64(a);
+    case 96: return launch_bwd_dq_d96(a);
+    case 128: return launch_bwd_dq_d128(a);
+    default: return launch_bwd_dq_d256(a);
+  }
+}
+int dispatch_bwd_dkv(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_bwd_dkv_d64(a);
+    case 96: return launch_bwd_dkv_d96(a);
+    case 128: return launch_bwd_dkv_d128(a);
+    default: return launch_bwd_dkv_d256(a);
+  }
+}
 int dispatch_delta(const AttnArgs& a) {
   switch (a.D) {
     case 64: return launch_delta_d64(a);
@@ -181,6 +197,45 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();
   return finish(dispatch_bwd(a));
+}
+
+// The two halves of attn_bwd, for callers that run them on separate streams.
+namespace {
+attn_status_t bwd_part(bool dq_part, const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
+  if (!q || !k || !v || !dO || !lse || !delta) return ATTN_ERR_INVALID_ARG;
+  if (dq_part ? !dq : (!dk || !dv)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO)) return ATTN_ERR_INVALID_ARG;
+  if (dq_part ? !aligned16(dq) : (!aligned16(dk) || !aligned16(dv))) return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.dO = dO, a.lse = lse, a.delta = delta;
+  a.dq = dq, a.dk = dk, a.dv = dv;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dq_part ? dispatch_bwd_dq(a) : dispatch_bwd_dkv(a));
+}
+}  // namespace
+
+extern "C" attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                     const float* delta, void* dq, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                                     float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
+  return bwd_part(true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype,
+                  stream);
+}
+
+extern "C" attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO,
+                                      const float* lse, const float* delta, void* dk, void* dv, int B, int Hq,
+                                      int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                      cudaStream_t stream) {
+  return bwd_part(false, q, k, v, dO, lse, delta, nullptr, dk, dv, B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype,
+                  stream);
 }
 
 extern "C" attn_status_t attn_last_device_status(cudaStream_t stream) {

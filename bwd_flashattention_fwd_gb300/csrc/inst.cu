@@ -125,16 +125,19 @@ int dq_impl(const AttnArgs& a) {
 }
 
 template <bool BF16, bool CAUSAL>
-int bwd_impl(const AttnArgs& a) {
-  int r;
+int dkv_all(const AttnArgs& a) {
   if constexpr (kD <= 128) {
-    r = dkv_impl<BF16, CAUSAL, kDkvBoth>(a);
+    return dkv_impl<BF16, CAUSAL, kDkvBoth>(a);
   } else {
-    r = dkv_impl<BF16, CAUSAL, kDkvDvOnly>(a);
-    if (r == kLaunchOk) r = dkv_impl<BF16, CAUSAL, kDkvDkOnly>(a);
+    const int r = dkv_impl<BF16, CAUSAL, kDkvDvOnly>(a);
+    return r == kLaunchOk ? dkv_impl<BF16, CAUSAL, kDkvDkOnly>(a) : r;
   }
-  if (r != kLaunchOk) return r;
-  return dq_impl<BF16, CAUSAL>(a);
+}
+
+template <bool BF16, bool CAUSAL>
+int bwd_impl(const AttnArgs& a) {
+  const int r = dkv_all<BF16, CAUSAL>(a);
+  return r == kLaunchOk ? dq_impl<BF16, CAUSAL>(a) : r;
 }
 
 template <bool BF16>
@@ -162,6 +165,16 @@ int GBATTN_CAT(launch_fwd_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
 int GBATTN_CAT(launch_bwd_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
   if (a.bf16) return a.causal ? bwd_impl<true, true>(a) : bwd_impl<true, false>(a);
   return a.causal ? bwd_impl<false, true>(a) : bwd_impl<false, false>(a);
+}
+
+int GBATTN_CAT(launch_bwd_dq_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? dq_impl<true, true>(a) : dq_impl<true, false>(a);
+  return a.causal ? dq_impl<false, true>(a) : dq_impl<false, false>(a);
+}
+
+int GBATTN_CAT(launch_bwd_dkv_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? dkv_all<true, true>(a) : dkv_all<true, false>(a);
+  return a.causal ? dkv_all<false, true>(a) : dkv_all<false, false>(a);
 }
 
 int GBATTN_CAT(launch_delta_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {

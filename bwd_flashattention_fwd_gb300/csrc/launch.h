@@ -46,6 +46,8 @@ enum LaunchResult : int { kLaunchOk = 0, kLaunchBadMap = 1, kLaunchCudaError = 2
 #define GBATTN_DECLARE_LAUNCHERS(DIM)                \
   int launch_fwd_d##DIM(const AttnArgs& a);          \
   int launch_bwd_d##DIM(const AttnArgs& a);          \
+  int launch_bwd_dq_d##DIM(const AttnArgs& a);       \
+  int launch_bwd_dkv_d##DIM(const AttnArgs& a);      \
   int launch_delta_d##DIM(const AttnArgs& a);
 
 GBATTN_DECLARE_LAUNCHERS(64)

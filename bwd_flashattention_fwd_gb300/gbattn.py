@@ -24,7 +24,8 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_last_device_status", "attn_status_string")
+EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_last_device_status",
+            "attn_status_string")
 
 _lib = None
 
@@ -52,6 +53,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd_delta.restype = ci
     lib.attn_bwd.argtypes = [vp] * 10 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.attn_bwd.restype = ci
+    lib.attn_bwd_dq.argtypes = [vp] * 7 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd_dq.restype = ci
+    lib.attn_bwd_dkv.argtypes = [vp] * 8 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd_dkv.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -114,6 +119,27 @@ def attn_bwd(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bool,
                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D, float(scale),
                                  int(bool(causal)), _dtype_code(q), _stream_handle(stream))
     return _check(st, "attn_bwd", check)
+
+
+def attn_bwd_dq(q, k, v, dO, lse, delta, dq, scale: float, causal: bool, stream=None, check: bool = True) -> int:
+    """dQ only (the query-row-owning half of attn_bwd)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(delta), _ptr(dq), B, Hq,
+                                    Hkv, Lq, Lk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                                    _stream_handle(stream))
+    return _check(st, "attn_bwd_dq", check)
+
+
+def attn_bwd_dkv(q, k, v, dO, lse, delta, dk, dv, scale: float, causal: bool, stream=None,
+                 check: bool = True) -> int:
+    """dK and dV only (the key-row-owning half of attn_bwd)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_bwd_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(delta), _ptr(dk),
+                                     _ptr(dv), B, Hq, Hkv, Lq, Lk, D, float(scale), int(bool(causal)),
+                                     _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_bwd_dkv", check)
 
 
 def attn_last_device_status(stream=None) -> int:

@@ -95,6 +95,22 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * The two halves of attn_bwd, for callers that want to run them on different
+ * streams (they share only read-only inputs, so they may run concurrently; the
+ * pages' dQ and dK/dV kernels are encoded to run concurrently, "feat(attention):
+ * complete Flash Attention VJP implementation", section "Two-Kernel Design").
+ * attn_bwd(...) is exactly attn_bwd_dkv(...) followed by attn_bwd_dq(...) on
+ * one stream.  Arguments as for attn_bwd; attn_bwd_dq writes only dq,
+ * attn_bwd_dkv writes only dk and dv.
+ */
+attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                          const float* delta, void* dq, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                          float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                           const float* delta, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk,
+                           int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device status word of the
  * current device: ATTN_ERR_TIMEOUT if a bounded device-side wait ran out in a
  * kernel since the last call, ATTN_ERR_CUDA if the stream reported an error,
