@@ -238,6 +238,88 @@ extern "C" attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* 
                   stream);
 }
 
+// ---------------------------------------------------------------------------
+// attn_bwd_noalloc: the backward for callers that cannot allocate device
+// memory.  Its scratch (the device status word and the delta vector) lives in
+// the static array below instead of in memory obtained from cudaMalloc.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr long long kNoAllocMaxRows = 1LL << 20;  // B * Hq * Lq, i.e. 4 MiB of delta
+constexpr size_t kNoAllocHeaderBytes = 256;        // status word, padded to the alignment
+constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + sizeof(float) * static_cast<size_t>(kNoAllocMaxRows);
+
+// Loaded with the library on every GPU that uses it, and kept until exit.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+EncodeTiledFn g_noalloc_encode = nullptr;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+int g_noalloc_sms[kMaxDevices] = {};
+
+// Once per device, with that device current: the device address of the
+// scratch array (host code only sees a stand-in for the symbol), the SM count
+// and the tensor-map encoder.  None of these calls allocates device memory.
+attn_status_t noalloc_setup(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return ATTN_ERR_CUDA;
+    g_noalloc_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_noalloc_sms[dev] = sms;
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *dev_out = dev;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                                          int Hq, int Hkv, int Lq, int Lk, int D, float scale, int causal,
+                                          attn_dtype_t dtype, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  if (static_cast<long long>(B) * Hq * Lq > kNoAllocMaxRows) return ATTN_ERR_UNSUPPORTED;
+  int dev = 0;
+  const attn_status_t ss = noalloc_setup(&dev);
+  if (ss != ATTN_OK) return ss;
+  unsigned char* scratch = g_noalloc_ptr[dev];
+  int* status = reinterpret_cast<int*>(scratch);
+  float* dlt = reinterpret_cast<float*>(scratch + kNoAllocHeaderBytes);
+  // The status word must start each call at zero; delta is fully rewritten.
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  AttnArgs a;
+  a.encode = g_noalloc_encode;
+  a.num_sms = g_noalloc_sms[dev];
+  a.status = status;
+  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = dlt, a.delta_out = dlt;
+  a.dq = dq, a.dk = dk, a.dv = dv;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  const int r = dispatch_delta(a);
+  if (r != kLaunchOk) return finish(r);
+  return finish(dispatch_bwd(a));
+}
+
 extern "C" attn_status_t attn_last_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
   int dev = 0;

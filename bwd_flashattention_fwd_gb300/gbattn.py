@@ -24,8 +24,8 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_last_device_status",
-            "attn_status_string")
+EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc",
+            "attn_last_device_status", "attn_status_string")
 
 _lib = None
 
@@ -57,6 +57,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd_dq.restype = ci
     lib.attn_bwd_dkv.argtypes = [vp] * 8 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.attn_bwd_dkv.restype = ci
+    lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd_noalloc.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -140,6 +142,18 @@ def attn_bwd_dkv(q, k, v, dO, lse, delta, dk, dv, scale: float, causal: bool, st
                                      _ptr(dv), B, Hq, Hkv, Lq, Lk, D, float(scale), int(bool(causal)),
                                      _dtype_code(q), _stream_handle(stream))
     return _check(st, "attn_bwd_dkv", check)
+
+
+def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, scale: float, causal: bool, stream=None,
+                     check: bool = True) -> int:
+    """attn_bwd for callers that cannot allocate device memory: delta and the
+    status word live in the library's fixed scratch array (B*Hq*Lq <= 2**20)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D, float(scale),
+                                         int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_bwd_noalloc", check)
 
 
 def attn_last_device_status(stream=None) -> int:

@@ -111,6 +111,42 @@ attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const vo
                            int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * attn_bwd for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is an entry point of this library only.)
+ *
+ * Who needs it: code whose device memory is fully managed by someone else --
+ * a framework whose caching allocator already holds the GPU's memory, a
+ * plugin whose execution callback must not allocate, a service that reserves
+ * all memory at start-up and forbids allocation afterwards.  The other entry
+ * points allocate one small device status word with cudaMalloc on their first
+ * call on a device, and attn_bwd needs the caller to allocate delta; this one
+ * needs neither.
+ *
+ * What it does: delta = rowsum(dO * O) (as attn_bwd_delta), then the dK/dV
+ * and dQ kernels (as attn_bwd), with delta and the device status word kept in
+ * a fixed scratch array that is part of the library image: 256 bytes of
+ * header plus room for B*Hq*Lq <= 1,048,576 delta values (4 MiB), held on
+ * every GPU that loads the library until the process exits.  The call makes
+ * no cudaMalloc, cudaFree or other allocating call.
+ *   Arguments as for attn_bwd, without delta.  Larger problems (B*Hq*Lq above
+ *   1,048,576) are rejected with ATTN_ERR_UNSUPPORTED before anything runs.
+ *   Set-up: the first call on each device looks up the scratch array's device
+ *   address (with that device current); make that first call before any
+ *   stream capture.
+ *   Sharing: every call on a device uses the same scratch array, and the
+ *   array keeps the last call's contents (the status word is cleared at the
+ *   start of each call; delta is fully rewritten).  Calls whose work overlaps
+ *   on the GPU -- on different streams without ordering between them -- race
+ *   on the scratch and give wrong results; order them on one stream.
+ *   Errors: argument and launch errors as for attn_bwd.  A bounded device wait
+ *   that runs out is recorded in the scratch's status word, which
+ *   attn_last_device_status does not read.
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq,
+                               int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device status word of the
  * current device: ATTN_ERR_TIMEOUT if a bounded device-side wait ran out in a
  * kernel since the last call, ATTN_ERR_CUDA if the stream reported an error,
