@@ -59,9 +59,24 @@ def load_peaks() -> dict:
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_source_hash() -> str:
+KERNEL_FILES = {
+    "fwd": "fwd_kernel.cuh",
+    "delta": "delta_kernel.cuh",
+    "bwd_dkv": "bwd_dkv_kernel.cuh",
+    "bwd_dq": "bwd_dq_kernel.cuh",
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources that define a kernel (its own file, the shared
+    device headers and the launch code), or of all sources."""
+    csrc = os.path.join(ROOT, "bwd_flashattention_fwd_gb300", "csrc")
+    if kernel is None:
+        files = sorted(glob.glob(os.path.join(csrc, "*")))
+    else:
+        files = [os.path.join(csrc, n) for n in (KERNEL_FILES[kernel], "kernel_common.cuh", "ptx.cuh", "inst.cu")]
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "bwd_flashattention_fwd_gb300", "csrc", "*"))):
+    for p in files:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode() + f.read())
     return h.hexdigest()[:16]
@@ -73,7 +88,7 @@ def recorded_traffic(kernel: str, workload: str):
     `<kernel> <workload> <bytes_per_launch> <source_hash>`."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(kernel)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
