@@ -9,14 +9,23 @@
 //   dV += P^T dO, dK += dS^T Q                        (tcgen05, A from TMEM)
 // and finally dK is scaled by `scale`.
 //
+// Pipelining: S^T and dP^T are double-buffered in tensor memory, so the MMAs
+// of query tile i+1 run while the row threads turn tile i into P^T and dS^T.
+// P^T and dS^T (16-bit pairs) are written back over the fp32 S^T / dP^T
+// columns the same warpgroup has just read, and the dV / dK MMAs read them
+// from there.  The next MMA that writes those columns is issued after the
+// MMAs that read them, by the same thread, and tcgen05 MMAs of one CTA run
+// in issue order.
+//
 // MODE selects which outputs one CTA accumulates.  kDkvBoth keeps dK and dV
 // in tensor memory together (D <= 128).  At D = 256 the two accumulators
 // alone fill the 512 TMEM columns, so dV (kDkvDvOnly: S^T, P^T, dV) and dK
 // (kDkvDkOnly: S^T, dP^T, dS^T, dK) are produced by separate CTAs.
 //
-// Warp roles (192 threads): warps 0-3 key-row threads, warp 4 producer (TMA
-// for Q/dO tiles, plain loads for the per-query lse/delta values), warp 5 MMA
-// issuer and TMEM owner.
+// Warp roles (320 threads): warps 0-7 row threads -- warp w owns TMEM lanes
+// 32*(w%4)..+31 (key rows) and query columns 32*(w/4)..+31 of each tile;
+// warp 8 producer (TMA for Q/dO tiles, plain loads for the per-query
+// lse/delta values); warp 9 MMA issuer and TMEM owner.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -42,28 +51,30 @@ struct DkvGeom {
   static constexpr int ACC_W = (D <= 128) ? 128 : 256;
   static constexpr int DK_COL = 0;
   static constexpr int DV_COL = (MODE == kDkvBoth) ? ACC_W : 0;
-  static constexpr int ST_COL = (MODE == kDkvBoth) ? 2 * ACC_W : ACC_W;
-  static constexpr int DPT_COL = ST_COL + BQ;                      // unused in DvOnly
-  static constexpr int PT_COL = (MODE == kDkvDvOnly) ? ST_COL + BQ : DPT_COL + BQ;
-  static constexpr int DST_COL = (MODE == kDkvDkOnly) ? DPT_COL + BQ : PT_COL + BQ / 2;
+  static constexpr int ST_COL = (MODE == kDkvBoth) ? 2 * ACC_W : ACC_W;  // two buffers of BQ columns
+  static constexpr int DPT_COL = ST_COL + 2 * BQ;                        // two buffers (not in DvOnly)
   static constexpr int TMEM_COLS = 512;
-  static constexpr int NUM_THREADS = 192;
+  static constexpr int NUM_COMPUTE_WARPS = 8;
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
+  static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
+  static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
   static_assert(STAGES >= 1, "shared memory budget");
   static_assert(MODE != kDkvBoth || D <= 128, "dK and dV together need D <= 128");
-  static_assert(DST_COL + BQ / 2 <= TMEM_COLS && PT_COL + BQ / 2 <= TMEM_COLS, "tensor memory budget");
+  static_assert((NEED_DS ? DPT_COL + 2 * BQ : ST_COL + 2 * BQ) <= TMEM_COLS, "tensor memory budget");
 };
 
 template <int D, bool BF16, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                         const BwdParams p) {
   using Gm = DkvGeom<D, MODE>;
   using E = Elem<BF16>;
   constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
+  constexpr int NCT = 32 * Gm::NUM_COMPUTE_WARPS;  // row threads
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_kv, bar_stfull[ST], bar_stempty[ST], bar_sfull, bar_pready, bar_accdone;
+  __shared__ uint64_t bar_kv, bar_stfull[ST], bar_stempty[ST], bar_sfull[2], bar_pready[2], bar_accdone;
   __shared__ float lse_s[ST][BQ], dlt_s[ST][BQ];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -91,12 +102,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(smem_u32(&bar_stfull[s]), 33);  // TMA expect_tx arrive + 32 producer lanes
       mbar_init(smem_u32(&bar_stempty[s]), 1);
     }
-    mbar_init(smem_u32(&bar_sfull), 1);
-    mbar_init(smem_u32(&bar_pready), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_sfull[i]), 1);
+      mbar_init(smem_u32(&bar_pready[i]), NCT);
+    }
     mbar_init(smem_u32(&bar_accdone), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == Gm::MMA_WARP) {
     tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
     tmem_relinquish();
   }
@@ -105,32 +118,31 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == Gm::PRODUCER_WARP) {
     // ---------------- producer (whole warp) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmdO);
       if (Gm::NEED_V) tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(smem_u32(&bar_kv), Gm::RES_BYTES);
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d(sK + c * BK * 128, &tmK, smem_u32(&bar_kv), c * 64, k0, bhk);
-        if (Gm::NEED_V) tma_load_3d(sV + c * BK * 128, &tmV, smem_u32(&bar_kv), c * 64, k0, bhk);
-      }
+    }
+    __syncwarp();
+    mbar_arrive_expect_tx_w(smem_u32(&bar_kv), Gm::RES_BYTES);
+    for (int c = 0; c < NCH; ++c) {
+      tma_load_3d_w(sK + c * BK * 128, &tmK, smem_u32(&bar_kv), c * 64, k0, bhk);
+      if (Gm::NEED_V) tma_load_3d_w(sV + c * BK * 128, &tmV, smem_u32(&bar_kv), c * 64, k0, bhk);
     }
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % ST, u = it / ST;
       if (u > 0) mbar_wait(smem_u32(&bar_stempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 21);
+      __syncwarp();
       const int gi = it / nq;
       const int q0 = (qt_start + (it - gi * nq)) * BQ;
       const int zq = b * p.Hq + hk * p.G + gi;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
-        for (int c = 0; c < NCH; ++c) {
-          tma_load_3d(sQ0 + s * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
-          tma_load_3d(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0,
-                      zq);
-        }
+      mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
+      for (int c = 0; c < NCH; ++c) {
+        tma_load_3d_w(sQ0 + s * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
+        tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
       }
 #pragma unroll
       for (int t = 0; t < BQ / 32; ++t) {
@@ -144,109 +156,125 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
       mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
-  } else if (warp == 5) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
-      constexpr uint32_t IDESC_ACC = make_idesc_f16(128, D, BF16, false, true);
-      mbar_wait(smem_u32(&bar_kv), 0, g, kDevTimeoutBase + 22);
+  } else if (warp == Gm::MMA_WARP) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
+    constexpr uint32_t IDESC_ACC = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dK = make_sdesc_sw128(sK, 16, 1024);             // K tile, K-major
+    const uint64_t dV = make_sdesc_sw128(sV, 16, 1024);             // V tile, K-major
+    const uint64_t dQk = make_sdesc_sw128(sQ0, 16, 1024);           // Q stage 0, K-major
+    const uint64_t dOk = make_sdesc_sw128(sdO0, 16, 1024);          // dO stage 0, K-major
+    const uint64_t dQm = make_sdesc_sw128(sQ0, BQ * 128, 1024);     // Q stage 0, MN-major
+    const uint64_t dOm = make_sdesc_sw128(sdO0, BQ * 128, 1024);    // dO stage 0, MN-major
+    mbar_wait(smem_u32(&bar_kv), 0, g, kDevTimeoutBase + 22);
+    __syncwarp();
+    tc_fence_after_sync();
+    // S^T (and dP^T) of iteration `it` into buffer it & 1
+    auto issue_s = [&](int it) {
+      const int s = it % ST, buf = it & 1;
+      mbar_wait(smem_u32(&bar_stfull[s]), (it / ST) & 1, g, kDevTimeoutBase + 23);
+      __syncwarp();
       tc_fence_after_sync();
-      for (int it = 0; it < n_iter; ++it) {
-        const int s = it % ST;
-        const uint32_t qb = sQ0 + s * Gm::Q_BYTES, ob = sdO0 + s * Gm::Q_BYTES;
-        mbar_wait(smem_u32(&bar_stfull[s]), (it / ST) & 1, g, kDevTimeoutBase + 23);
-        tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          mma_ss(tmem + Gm::ST_COL, make_sdesc_sw128(sK + ko, 16, 1024), make_sdesc_sw128(qb + qo, 16, 1024),
-                 IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        if (Gm::NEED_DS) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + Gm::DPT_COL, make_sdesc_sw128(sV + ko, 16, 1024),
-                   make_sdesc_sw128(ob + qo, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-          }
-        }
-        mma_commit(smem_u32(&bar_sfull));
-        mbar_wait(smem_u32(&bar_pready), it & 1, g, kDevTimeoutBase + 24);
-        tc_fence_after_sync();
-        if (Gm::NEED_DV) {
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tmem + Gm::DV_COL, tmem + Gm::PT_COL + kk * 8,
-                   make_sdesc_sw128(ob + kk * 2048, BQ * 128, 1024), IDESC_ACC, (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (Gm::NEED_DS) {
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tmem + Gm::DK_COL, tmem + Gm::DST_COL + kk * 8,
-                   make_sdesc_sw128(qb + kk * 2048, BQ * 128, 1024), IDESC_ACC, (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&bar_stempty[s]));
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        const uint32_t qo = s * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::ST_COL + buf * BQ, sdesc_add(dK, ko), sdesc_add(dQk, qo), IDESC_S, kk > 0 ? 1u : 0u);
+        if (Gm::NEED_DS)
+          mma_ss_w(tmem + Gm::DPT_COL + buf * BQ, sdesc_add(dV, ko), sdesc_add(dOk, qo), IDESC_S,
+                   kk > 0 ? 1u : 0u);
       }
-      mma_commit(smem_u32(&bar_accdone));
-      mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+      mma_commit_w(smem_u32(&bar_sfull[buf]));
+    };
+    // With a single Q/dO stage the next tile can only be loaded once this
+    // tile's dV/dK MMAs are done, so the next S^T is issued after them.
+    constexpr bool kAhead = ST >= 2;
+    if (n_iter > 0) issue_s(0);
+    for (int it = 0; it < n_iter; ++it) {
+      if (kAhead && it + 1 < n_iter) issue_s(it + 1);
+      const int s = it % ST, buf = it & 1;
+      mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 24);
+      __syncwarp();
+      tc_fence_after_sync();
+      // A operand: 16 queries per K step; queries 32w'..32w'+31 of warpgroup
+      // w' sit as pairs in columns 32w'..32w'+15 of the buffer.
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk) {
+        const uint32_t acol = buf * BQ + (kk >> 1) * 32 + (kk & 1) * 8;
+        const uint32_t bo = s * Gm::Q_BYTES + kk * 2048;
+        if (Gm::NEED_DV)
+          mma_ts_w(tmem + Gm::DV_COL, tmem + Gm::ST_COL + acol, sdesc_add(dOm, bo), IDESC_ACC,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        if (Gm::NEED_DS)
+          mma_ts_w(tmem + Gm::DK_COL, tmem + Gm::DPT_COL + acol, sdesc_add(dQm, bo), IDESC_ACC,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_stempty[s]));
+      if (!kAhead && it + 1 < n_iter) issue_s(it + 1);
     }
+    mma_commit_w(smem_u32(&bar_accdone));
+    mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+    __syncwarp();
   } else {
     // ---------------- key-row threads ----------------
-    const int r = warp * 32 + lane;
+    const int quad = warp & 3;        // TMEM lane quadrant
+    const int half = warp >> 2;       // query columns 32*half .. +31
+    const int r = quad * 32 + lane;
     const int kj = k0 + r;
-    const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
     const int qmin = kj - p.off;  // causal: queries below this index cannot see key kj
     for (int it = 0; it < n_iter; ++it) {
-      const int s = it % ST;
+      const int s = it % ST, buf = it & 1;
       const int gi = it / nq;
       const int q0 = (qt_start + (it - gi * nq)) * BQ;
       mbar_wait(smem_u32(&bar_stfull[s]), (it / ST) & 1, g, kDevTimeoutBase + 25);
-      mbar_wait(smem_u32(&bar_sfull), it & 1, g, kDevTimeoutBase + 26);
+      mbar_wait(smem_u32(&bar_sfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 26);
       __syncwarp();
       tc_fence_after_sync();
       const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
+      const uint32_t scol = tmem + lrow + Gm::ST_COL + buf * BQ + half * 32;
+      const uint32_t dcol = tmem + lrow + Gm::DPT_COL + buf * BQ + half * 32;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(scol, sr);
+      if (Gm::NEED_DS) tmem_ld32(dcol, dr);
+      tmem_ld_wait(sr);
+      if (Gm::NEED_DS) reg_fence(dr);
+      const float* lse_row = &lse_s[s][half * 32];
+      const float* dlt_row = &dlt_s[s][half * 32];
+      const int qc0 = q0 + half * 32;
+      uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int c = 0; c < BQ / 32; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lrow + Gm::ST_COL + c * 32, sr);
-        if (Gm::NEED_DS) tmem_ld32(tmem + lrow + Gm::DPT_COL + c * 32, dr);
-        tmem_ld_wait(sr);
-        if (Gm::NEED_DS) reg_fence(dr);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c0 = c * 32 + 2 * i;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_s[s][c0]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_s[s][c0 + 1]));
-          if (need_mask) {
-            if (q0 + c0 < qmin) p0 = 0.f;
-            if (q0 + c0 + 1 < qmin) p1 = 0.f;
-          }
-          pk[i] = E::pack(p0, p1);
-          if (Gm::NEED_DS) {
-            const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_s[s][c0]);
-            const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_s[s][c0 + 1]);
-            dk[i] = E::pack(ds0, ds1);
-          }
+      for (int i = 0; i < 16; ++i) {
+        const int c0 = 2 * i;
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c0]), sl2, -lse_row[c0]));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c0 + 1]), sl2, -lse_row[c0 + 1]));
+        if (need_mask) {
+          if (qc0 + c0 < qmin) p0 = 0.f;
+          if (qc0 + c0 + 1 < qmin) p1 = 0.f;
         }
-        if (Gm::NEED_DV) tmem_st16(tmem + lrow + Gm::PT_COL + c * 16, pk);
-        if (Gm::NEED_DS) tmem_st16(tmem + lrow + Gm::DST_COL + c * 16, dk);
+        pk[i] = E::pack(p0, p1);
+        if (Gm::NEED_DS) {
+          const float ds0 = p0 * (__uint_as_float(dr[c0]) - dlt_row[c0]);
+          const float ds1 = p1 * (__uint_as_float(dr[c0 + 1]) - dlt_row[c0 + 1]);
+          dk[i] = E::pack(ds0, ds1);
+        }
       }
+      if (Gm::NEED_DV) tmem_st16(scol, pk);
+      if (Gm::NEED_DS) tmem_st16(dcol, dk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_pready));
+      mbar_arrive(smem_u32(&bar_pready[buf]));
     }
     mbar_wait(smem_u32(&bar_accdone), 0, g, kDevTimeoutBase + 27);
     __syncwarp();
     tc_fence_after_sync();
+    // epilogue: warpgroup `half` writes output columns [half*D/2, (half+1)*D/2)
     const size_t row = static_cast<size_t>(bhk) * p.Lk + kj;
     if (Gm::NEED_DS) {
       typename E::T* dst = reinterpret_cast<typename E::T*>(p.dk) + row * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half; c < D / 32; c += 2) {
         uint32_t rr[32];
         tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
         tmem_ld_wait(rr);
@@ -256,7 +284,7 @@ __global__ void __launch_bounds__(192, 1)
     if (Gm::NEED_DV) {
       typename E::T* dst = reinterpret_cast<typename E::T*>(p.dv) + row * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half; c < D / 32; c += 2) {
         uint32_t rr[32];
         tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
         tmem_ld_wait(rr);
@@ -267,7 +295,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == Gm::MMA_WARP) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
   }

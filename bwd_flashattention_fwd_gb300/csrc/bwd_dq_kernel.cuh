@@ -9,8 +9,17 @@
 // and finally dQ is scaled by `scale` (section "Background": dS carries the
 // softmax scale, dQ = dS K).  No other CTA writes these dQ rows, so no atomics.
 //
-// Warp roles (192 threads): warps 0-3 row threads (TMEM lane = row), warp 4
-// TMA producer, warp 5 MMA issuer and TMEM owner.
+// Pipelining: S and dP are double-buffered in tensor memory (key tiles of
+// BK = 64), so the MMAs of key tile j+1 run while the row threads turn tile j
+// into dS.  dS (16-bit pairs) is written back over the fp32 S columns the same
+// warpgroup has just read; the dQ MMA reads it from there, and the next MMA
+// writing those columns is issued after it by the same thread (tcgen05 MMAs of
+// one CTA run in issue order).  K and V tiles arrive in separate TMA rings:
+// V is released as soon as dP has used it, K only after dQ += dS K.
+//
+// Warp roles (320 threads): warps 0-7 row threads -- warp w owns TMEM lanes
+// 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each tile;
+// warp 8 TMA producer; warp 9 MMA issuer and TMEM owner.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -20,36 +29,42 @@ namespace gbattn {
 template <int D>
 struct DqGeom {
   static constexpr int BQ = 128;
-  static constexpr int BK = (D == 256) ? 64 : 128;
+  static constexpr int BK = 64;
   static constexpr int NCH = n_chunks(D);
   static constexpr int Q_BYTES = NCH * BQ * 128;
   static constexpr int KV_BYTES = NCH * BK * 128;
-  static constexpr int STAGES_FIT =
-      (kMaxDynSmem - kSmemReserve - 1024 - 2 * Q_BYTES) / (2 * KV_BYTES);
-  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + STAGES * 2 * KV_BYTES;
+  // static shared memory here is only the barriers (< 512 B)
+  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * Q_BYTES;
+  // K stays in flight longer (until dQ += dS K), so it gets the extra stage.
+  static constexpr int KSTAGES = (AVAIL / KV_BYTES) >= 8 ? 4 : (AVAIL / KV_BYTES + 1) / 2;
+  static constexpr int VSTAGES = (AVAIL / KV_BYTES - KSTAGES) > 4 ? 4 : (AVAIL / KV_BYTES - KSTAGES);
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES;
   static constexpr int DQ_COL = 0;
-  static constexpr int S_COL = (D <= 128) ? 128 : 256;
-  static constexpr int DP_COL = S_COL + BK;
-  static constexpr int DS_COL = DP_COL + BK;
+  static constexpr int S_COL = (D <= 128) ? 128 : 256;  // two buffers of BK columns
+  static constexpr int DP_COL = S_COL + 2 * BK;         // two buffers of BK columns
   static constexpr int TMEM_COLS = 512;
-  static constexpr int NUM_THREADS = 192;
-  static_assert(STAGES >= 1, "shared memory budget");
-  static_assert(DS_COL + BK / 2 <= TMEM_COLS, "tensor memory budget");
+  static constexpr int NUM_COMPUTE_WARPS = 8;
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
+  static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
+  static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
+  // S of tile j+1 is issued before dQ of tile j releases K_j: K needs 2 stages.
+  static_assert(KSTAGES >= 2 && VSTAGES >= 1, "shared memory budget");
+  static_assert(DP_COL + 2 * BK <= TMEM_COLS, "tensor memory budget");
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const BwdParams p) {
   using Gm = DqGeom<D>;
   using E = Elem<BF16>;
-  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
+  constexpr int NCT = 32 * Gm::NUM_COMPUTE_WARPS;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kfull[ST], bar_vfull[ST], bar_kvempty[ST], bar_sfull, bar_dsready,
-      bar_dqdone;
+  __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
+      bar_dsready[2], bar_dqdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -58,7 +73,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = sbase;
   const uint32_t sdO = sQ + Gm::Q_BYTES;
   const uint32_t sK0 = sdO + Gm::Q_BYTES;
-  const uint32_t sV0 = sK0 + ST * Gm::KV_BYTES;
+  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
 
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
@@ -73,17 +88,22 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(smem_u32(&bar_kfull[s]), 1);
-      mbar_init(smem_u32(&bar_vfull[s]), 1);
-      mbar_init(smem_u32(&bar_kvempty[s]), 1);
+      mbar_init(smem_u32(&bar_kempty[s]), 1);
     }
-    mbar_init(smem_u32(&bar_sfull), 1);
-    mbar_init(smem_u32(&bar_dsready), 128);
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(smem_u32(&bar_vfull[s]), 1);
+      mbar_init(smem_u32(&bar_vempty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_sfull[i]), 1);
+      mbar_init(smem_u32(&bar_dsready[i]), NCT);
+    }
     mbar_init(smem_u32(&bar_dqdone), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == Gm::MMA_WARP) {
     tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
     tmem_relinquish();
   }
@@ -92,121 +112,143 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == Gm::PRODUCER_WARP) {
+    // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      const int zkv = b * p.Hkv + hk;
-      mbar_arrive_expect_tx(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
-        tma_load_3d(sdO + c * BQ * 128, &tmdO, smem_u32(&bar_q), c * 64, q0, bh);
-      }
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % ST, u = j / ST;
-        if (u > 0) mbar_wait(smem_u32(&bar_kvempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 11);
-        mbar_arrive_expect_tx(smem_u32(&bar_kfull[s]), Gm::KV_BYTES);
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64,
-                      j * BK, zkv);
-        mbar_arrive_expect_tx(smem_u32(&bar_vfull[s]), Gm::KV_BYTES);
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64,
-                      j * BK, zkv);
-      }
-      for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
-        mbar_wait_drain(smem_u32(&bar_vfull[j % ST]), (j / ST) & 1, p.limit_ns);
     }
-  } else if (warp == 5) {
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
-      constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
-      mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 12);
+    __syncwarp();
+    const int zkv = b * p.Hkv + hk;
+    mbar_arrive_expect_tx_w(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
+    for (int c = 0; c < NCH; ++c) {
+      tma_load_3d_w(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
+      tma_load_3d_w(sdO + c * BQ * 128, &tmdO, smem_u32(&bar_q), c * 64, q0, bh);
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, vs = j % VST;
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 11);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 18);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+    }
+    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+    __syncwarp();
+  } else if (warp == Gm::MMA_WARP) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
+    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);         // Q, K-major
+    const uint64_t dOd = make_sdesc_sw128(sdO, 16, 1024);        // dO, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);        // K stage 0, K-major
+    const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);        // V stage 0, K-major
+    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
+    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 12);
+    __syncwarp();
+    tc_fence_after_sync();
+    // S and dP of key tile j into buffer j & 1
+    auto issue_s = [&](int j) {
+      const int ks = j % KST, vs = j % VST, buf = j & 1;
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 13);
+      __syncwarp();
       tc_fence_after_sync();
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % ST;
-        const uint32_t kbase = sK0 + s * Gm::KV_BYTES, vbase = sV0 + s * Gm::KV_BYTES;
-        mbar_wait(smem_u32(&bar_kfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 13);
-        tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-          mma_ss(tmem + Gm::S_COL, make_sdesc_sw128(sQ + qo, 16, 1024),
-                 make_sdesc_sw128(kbase + ko, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        mbar_wait(smem_u32(&bar_vfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 14);
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-          mma_ss(tmem + Gm::DP_COL, make_sdesc_sw128(sdO + qo, 16, 1024),
-                 make_sdesc_sw128(vbase + ko, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&bar_sfull));
-        mbar_wait(smem_u32(&bar_dsready), j & 1, g, kDevTimeoutBase + 15);
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          mma_ts(tmem + Gm::DQ_COL, tmem + Gm::DS_COL + kk * 8,
-                 make_sdesc_sw128(kbase + kk * 2048, BK * 128, 1024), IDESC_DQ,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&bar_kvempty[s]));
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::S_COL + buf * BK, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
       }
-      mma_commit(smem_u32(&bar_dqdone));
-      mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
+      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 14);
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t vo = vs * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::DP_COL + buf * BK, sdesc_add(dOd, qo), sdesc_add(dVk, vo), IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_vempty[vs]));
+      mma_commit_w(smem_u32(&bar_sfull[buf]));
+    };
+    if (n_kv > 0) issue_s(0);
+    for (int j = 0; j < n_kv; ++j) {
+      if (j + 1 < n_kv) issue_s(j + 1);
+      const int ks = j % KST, buf = j & 1;
+      mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 15);
+      __syncwarp();
+      tc_fence_after_sync();
+      // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
+      // pairs in columns 32h..32h+15 of the S buffer.
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint32_t acol = Gm::S_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
+        mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, ks * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
     }
+    mma_commit_w(smem_u32(&bar_dqdone));
+    mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
+    __syncwarp();
   } else {
-    const int r = warp * 32 + lane;
+    const int quad = warp & 3;   // TMEM lane quadrant (query rows)
+    const int half = warp >> 2;  // key columns 32*half .. +31 of each tile
+    const int r = quad * 32 + lane;
     const int qi = q0 + r;
-    const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
     const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
     const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
     const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
     const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
     for (int j = 0; j < n_kv; ++j) {
-      mbar_wait(smem_u32(&bar_sfull), j & 1, g, kDevTimeoutBase + 16);
+      const int buf = j & 1;
+      mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 16);
       __syncwarp();
       tc_fence_after_sync();
-      const int k0 = j * BK;
-      const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
+      const int kc0 = j * BK + half * 32;  // first key of this thread's columns
+      const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
+      const uint32_t scol = tmem + lrow + Gm::S_COL + buf * BK + half * 32;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(scol, sr);
+      tmem_ld32(tmem + lrow + Gm::DP_COL + buf * BK + half * 32, dr);
+      tmem_ld_wait(sr);
+      reg_fence(dr);
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < BK / 32; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lrow + Gm::S_COL + c * 32, sr);
-        tmem_ld32(tmem + lrow + Gm::DP_COL + c * 32, dr);
-        tmem_ld_wait(sr);
-        reg_fence(dr);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_r));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_r));
-          if (need_mask) {
-            if (k0 + c * 32 + 2 * i > lim) p0 = 0.f;
-            if (k0 + c * 32 + 2 * i + 1 > lim) p1 = 0.f;
-          }
-          const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_r);
-          const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_r);
-          pk[i] = E::pack(ds0, ds1);
+      for (int i = 0; i < 16; ++i) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_r));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_r));
+        if (need_mask) {
+          if (kc0 + 2 * i > lim) p0 = 0.f;
+          if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
         }
-        tmem_st16(tmem + lrow + Gm::DS_COL + c * 16, pk);
+        const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_r);
+        const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_r);
+        pk[i] = E::pack(ds0, ds1);
       }
+      tmem_st16(scol, pk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_dsready));
+      mbar_arrive(smem_u32(&bar_dsready[buf]));
     }
     mbar_wait(smem_u32(&bar_dqdone), 0, g, kDevTimeoutBase + 17);
     __syncwarp();
     tc_fence_after_sync();
     typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = half; c < D / 32; c += 2) {
       uint32_t rr[32];
       tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
       tmem_ld_wait(rr);
@@ -216,7 +258,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == Gm::MMA_WARP) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
   }

@@ -100,73 +100,75 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp == 4) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int zkv = b * p.Hkv + hk;
-      mbar_arrive_expect_tx(smem_u32(&bar_q), Gm::Q_BYTES);
+    }
+    __syncwarp();
+    const int zkv = b * p.Hkv + hk;
+    mbar_arrive_expect_tx_w(smem_u32(&bar_q), Gm::Q_BYTES);
+    for (int c = 0; c < NCH; ++c) tma_load_3d_w(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j % ST, u = j / ST;
+      if (u > 0) mbar_wait(smem_u32(&bar_kvempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 1);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[s]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % ST, u = j / ST;
-        if (u > 0) mbar_wait(smem_u32(&bar_kvempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 1);
-        mbar_arrive_expect_tx(smem_u32(&bar_kfull[s]), Gm::KV_BYTES);
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64,
-                      j * BK, zkv);
-        mbar_arrive_expect_tx(smem_u32(&bar_vfull[s]), Gm::KV_BYTES);
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64,
-                      j * BK, zkv);
-      }
-      // Do not leave the CTA while a copy may still be landing.
-      for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
-        mbar_wait_drain(smem_u32(&bar_vfull[j % ST]), (j / ST) & 1, p.limit_ns);
+        tma_load_3d_w(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64, j * BK, zkv);
+      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[s]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64, j * BK, zkv);
     }
+    // Do not leave the CTA while a copy may still be landing.
+    for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_vfull[j % ST]), (j / ST) & 1, p.limit_ns);
+    __syncwarp();
   } else if (warp == 5) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
-      constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
-      mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 2);
-      tc_fence_after_sync();
-      for (int j = 0; j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int s = j % ST;
-          mbar_wait(smem_u32(&bar_kfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 3);
-          tc_fence_after_sync();
-          const uint32_t d = tmem + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
-          const uint32_t kbase = sK0 + s * Gm::KV_BYTES;
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
+    constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);         // Q, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);        // K stage 0, K-major
+    const uint64_t dVm = make_sdesc_sw128(sV0, BK * 128, 1024);  // V stage 0, MN-major
+    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 2);
+    __syncwarp();
+    tc_fence_after_sync();
+    for (int j = 0; j <= n_kv; ++j) {
+      if (j < n_kv) {
+        const int s = j % ST;
+        mbar_wait(smem_u32(&bar_kfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 3);
+        __syncwarp();
+        tc_fence_after_sync();
+        const uint32_t d = tmem + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = make_sdesc_sw128(sQ + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = make_sdesc_sw128(kbase + (kk >> 2) * (BK * 128) + (kk & 3) * 32, 16, 1024);
-            mma_ss(d, a, bd, IDESC_QK, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bar_sfull[j & 1]));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          const uint32_t ko = s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+          mma_ss_w(d, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        if (j >= 1) {
-          const int jp = j - 1, sp = jp % ST;
-          mbar_wait(smem_u32(&bar_pready[jp & 1]), (jp >> 1) & 1, g, kDevTimeoutBase + 4);
-          mbar_wait(smem_u32(&bar_vfull[sp]), (jp / ST) & 1, g, kDevTimeoutBase + 5);
-          tc_fence_after_sync();
-          const uint32_t pcol = tmem + ((jp & 1) ? Gm::P_COL1 : Gm::P_COL0);
-          const uint32_t vbase = sV0 + sp * Gm::KV_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bd = make_sdesc_sw128(vbase + kk * 2048, BK * 128, 1024);
-            mma_ts(tmem + Gm::O_COL, pcol + kk * 8, bd, IDESC_PV, (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bar_kvempty[sp]));
-          mma_commit(smem_u32(&bar_odone));
-        }
+        mma_commit_w(smem_u32(&bar_sfull[j & 1]));
       }
-      // Wait for every MMA of this CTA before tensor memory is released.
-      mma_commit(smem_u32(&bar_drain));
-      mbar_wait_drain(smem_u32(&bar_drain), 0, p.limit_ns);
+      if (j >= 1) {
+        const int jp = j - 1, sp = jp % ST;
+        mbar_wait(smem_u32(&bar_pready[jp & 1]), (jp >> 1) & 1, g, kDevTimeoutBase + 4);
+        mbar_wait(smem_u32(&bar_vfull[sp]), (jp / ST) & 1, g, kDevTimeoutBase + 5);
+        __syncwarp();
+        tc_fence_after_sync();
+        const uint32_t pcol = tmem + ((jp & 1) ? Gm::P_COL1 : Gm::P_COL0);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_ts_w(tmem + Gm::O_COL, pcol + kk * 8, sdesc_add(dVm, sp * Gm::KV_BYTES + kk * 2048), IDESC_PV,
+                   (jp > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(smem_u32(&bar_kvempty[sp]));
+        mma_commit_w(smem_u32(&bar_odone));
+      }
     }
+    // Wait for every MMA of this CTA before tensor memory is released.
+    mma_commit_w(smem_u32(&bar_drain));
+    mbar_wait_drain(smem_u32(&bar_drain), 0, p.limit_ns);
+    __syncwarp();
   } else {
     // ---------------- softmax warps ----------------
     const int r = warp * 32 + lane;
