@@ -1,0 +1,308 @@
+// Forward attention with saved base-2 log-sum-exp, two query tiles per CTA
+// (head dims up to 128).
+//
+// Same mathematics as fwd_kernel.cuh (online softmax over key tiles in the
+// log2 domain: "When the Bottleneck Moved", section 3; "feat(attention):
+// complete Flash Attention VJP implementation", section "Background"), laid
+// out so the tensor cores and the softmax work overlap:
+//   * the CTA owns 256 query rows as two 128-row tiles that share every K/V
+//     tile, with one softmax warpgroup per tile;
+//   * keys come in tiles of BK = 64 and each query tile has two S buffers in
+//     tensor memory, so S_t for key tile j+1 (and j+2) is computed while the
+//     softmax warpgroup works on tile j;  O_0, O_1 (fp32, 128 columns each)
+//     and S_0[2], S_1[2] (fp32, 64 columns each) fill the 512 TMEM columns;
+//   * P_t (16-bit pairs) is written back over the first 32 columns of its S
+//     buffer, which the warpgroup has already read; the MMA that next writes
+//     that buffer is issued after O_t += P_t V_j by the same thread (tcgen05
+//     MMAs of one CTA run in issue order);
+//   * lazy rescaling: a row keeps its reference maximum m until a new tile
+//     raises the row maximum by more than TAU = 8 (in log2 units), so P <= 2^8
+//     and O / l are rescaled only on those (rare) tiles, after waiting for the
+//     previous P V product.  The final O = acc / l and lse = m + log2 l use the
+//     same reference, so the result is exact in exact arithmetic.
+//
+// Warp roles (352 threads): warps 0-3 softmax for tile 0, warps 4-7 for tile 1
+// (thread = query row = TMEM lane), warp 8 TMA producer (Q once, then K and V
+// in separate rings), warp 9 issues tile 0's MMAs and owns the TMEM
+// allocation, warp 10 issues tile 1's MMAs.  Each MMA warp orders its own
+// tile's S / P aliasing; splitting the issue over two warps halves the serial
+// barrier-wait and commit overhead per key tile, which otherwise exceeds the
+// tensor time of a 64-key step.
+#pragma once
+
+#include "kernel_common.cuh"
+
+namespace gbattn {
+
+template <int D>
+struct Fwd2Geom {
+  static constexpr int BQ = 128;  // rows per query tile; the CTA owns 2 tiles
+  static constexpr int BK = 64;
+  static constexpr int NCH = n_chunks(D);
+  static constexpr int Q_BYTES = NCH * BQ * 128;
+  static constexpr int KV_BYTES = NCH * BK * 128;
+  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * Q_BYTES;
+  static constexpr int NKV = AVAIL / KV_BYTES;
+  static constexpr int KSTAGES = (NKV + 1) / 2 > 4 ? 4 : (NKV + 1) / 2;
+  static constexpr int VSTAGES = (NKV - KSTAGES) > 4 ? 4 : (NKV - KSTAGES);
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_THREADS = 352;
+  static constexpr float TAU = 8.0f;
+  __host__ __device__ static constexpr int o_col(int t) { return t * 128; }
+  __host__ __device__ static constexpr int s_col(int t, int b) { return 256 + t * 128 + b * 64; }
+  static_assert(D <= 128, "two O accumulators need D <= 128");
+  // S for key tile j+2 is issued while K_j may still be in use
+  static_assert(KSTAGES >= 3 && VSTAGES >= 2, "shared memory budget");
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(352, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using Gm = Fwd2Geom<D>;
+  using E = Elem<BF16>;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2][2],
+      bar_pready[2][2], bar_odone[2], bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = sbase;  // tile t at sQ + t * Q_BYTES
+  const uint32_t sK0 = sQ + 2 * Gm::Q_BYTES;
+  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
+
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq, hq = bh - b * p.Hq;
+  const int hk = hq / p.G;
+  const int pt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest first; n_qtiles counts 256-row pairs
+  const int q0 = pt * 2 * BQ;
+  const int q_hi = min(q0 + 2 * BQ, p.Lq);
+  const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
+  const int n_kv = (kv_end + BK - 1) / BK;
+  const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    // K_j / V_j are free once both tiles' MMAs that read them completed:
+    // one commit from each MMA warp.
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(smem_u32(&bar_kfull[s]), 1);
+      mbar_init(smem_u32(&bar_kempty[s]), 2);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(smem_u32(&bar_vfull[s]), 1);
+      mbar_init(smem_u32(&bar_vempty[s]), 2);
+    }
+    for (int t = 0; t < 2; ++t) {
+      for (int bb = 0; bb < 2; ++bb) {
+        mbar_init(smem_u32(&bar_sfull[t][bb]), 1);
+        mbar_init(smem_u32(&bar_pready[t][bb]), 128);
+      }
+      mbar_init(smem_u32(&bar_odone[t]), 1);
+    }
+    mbar_init(smem_u32(&bar_done), 2);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 8) {
+    // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    __syncwarp();
+    const int zkv = b * p.Hkv + hk;
+    mbar_arrive_expect_tx_w(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
+    for (int t = 0; t < 2; ++t)
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sQ + t * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0 + t * BQ, bh);
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, vs = j % VST;
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 31);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 32);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+    }
+    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+    __syncwarp();
+  } else if (warp == 9 || warp == 10) {
+    // ---------------- MMA issuers: warp 9 for tile 0, warp 10 for tile 1 ----------------
+    const int t = warp - 9;
+    constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
+    constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dQd = make_sdesc_sw128(sQ + t * Gm::Q_BYTES, 16, 1024);  // this tile's Q, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);                   // K stage 0, K-major
+    const uint64_t dVm = make_sdesc_sw128(sV0, BK * 128, 1024);             // V stage 0, MN-major
+    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 33);
+    __syncwarp();
+    tc_fence_after_sync();
+    auto issue_s = [&](int j) {
+      const int ks = j % KST;
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 34);
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::s_col(t, j & 1), sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_sfull[t][j & 1]));
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
+    };
+    auto issue_pv = [&](int j) {
+      const int vs = j % VST;
+      mbar_wait(smem_u32(&bar_pready[t][j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 35);
+      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 36);
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_ts_w(tmem + Gm::o_col(t), tmem + Gm::s_col(t, j & 1) + kk * 8,
+                 sdesc_add(dVm, vs * Gm::KV_BYTES + kk * 2048), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(smem_u32(&bar_vempty[vs]));
+      // A rescale on the last key tile needs this product done; earlier
+      // rescales use the next tile's S barrier, which covers it.
+      if (j == n_kv - 2) mma_commit_w(smem_u32(&bar_odone[t]));
+    };
+    for (int j = 0; j < 2 && j < n_kv; ++j) issue_s(j);
+    for (int j = 0; j < n_kv; ++j) {
+      issue_pv(j);
+      if (j + 2 < n_kv) issue_s(j + 2);
+    }
+    mma_commit_w(smem_u32(&bar_done));
+    mbar_wait_drain(smem_u32(&bar_done), 0, p.limit_ns);
+    __syncwarp();
+  } else {
+    // ---------------- softmax warpgroups ----------------
+    const int t = warp >> 2;  // query tile
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int q0t = q0 + t * BQ;
+    const int qi = q0t + r;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t o_col = tmem + lrow + Gm::o_col(t);
+    const float sl2 = p.scale_log2;
+    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;  // last visible key
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_kv; ++j) {
+      const int bb = j & 1;
+      const uint32_t s_col = tmem + lrow + Gm::s_col(t, bb);
+      mbar_wait(smem_u32(&bar_sfull[t][bb]), (j >> 1) & 1, g, kDevTimeoutBase + 37);
+      __syncwarp();
+      tc_fence_after_sync();
+      uint32_t ra[32], rb[32];
+      tmem_ld32(s_col, ra);
+      tmem_ld32(s_col + 32, rb);
+      tmem_ld_wait(ra);
+      reg_fence(rb);
+      const int k0 = j * BK;
+      if ((CAUSAL && (k0 + BK - 1 > q0t + p.off)) || (k0 + BK > p.Lk)) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (k0 + i > lim) ra[i] = __float_as_uint(-INFINITY);
+          if (k0 + 32 + i > lim) rb[i] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i]));
+#pragma unroll
+      for (int i = 8; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i])));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      const float m_new = fmaxf(m, mt);
+      if (__any_sync(0xffffffffu, m_new > m + Gm::TAU)) {
+        const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+        m = m_new;
+        l *= alpha;
+        if (j > 0) {
+          // O_t holds P V up to key tile j-1 once that MMA is done.  S_t of
+          // key tile j+1 was issued right after it, so its barrier covers it;
+          // on the last key tile a dedicated commit does.
+          if (j + 1 < n_kv)
+            mbar_wait(smem_u32(&bar_sfull[t][(j + 1) & 1]), ((j + 1) >> 1) & 1, g, kDevTimeoutBase + 39);
+          else
+            mbar_wait(smem_u32(&bar_odone[t]), 0, g, kDevTimeoutBase + 40);
+          __syncwarp();
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(o_col + c * 32, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(o_col + c * 32, rr);
+          }
+        }
+      }
+      float sa = 0.f, sb = 0.f;
+      uint32_t pa[16], pb[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a0 = ex2_approx(fmaf(__uint_as_float(ra[2 * i]), sl2, -m));
+        const float a1 = ex2_approx(fmaf(__uint_as_float(ra[2 * i + 1]), sl2, -m));
+        const float b0 = ex2_approx(fmaf(__uint_as_float(rb[2 * i]), sl2, -m));
+        const float b1 = ex2_approx(fmaf(__uint_as_float(rb[2 * i + 1]), sl2, -m));
+        sa += a0 + a1;
+        sb += b0 + b1;
+        pa[i] = E::pack(a0, a1);
+        pb[i] = E::pack(b0, b1);
+      }
+      l += sa + sb;
+      // P: keys 0..31 -> columns 0..15, keys 32..63 -> columns 16..31 of S_t
+      tmem_st16(s_col, pa);
+      tmem_st16(s_col + 16, pb);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_pready[t][bb]));
+    }
+    // ---------------- epilogue ----------------
+    mbar_wait(smem_u32(&bar_done), 0, g, kDevTimeoutBase + 38);
+    __syncwarp();
+    tc_fence_after_sync();
+    const float inv_l = 1.f / l;
+    typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t rr[32];
+      tmem_ld32(o_col + c * 32, rr);
+      tmem_ld_wait(rr);
+      if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
+    }
+    if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+}
+
+}  // namespace gbattn

@@ -6,6 +6,7 @@
 #include "bwd_dkv_kernel.cuh"
 #include "bwd_dq_kernel.cuh"
 #include "delta_kernel.cuh"
+#include "fwd2_kernel.cuh"
 #include "fwd_kernel.cuh"
 
 #ifndef GBATTN_HEAD_DIM
@@ -57,8 +58,31 @@ int launch(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, con
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
+// D <= 128: two 128-row query tiles per CTA (fwd2_kernel.cuh).
+template <bool BF16, bool CAUSAL>
+int fwd2_impl(const AttnArgs& a) {
+  using Gm = Fwd2Geom<(kD <= 128 ? kD : 128)>;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+    return kLaunchBadMap;
+  FwdParams p{};
+  p.o = a.o_out;
+  p.lse = a.lse_out;
+  p.status = a.status;
+  p.B = a.B, p.Hq = a.Hq, p.Hkv = a.Hkv, p.Lq = a.Lq, p.Lk = a.Lk, p.G = a.Hq / a.Hkv;
+  p.off = a.Lk - a.Lq;
+  p.n_qtiles = (a.Lq + 2 * Gm::BQ - 1) / (2 * Gm::BQ);  // 256-row pairs of tiles
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.limit_ns = a.limit_ns;
+  const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  return launch(attn_fwd2_kernel<(kD <= 128 ? kD : 128), BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
+                a.stream, tq, tk, tv, p);
+}
+
 template <bool BF16, bool CAUSAL>
 int fwd_impl(const AttnArgs& a) {
+  if constexpr (kD <= 128) return fwd2_impl<BF16, CAUSAL>(a);
   using Gm = FwdGeom<kD>;
   CUtensorMap tq, tk, tv;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) ||
