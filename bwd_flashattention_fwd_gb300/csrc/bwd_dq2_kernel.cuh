@@ -1,0 +1,271 @@
+// Backward, dQ kernel for head dims up to 128: same mathematics as
+// bwd_dq_kernel.cuh ("feat(attention): complete Flash Attention VJP
+// implementation", sections "Background" and "Two-Kernel Design": the dQ
+// kernel owns query rows and loops over key tiles; S = Q K^T and dP = dO V^T
+// are recomputed, P = exp2(S * scale_log2 - lse), dS = P * (dP - delta),
+// dQ += dS K, and dQ is scaled by `scale` at the end).
+//
+// Layout for the tensor cores: key tiles of 128 (MMA N = 128, the shape that
+// runs at full rate with both operands in shared memory).  Tensor memory holds
+// dQ (128 columns), S (128), dP (128) and two dS buffers (64 columns of
+// 16-bit pairs each): 512 columns.  S and dP are single-buffered but released
+// as soon as every row thread has copied its part into registers, so the MMAs
+// of key tile j+1 run while the threads turn tile j into dS; dS has its own
+// double buffer, freed by the dQ MMA that reads it.
+//
+// Warp roles (608 threads): warps 0-15 row threads -- warp w owns TMEM lanes
+// 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each tile;
+// warp 16 TMA producer (Q and dO once, then K and V in separate rings);
+// warp 17 issues S and dP and owns the TMEM allocation; warp 18 issues
+// dQ += dS K.
+#pragma once
+
+#include "kernel_common.cuh"
+
+namespace gbattn {
+
+template <int D>
+struct Dq2Geom {
+  static constexpr int BQ = 128;
+  static constexpr int BK = 128;
+  static constexpr int NCH = n_chunks(D);
+  static constexpr int Q_BYTES = NCH * BQ * 128;
+  static constexpr int KV_BYTES = NCH * BK * 128;
+  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * Q_BYTES;
+  static constexpr int NKV = AVAIL / KV_BYTES;
+  static constexpr int KSTAGES = (NKV + 1) / 2 > 4 ? 4 : (NKV + 1) / 2;
+  static constexpr int VSTAGES = (NKV - KSTAGES) > 4 ? 4 : (NKV - KSTAGES);
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int DQ_COL = 0, S_COL = 128, DP_COL = 256, DS_COL = 384;  // dS buffer b at DS_COL + 64 b
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_COMPUTE_WARPS = 16;
+  static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
+  static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
+  static constexpr int S_MMA_WARP = NUM_COMPUTE_WARPS + 1;
+  static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
+  static_assert(D <= 128, "dQ, S, dP and two dS buffers fill TMEM at D = 128");
+  static_assert(KSTAGES >= 2 && VSTAGES >= 1, "shared memory budget");
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(Dq2Geom<D>::NUM_THREADS, 1)
+    attn_bwd_dq2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                        const BwdParams p) {
+  using Gm = Dq2Geom<D>;
+  using E = Elem<BF16>;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull,
+      bar_sfree, bar_dsready[2], bar_pfree[2], bar_dqdone;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = sbase;
+  const uint32_t sdO = sQ + Gm::Q_BYTES;
+  const uint32_t sK0 = sdO + Gm::Q_BYTES;
+  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
+
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq, hq = bh - b * p.Hq;
+  const int hk = hq / p.G;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
+  const int q0 = qt * BQ;
+  const int q_hi = min(q0 + BQ, p.Lq);
+  const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
+  const int n_kv = (kv_end + BK - 1) / BK;
+  const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(smem_u32(&bar_kfull[s]), 1);
+      mbar_init(smem_u32(&bar_kempty[s]), 2);  // S (S warp) and dQ (dQ warp) read K_j
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(smem_u32(&bar_vfull[s]), 1);
+      mbar_init(smem_u32(&bar_vempty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_sfull), 1);
+    mbar_init(smem_u32(&bar_sfree), Gm::NCT);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_dsready[i]), Gm::NCT);
+      mbar_init(smem_u32(&bar_pfree[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_dqdone), 1);
+    fence_mbar_init();
+  }
+  if (warp == Gm::S_MMA_WARP) {
+    tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == Gm::PRODUCER_WARP) {
+    // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+    }
+    __syncwarp();
+    const int zkv = b * p.Hkv + hk;
+    mbar_arrive_expect_tx_w(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
+    for (int c = 0; c < NCH; ++c) {
+      tma_load_3d_w(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
+      tma_load_3d_w(sdO + c * BQ * 128, &tmdO, smem_u32(&bar_q), c * 64, q0, bh);
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, vs = j % VST;
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 41);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 42);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+    }
+    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+    __syncwarp();
+  } else if (warp == Gm::S_MMA_WARP) {
+    // ---------------- S / dP issuer ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
+    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);   // Q, K-major
+    const uint64_t dOd = make_sdesc_sw128(sdO, 16, 1024);  // dO, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
+    const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);  // V stage 0, K-major
+    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 43);
+    __syncwarp();
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, vs = j % VST;
+      // every row thread has copied S / dP of key tile j-1 into registers
+      if (j >= 1) mbar_wait(smem_u32(&bar_sfree), (j - 1) & 1, g, kDevTimeoutBase + 44);
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 45);
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::S_COL, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
+      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 46);
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t vo = vs * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::DP_COL, sdesc_add(dOd, qo), sdesc_add(dVk, vo), IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_vempty[vs]));
+      mma_commit_w(smem_u32(&bar_sfull));
+    }
+    __syncwarp();
+  } else if (warp == Gm::DQ_MMA_WARP) {
+    // ---------------- dQ += dS K issuer ----------------
+    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, buf = j & 1;
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 47);
+      mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 48);
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_ts_w(tmem + Gm::DQ_COL, tmem + Gm::DS_COL + buf * 64 + kk * 8,
+                 sdesc_add(dKm, ks * Gm::KV_BYTES + kk * 2048), IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(smem_u32(&bar_pfree[buf]));
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
+    }
+    // Every S / dP MMA completed before the last dS was ready, so this commit
+    // covers all MMAs of the CTA.
+    mma_commit_w(smem_u32(&bar_dqdone));
+    mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
+    __syncwarp();
+  } else {
+    // ---------------- row threads ----------------
+    const int quad = warp & 3;  // TMEM lane quadrant (query rows)
+    const int cg = warp >> 2;   // key columns 32*cg .. +31 of each tile
+    const int r = quad * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
+    const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
+    const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
+    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
+    for (int j = 0; j < n_kv; ++j) {
+      const int buf = j & 1;
+      mbar_wait(smem_u32(&bar_sfull), j & 1, g, kDevTimeoutBase + 49);
+      __syncwarp();
+      tc_fence_after_sync();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + lrow + Gm::S_COL + cg * 32, sr);
+      tmem_ld32(tmem + lrow + Gm::DP_COL + cg * 32, dr);
+      tmem_ld_wait(sr);
+      reg_fence(dr);
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_sfree));
+      const int kc0 = j * BK + cg * 32;
+      const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_r));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_r));
+        if (need_mask) {
+          if (kc0 + 2 * i > lim) p0 = 0.f;
+          if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
+        }
+        const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_r);
+        const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_r);
+        pk[i] = E::pack(ds0, ds1);
+      }
+      // the dQ MMA of key tile j-2 has finished reading this dS buffer
+      if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 50);
+      __syncwarp();
+      tc_fence_after_sync();
+      tmem_st16(tmem + lrow + Gm::DS_COL + buf * 64 + cg * 16, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_dsready[buf]));
+    }
+    mbar_wait(smem_u32(&bar_dqdone), 0, g, kDevTimeoutBase + 51);
+    __syncwarp();
+    tc_fence_after_sync();
+    typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
+    // warp group cg writes 32-column chunks cg, cg+4, ... of the dQ row
+    for (int c = cg; c < D / 32; c += 4) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+      tmem_ld_wait(rr);
+      if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Gm::S_MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+}
+
+}  // namespace gbattn

@@ -12,14 +12,18 @@
 // Pipelining: S and dP are double-buffered in tensor memory (key tiles of
 // BK = 64), so the MMAs of key tile j+1 run while the row threads turn tile j
 // into dS.  dS (16-bit pairs) is written back over the fp32 S columns the same
-// warpgroup has just read; the dQ MMA reads it from there, and the next MMA
-// writing those columns is issued after it by the same thread (tcgen05 MMAs of
-// one CTA run in issue order).  K and V tiles arrive in separate TMA rings:
-// V is released as soon as dP has used it, K only after dQ += dS K.
+// warpgroup has just read, and the dQ MMA reads it from there.  Two warps issue
+// the MMAs: one S / dP, one dQ += dS K (a single issuing warp spends more time
+// in barrier waits and commits than the tensor core needs for a tile).  MMAs of
+// different issuing threads are not ordered, so the S warp waits on a "buffer
+// free" barrier, committed after the dQ MMA that read the buffer, before it
+// writes that buffer again.  K and V tiles arrive in separate TMA rings: V is
+// released as soon as dP has used it, K only after dQ += dS K.
 //
-// Warp roles (320 threads): warps 0-7 row threads -- warp w owns TMEM lanes
+// Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each tile;
-// warp 8 TMA producer; warp 9 MMA issuer and TMEM owner.
+// warp 8 TMA producer; warp 9 issues S / dP and owns the TMEM allocation;
+// warp 10 issues dQ += dS K.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -44,7 +48,8 @@ struct DqGeom {
   static constexpr int DP_COL = S_COL + 2 * BK;         // two buffers of BK columns
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_COMPUTE_WARPS = 8;
-  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
+  static constexpr int ACC_MMA_WARP = NUM_COMPUTE_WARPS + 2;
   static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
   static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
   // S of tile j+1 is issued before dQ of tile j releases K_j: K needs 2 stages.
@@ -64,7 +69,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
-      bar_dsready[2], bar_dqdone;
+      bar_dsready[2], bar_pfree[2], bar_dqdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     mbar_init(smem_u32(&bar_q), 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(smem_u32(&bar_kfull[s]), 1);
-      mbar_init(smem_u32(&bar_kempty[s]), 1);
+      mbar_init(smem_u32(&bar_kempty[s]), 2);  // S (S warp) and dQ (dQ warp) read K_j
     }
     for (int s = 0; s < VST; ++s) {
       mbar_init(smem_u32(&bar_vfull[s]), 1);
@@ -99,6 +104,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_sfull[i]), 1);
       mbar_init(smem_u32(&bar_dsready[i]), NCT);
+      mbar_init(smem_u32(&bar_pfree[i]), 1);
     }
     mbar_init(smem_u32(&bar_dqdone), 1);
     fence_mbar_init();
@@ -146,20 +152,18 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == Gm::MMA_WARP) {
-    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    // ---------------- S / dP issuer (whole warp, one elected lane issues) ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
-    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
-    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);         // Q, K-major
-    const uint64_t dOd = make_sdesc_sw128(sdO, 16, 1024);        // dO, K-major
-    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);        // K stage 0, K-major
-    const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);        // V stage 0, K-major
-    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
+    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);   // Q, K-major
+    const uint64_t dOd = make_sdesc_sw128(sdO, 16, 1024);  // dO, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
+    const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);  // V stage 0, K-major
     mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 12);
     __syncwarp();
-    tc_fence_after_sync();
-    // S and dP of key tile j into buffer j & 1
-    auto issue_s = [&](int j) {
+    for (int j = 0; j < n_kv; ++j) {
       const int ks = j % KST, vs = j % VST, buf = j & 1;
+      // the dQ MMA of key tile j-2 has read this buffer's dS
+      if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 19);
       mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 13);
       __syncwarp();
       tc_fence_after_sync();
@@ -169,9 +173,9 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
         const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
         mma_ss_w(tmem + Gm::S_COL + buf * BK, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
       }
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
       mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 14);
       __syncwarp();
-      tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
@@ -180,11 +184,15 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       }
       mma_commit_w(smem_u32(&bar_vempty[vs]));
       mma_commit_w(smem_u32(&bar_sfull[buf]));
-    };
-    if (n_kv > 0) issue_s(0);
+    }
+    __syncwarp();
+  } else if (warp == Gm::ACC_MMA_WARP) {
+    // ---------------- dQ += dS K issuer ----------------
+    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
     for (int j = 0; j < n_kv; ++j) {
-      if (j + 1 < n_kv) issue_s(j + 1);
       const int ks = j % KST, buf = j & 1;
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 10);
       mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 15);
       __syncwarp();
       tc_fence_after_sync();
@@ -196,8 +204,11 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
         mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, ks * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
                  (j > 0 || kk > 0) ? 1u : 0u);
       }
+      mma_commit_w(smem_u32(&bar_pfree[buf]));
       mma_commit_w(smem_u32(&bar_kempty[ks]));
     }
+    // Every S / dP MMA completed before the last dS was ready, so this commit
+    // covers all MMAs of the CTA.
     mma_commit_w(smem_u32(&bar_dqdone));
     mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
     __syncwarp();
