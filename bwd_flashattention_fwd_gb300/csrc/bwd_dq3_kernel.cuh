@@ -1,0 +1,306 @@
+// Backward, dQ kernel for head dims up to 128: same mathematics as
+// bwd_dq_kernel.cuh ("feat(attention): complete Flash Attention VJP
+// implementation", sections "Background" and "Two-Kernel Design": the dQ
+// kernel owns query rows and loops over key tiles; S = Q K^T and dP = dO V^T
+// are recomputed, P = exp2(S * scale_log2 - lse), dS = P * (dP - delta),
+// dQ += dS K, and dQ is scaled by `scale` at the end).
+//
+// Shared-memory bandwidth (128 B per clock per SM) is what limits an MMA
+// whose two operands both come from shared memory at N = 64.  Q and dO do not
+// change over the CTA's key loop, so the row threads copy them once into
+// tensor memory and every MMA reads its A operand from there: S = Q K^T and
+// dP = dO V^T read only the K / V tile from shared memory, dQ += dS K reads dS
+// from tensor memory.  Tensor memory (512 columns): dQ (D), Q and dO (D/2
+// columns of 16-bit pairs each), two S and two dP buffers of 64 columns; dS
+// (16-bit pairs) is written back over the S columns its warpgroup has read.
+// S / dP of key tile j+1 run while the row threads work on tile j.  Two warps
+// issue the MMAs (S / dP, and dQ); MMAs of different threads are not ordered,
+// so the S warp waits on a "buffer free" barrier, committed after the dQ MMA
+// that read a buffer's dS, before it writes that buffer again.
+//
+// Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
+// 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each 64-key
+// tile, and copies D/2 columns of its rows of Q and dO into tensor memory;
+// warp 8 TMA producer (K and V rings); warp 9 issues S / dP and owns the TMEM
+// allocation; warp 10 issues dQ += dS K.
+#pragma once
+
+#include "kernel_common.cuh"
+
+namespace gbattn {
+
+template <int D>
+struct Dq3Geom {
+  static constexpr int BQ = 128;
+  static constexpr int BK = 64;
+  static constexpr int NCH = n_chunks(D);
+  static constexpr int KV_BYTES = NCH * BK * 128;
+  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024;
+  static constexpr int NKV = AVAIL / KV_BYTES;
+  static constexpr int KSTAGES = NKV / 2 > 6 ? 6 : NKV / 2;
+  static constexpr int VSTAGES = KSTAGES;
+  static constexpr int SMEM_BYTES = 1024 + (KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int DQ_COL = 0, Q_COL = 128, DO_COL = 192, S_COL = 256, DP_COL = 384;  // S/dP: 2 x 64
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_COMPUTE_WARPS = 8;
+  static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
+  static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
+  static constexpr int S_MMA_WARP = NUM_COMPUTE_WARPS + 1;
+  static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
+  static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
+  static_assert(KSTAGES >= 2, "S of tile j+1 is issued while K_j is still in use");
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
+    attn_bwd_dq3_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const void* __restrict__ q, const void* __restrict__ dO, const BwdParams p) {
+  using Gm = Dq3Geom<D>;
+  using E = Elem<BF16>;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_qready, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
+      bar_dsready[2], bar_pfree[2], bar_dqdone;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sK0 = sbase;
+  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
+
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq, hq = bh - b * p.Hq;
+  const int hk = hq / p.G;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
+  const int q0 = qt * BQ;
+  const int q_hi = min(q0 + BQ, p.Lq);
+  const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
+  const int n_kv = (kv_end + BK - 1) / BK;
+  const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_qready), Gm::NCT);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(smem_u32(&bar_kfull[s]), 1);
+      mbar_init(smem_u32(&bar_kempty[s]), 2);  // S (S warp) and dQ (dQ warp) read K_j
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(smem_u32(&bar_vfull[s]), 1);
+      mbar_init(smem_u32(&bar_vempty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_sfull[i]), 1);
+      mbar_init(smem_u32(&bar_dsready[i]), Gm::NCT);
+      mbar_init(smem_u32(&bar_pfree[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_dqdone), 1);
+    fence_mbar_init();
+  }
+  if (warp == Gm::S_MMA_WARP) {
+    tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == Gm::PRODUCER_WARP) {
+    // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    __syncwarp();
+    const int zkv = b * p.Hkv + hk;
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, vs = j % VST;
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 61);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 62);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+    }
+    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+    __syncwarp();
+  } else if (warp == Gm::S_MMA_WARP) {
+    // ---------------- S / dP issuer (A operands Q and dO from tensor memory) ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
+    const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);  // V stage 0, K-major
+    mbar_wait(smem_u32(&bar_qready), 0, g, kDevTimeoutBase + 63);
+    __syncwarp();
+    tc_fence_after_sync();
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, vs = j % VST, buf = j & 1;
+      // the dQ MMA of key tile j-2 has read this buffer's dS
+      if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 64);
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 65);
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ts_w(tmem + Gm::S_COL + buf * BK, tmem + Gm::Q_COL + kk * 8, sdesc_add(dKk, ko), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
+      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 66);
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t vo = vs * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ts_w(tmem + Gm::DP_COL + buf * BK, tmem + Gm::DO_COL + kk * 8, sdesc_add(dVk, vo), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_vempty[vs]));
+      mma_commit_w(smem_u32(&bar_sfull[buf]));
+    }
+    __syncwarp();
+  } else if (warp == Gm::DQ_MMA_WARP) {
+    // ---------------- dQ += dS K issuer ----------------
+    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
+    for (int j = 0; j < n_kv; ++j) {
+      const int ks = j % KST, buf = j & 1;
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 67);
+      mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 68);
+      __syncwarp();
+      tc_fence_after_sync();
+      // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
+      // pairs in columns 32h..32h+15 of the S buffer.
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint32_t acol = Gm::S_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
+        mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, ks * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_pfree[buf]));
+      mma_commit_w(smem_u32(&bar_kempty[ks]));
+    }
+    // Every S / dP MMA completed before the last dS was ready, so this commit
+    // covers all MMAs of the CTA.
+    mma_commit_w(smem_u32(&bar_dqdone));
+    mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
+    __syncwarp();
+  } else {
+    // ---------------- row threads ----------------
+    const int quad = warp & 3;   // TMEM lane quadrant (query rows)
+    const int half = warp >> 2;  // key columns 32*half .. +31 of each tile
+    const int r = quad * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
+    // Q and dO rows into tensor memory: this warp copies columns
+    // [half*D/2, (half+1)*D/2) of its 32 rows (zeros past Lq), as 16-bit pairs.
+    {
+      constexpr int HALF = D / 2;  // elements per thread per tensor
+      constexpr int NV = HALF / 8;  // 16-byte loads per thread per tensor
+      const uint4* qrow =
+          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(q) + row * D + half * HALF);
+      const uint4* orow =
+          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(dO) + row * D + half * HALF);
+      uint32_t qa[HALF / 2], oa[HALF / 2];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u), y = make_uint4(0u, 0u, 0u, 0u);
+        if (qi < p.Lq) {
+          x = qrow[v];
+          y = orow[v];
+        }
+        qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
+        oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
+      }
+      // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
+#pragma unroll
+      for (int c = 0; c + 16 <= HALF / 2; c += 16) {
+        uint32_t t16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t16[i] = qa[c + i];
+        tmem_st16(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t16);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t16[i] = oa[c + i];
+        tmem_st16(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t16);
+      }
+      if constexpr ((HALF / 2) % 16 == 8) {
+        constexpr int c = HALF / 2 - 8;
+        uint32_t t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = qa[c + i];
+        tmem_st8(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = oa[c + i];
+        tmem_st8(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t8);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_qready));
+    }
+    const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
+    const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
+    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
+    for (int j = 0; j < n_kv; ++j) {
+      const int buf = j & 1;
+      mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 69);
+      __syncwarp();
+      tc_fence_after_sync();
+      const int kc0 = j * BK + half * 32;  // first key of this thread's columns
+      const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
+      const uint32_t scol = tmem + lrow + Gm::S_COL + buf * BK + half * 32;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(scol, sr);
+      tmem_ld32(tmem + lrow + Gm::DP_COL + buf * BK + half * 32, dr);
+      tmem_ld_wait(sr);
+      reg_fence(dr);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_r));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_r));
+        if (need_mask) {
+          if (kc0 + 2 * i > lim) p0 = 0.f;
+          if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
+        }
+        const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_r);
+        const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_r);
+        pk[i] = E::pack(ds0, ds1);
+      }
+      tmem_st16(scol, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_dsready[buf]));
+    }
+    mbar_wait(smem_u32(&bar_dqdone), 0, g, kDevTimeoutBase + 70);
+    __syncwarp();
+    tc_fence_after_sync();
+    typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
+#pragma unroll 1
+    for (int c = half; c < D / 32; c += 2) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+      tmem_ld_wait(rr);
+      if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Gm::S_MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+}
+
+}  // namespace gbattn

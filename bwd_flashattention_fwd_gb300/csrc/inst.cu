@@ -5,6 +5,7 @@
 
 #include "bwd_dkv_kernel.cuh"
 #include "bwd_dq2_kernel.cuh"
+#include "bwd_dq3_kernel.cuh"
 #include "bwd_dq_kernel.cuh"
 #include "delta_kernel.cuh"
 #include "fwd2_kernel.cuh"
@@ -151,9 +152,28 @@ int dq2_impl(const AttnArgs& a) {
                 tv, tdo, p);
 }
 
+// D <= 128: Q and dO held in tensor memory as MMA A operands (bwd_dq3_kernel.cuh).
+template <bool BF16, bool CAUSAL>
+int dq3_impl(const AttnArgs& a) {
+  constexpr int DD = kD <= 128 ? kD : 128;
+  using Gm = Dq3Geom<DD>;
+  CUtensorMap tk, tv;
+  if (!make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+    return kLaunchBadMap;
+  BwdParams p = bwd_params(a);
+  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+  p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
+  const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  auto kern = attn_bwd_dq3_kernel<DD, BF16, CAUSAL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+    return kLaunchCudaError;
+  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tk, tv, a.q, a.dO, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
 template <bool BF16, bool CAUSAL>
 int dq_impl(const AttnArgs& a) {
-  if constexpr (kD <= 128) return dq2_impl<BF16, CAUSAL>(a);
+  if constexpr (kD <= 128) return dq3_impl<BF16, CAUSAL>(a);
   using Gm = DqGeom<kD>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
