@@ -60,10 +60,10 @@ def load_peaks() -> dict:
 
 
 KERNEL_FILES = {
-    "fwd": "fwd_kernel.cuh",
+    "fwd": "fwd2_kernel.cuh",
     "delta": "delta_kernel.cuh",
     "bwd_dkv": "bwd_dkv_kernel.cuh",
-    "bwd_dq": "bwd_dq_kernel.cuh",
+    "bwd_dq": "bwd_dq3_kernel.cuh",
 }
 
 
