@@ -4,7 +4,6 @@
 #include "launch.h"
 
 #include "bwd_dkv_kernel.cuh"
-#include "bwd_dq2_kernel.cuh"
 #include "bwd_dq3_kernel.cuh"
 #include "bwd_dq_kernel.cuh"
 #include "delta_kernel.cuh"
@@ -133,23 +132,6 @@ int dkv_impl(const AttnArgs& a) {
   const dim3 grid(a.B * a.Hkv, p.n_ktiles);
   return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL, MODE>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
                 tq, tk, tv, tdo, p);
-}
-
-// D <= 128: key tiles of 128 with early-released S / dP (bwd_dq2_kernel.cuh).
-template <bool BF16, bool CAUSAL>
-int dq2_impl(const AttnArgs& a) {
-  constexpr int DD = kD <= 128 ? kD : 128;
-  using Gm = Dq2Geom<DD>;
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
-    return kLaunchBadMap;
-  BwdParams p = bwd_params(a);
-  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
-  p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
-  const dim3 grid(a.B * a.Hq, p.n_qtiles);
-  return launch(attn_bwd_dq2_kernel<DD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
-                tv, tdo, p);
 }
 
 // D <= 128: Q and dO held in tensor memory as MMA A operands (bwd_dq3_kernel.cuh).
