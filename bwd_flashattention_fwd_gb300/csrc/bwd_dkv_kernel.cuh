@@ -25,8 +25,13 @@
 // Warp roles (320 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (key rows) and query columns 32*(w/4)..+31 of each tile;
 // warp 8 producer (TMA for Q/dO tiles, plain loads for the per-query
-// lse/delta values); warp 9 MMA issuer and TMEM owner.
+// lse/delta values); warp 9 MMA issuer and TMEM owner.  MMA issue competes
+// with MUFU instructions issued on the same SM sub-partition, so the row warps
+// on sub-partition 1 evaluate part of their exponentials with a polynomial on
+// the FMA pipe (ex2_poly2).
 #pragma once
+
+#include <type_traits>
 
 #include "kernel_common.cuh"
 
@@ -59,6 +64,14 @@ struct DkvGeom {
   static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
   static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
   static_assert(STAGES >= 1, "shared memory budget");
+  // element pairs (of 16 per thread and query tile) whose exponentials use
+  // the polynomial on the MMA warp's sub-partition
+#ifndef GBATTN_DKV_POLY_PAIRS
+  static constexpr int POLY_PAIRS = 8;
+#else
+  static constexpr int POLY_PAIRS = GBATTN_DKV_POLY_PAIRS;
+#endif
+  static_assert(POLY_PAIRS == 0 || 16 % POLY_PAIRS == 0, "polynomial share");
   static_assert(MODE != kDkvBoth || D <= 128, "dK and dV together need D <= 128");
   static_assert((NEED_DS ? DPT_COL + 2 * BQ : ST_COL + 2 * BQ) <= TMEM_COLS, "tensor memory budget");
 };
@@ -75,7 +88,8 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_kv, bar_stfull[ST], bar_stempty[ST], bar_sfull[2], bar_pready[2], bar_accdone;
-  __shared__ float lse_s[ST][BQ], dlt_s[ST][BQ];
+  __shared__ __align__(16) float nlse_s[ST][BQ];  // -lse per query column
+  __shared__ __align__(16) float dlt_s[ST][BQ];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -149,7 +163,7 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
         const int c = lane + 32 * t;
         const int qi = q0 + c;
         const size_t row = static_cast<size_t>(zq) * p.Lq + qi;
-        lse_s[s][c] = qi < p.Lq ? p.lse[row] : INFINITY;
+        nlse_s[s][c] = qi < p.Lq ? -p.lse[row] : -INFINITY;
         dlt_s[s][c] = (Gm::NEED_DS && qi < p.Lq) ? p.delta[row] : 0.f;
       }
       mbar_arrive(smem_u32(&bar_stfull[s]));
@@ -223,6 +237,7 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
     const int kj = k0 + r;
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const int qmin = kj - p.off;  // causal: queries below this index cannot see key kj
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % ST, buf = it & 1;
@@ -240,26 +255,41 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
       if (Gm::NEED_DS) tmem_ld32(dcol, dr);
       tmem_ld_wait(sr);
       if (Gm::NEED_DS) reg_fence(dr);
-      const float* lse_row = &lse_s[s][half * 32];
-      const float* dlt_row = &dlt_s[s][half * 32];
+      const uint64_t* nlse_row = reinterpret_cast<const uint64_t*>(&nlse_s[s][half * 32]);
+      const uint64_t* dlt_row = reinterpret_cast<const uint64_t*>(&dlt_s[s][half * 32]);
       const int qc0 = q0 + half * 32;
       uint32_t pk[16], dk[16];
+      auto pds_tile = [&](auto poly_tag) {
+        constexpr bool POLY = decltype(poly_tag)::value;
+        constexpr int EVERY = Gm::POLY_PAIRS > 0 ? 16 / Gm::POLY_PAIRS : 1;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c0 = 2 * i;
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c0]), sl2, -lse_row[c0]));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c0 + 1]), sl2, -lse_row[c0 + 1]));
-        if (need_mask) {
-          if (qc0 + c0 < qmin) p0 = 0.f;
-          if (qc0 + c0 + 1 < qmin) p1 = 0.f;
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = 2 * i;
+          float x0, x1, p0, p1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), sl2x2, nlse_row[i]), x0, x1);
+          if (POLY && i % EVERY == EVERY - 1) {
+            ex2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          if (need_mask) {
+            if (qc0 + c0 < qmin) p0 = 0.f;
+            if (qc0 + c0 + 1 < qmin) p1 = 0.f;
+          }
+          pk[i] = E::pack(p0, p1);
+          if (Gm::NEED_DS) {
+            const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[c0]), __uint_as_float(dr[c0 + 1])), dlt_row[i]);
+            float ds0, ds1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
+            dk[i] = E::pack(ds0, ds1);
+          }
         }
-        pk[i] = E::pack(p0, p1);
-        if (Gm::NEED_DS) {
-          const float ds0 = p0 * (__uint_as_float(dr[c0]) - dlt_row[c0]);
-          const float ds1 = p1 * (__uint_as_float(dr[c0 + 1]) - dlt_row[c0 + 1]);
-          dk[i] = E::pack(ds0, ds1);
-        }
-      }
+      };
+      if (Gm::POLY_PAIRS > 0 && quad == 1)  // sub-partition of the MMA warp
+        pds_tile(std::true_type{});
+      else
+        pds_tile(std::false_type{});
       if (Gm::NEED_DV) tmem_st16(scol, pk);
       if (Gm::NEED_DS) tmem_st16(dcol, dk);
       tmem_st_wait();

@@ -21,9 +21,14 @@
 // Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each 64-key
 // tile, and copies D/2 columns of its rows of Q and dO into tensor memory;
-// warp 8 TMA producer (K and V rings); warp 9 issues S / dP and owns the TMEM
-// allocation; warp 10 issues dQ += dS K.
+// warp 8 TMA producer (K_j and V_j together into one ring stage); warp 9
+// issues S / dP and owns the TMEM allocation; warp 10 issues dQ += dS K.
+// MMA issue competes with MUFU instructions issued on the same SM
+// sub-partition, so the row warps on sub-partitions 1 and 2 evaluate part of
+// their exponentials with a polynomial on the FMA pipe (ex2_poly2).
 #pragma once
+
+#include <type_traits>
 
 #include "kernel_common.cuh"
 
@@ -36,10 +41,8 @@ struct Dq3Geom {
   static constexpr int NCH = n_chunks(D);
   static constexpr int KV_BYTES = NCH * BK * 128;
   static constexpr int AVAIL = kMaxDynSmem - 512 - 1024;
-  static constexpr int NKV = AVAIL / KV_BYTES;
-  static constexpr int KSTAGES = NKV / 2 > 6 ? 6 : NKV / 2;
-  static constexpr int VSTAGES = KSTAGES;
-  static constexpr int SMEM_BYTES = 1024 + (KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int STAGES = AVAIL / (2 * KV_BYTES) > 6 ? 6 : AVAIL / (2 * KV_BYTES);  // K_j + V_j each
+  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * KV_BYTES;
   static constexpr int DQ_COL = 0, Q_COL = 128, DO_COL = 192, S_COL = 256, DP_COL = 384;  // S/dP: 2 x 64
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_COMPUTE_WARPS = 8;
@@ -49,7 +52,15 @@ struct Dq3Geom {
   static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
   static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
-  static_assert(KSTAGES >= 2, "S of tile j+1 is issued while K_j is still in use");
+  static_assert(STAGES >= 2, "S of tile j+1 is issued while K_j is still in use");
+  // element pairs (of 16 per thread and key tile) whose exponentials use the
+  // polynomial on the MMA warps' sub-partitions
+#ifndef GBATTN_DQ_POLY_PAIRS
+  static constexpr int POLY_PAIRS = 8;
+#else
+  static constexpr int POLY_PAIRS = GBATTN_DQ_POLY_PAIRS;
+#endif
+  static_assert(POLY_PAIRS == 0 || 16 % POLY_PAIRS == 0, "polynomial share");
 };
 
 template <int D, bool BF16, bool CAUSAL>
@@ -58,18 +69,17 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
                         const void* __restrict__ q, const void* __restrict__ dO, const BwdParams p) {
   using Gm = Dq3Geom<D>;
   using E = Elem<BF16>;
-  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_qready, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
-      bar_dsready[2], bar_pfree[2], bar_dqdone;
+  __shared__ uint64_t bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2], bar_dsready[2], bar_pfree[2],
+      bar_dqdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sK0 = sbase;
-  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
+  const uint32_t sK0 = sbase;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
 
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
@@ -84,13 +94,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_qready), Gm::NCT);
-    for (int s = 0; s < KST; ++s) {
-      mbar_init(smem_u32(&bar_kfull[s]), 1);
-      mbar_init(smem_u32(&bar_kempty[s]), 2);  // S (S warp) and dQ (dQ warp) read K_j
-    }
-    for (int s = 0; s < VST; ++s) {
-      mbar_init(smem_u32(&bar_vfull[s]), 1);
-      mbar_init(smem_u32(&bar_vempty[s]), 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(smem_u32(&bar_kvfull[s]), 1);
+      mbar_init(smem_u32(&bar_kvempty[s]), 2);  // S / dP (S warp) and dQ (dQ warp) read the stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_sfull[i]), 1);
@@ -118,54 +124,48 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     __syncwarp();
     const int zkv = b * p.Hkv + hk;
     for (int j = 0; j < n_kv; ++j) {
-      const int ks = j % KST, vs = j % VST;
-      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 61);
+      const int s = j % ST;
+      if (j >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (j / ST - 1) & 1, g, kDevTimeoutBase + 61);
       __syncwarp();
-      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
-      for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
-      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 62);
-      __syncwarp();
-      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
-      for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+      const uint32_t bar = smem_u32(&bar_kvfull[s]);
+      const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
+      mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c) {
+        tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
+        tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
+      }
     }
-    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
-    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+    for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kvfull[j % ST]), (j / ST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == Gm::S_MMA_WARP) {
     // ---------------- S / dP issuer (A operands Q and dO from tensor memory) ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
-    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
-    const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);  // V stage 0, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);                  // K stage 0, K-major
+    const uint64_t dVk = make_sdesc_sw128(sK0 + Gm::KV_BYTES, 16, 1024);   // V stage 0, K-major
     mbar_wait(smem_u32(&bar_qready), 0, g, kDevTimeoutBase + 63);
     __syncwarp();
     tc_fence_after_sync();
     for (int j = 0; j < n_kv; ++j) {
-      const int ks = j % KST, vs = j % VST, buf = j & 1;
+      const int s = j % ST, buf = j & 1;
       // the dQ MMA of key tile j-2 has read this buffer's dS
       if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 64);
-      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 65);
+      mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 65);
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        const uint32_t ko = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
         mma_ts_w(tmem + Gm::S_COL + buf * BK, tmem + Gm::Q_COL + kk * 8, sdesc_add(dKk, ko), IDESC_S,
                  kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(smem_u32(&bar_kempty[ks]));
-      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 66);
-      __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t vo = vs * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        const uint32_t vo = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
         mma_ts_w(tmem + Gm::DP_COL + buf * BK, tmem + Gm::DO_COL + kk * 8, sdesc_add(dVk, vo), IDESC_S,
                  kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(smem_u32(&bar_vempty[vs]));
       mma_commit_w(smem_u32(&bar_sfull[buf]));
+      mma_commit_w(smem_u32(&bar_kvempty[s]));
     }
     __syncwarp();
   } else if (warp == Gm::DQ_MMA_WARP) {
@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
     const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
     for (int j = 0; j < n_kv; ++j) {
-      const int ks = j % KST, buf = j & 1;
-      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 67);
+      const int s = j % ST, buf = j & 1;
+      // dS of tile j implies its S MMA completed, so K_j is in shared memory
       mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 68);
       __syncwarp();
       tc_fence_after_sync();
@@ -183,11 +183,11 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
         const uint32_t acol = Gm::S_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
-        mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, ks * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
+        mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
                  (j > 0 || kk > 0) ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_pfree[buf]));
-      mma_commit_w(smem_u32(&bar_kempty[ks]));
+      mma_commit_w(smem_u32(&bar_kvempty[s]));
     }
     // Every S / dP MMA completed before the last dS was ready, so this commit
     // covers all MMAs of the CTA.
@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     }
     const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
     const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
     const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
     for (int j = 0; j < n_kv; ++j) {
       const int buf = j & 1;
@@ -265,18 +266,33 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       tmem_ld_wait(sr);
       reg_fence(dr);
       uint32_t pk[16];
+      auto ds_tile = [&](auto poly_tag) {
+        constexpr bool POLY = decltype(poly_tag)::value;
+        constexpr int EVERY = Gm::POLY_PAIRS > 0 ? 16 / Gm::POLY_PAIRS : 1;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_r));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_r));
-        if (need_mask) {
-          if (kc0 + 2 * i > lim) p0 = 0.f;
-          if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1, p0, p1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, nlse2), x0, x1);
+          if (POLY && i % EVERY == EVERY - 1) {
+            ex2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          if (need_mask) {
+            if (kc0 + 2 * i > lim) p0 = 0.f;
+            if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
+          }
+          const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])), dlt2);
+          float ds0, ds1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
+          pk[i] = E::pack(ds0, ds1);
         }
-        const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_r);
-        const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_r);
-        pk[i] = E::pack(ds0, ds1);
-      }
+      };
+      if (Gm::POLY_PAIRS > 0 && (quad == 1 || quad == 2))  // sub-partitions of MMA warps 9 and 10
+        ds_tile(std::true_type{});
+      else
+        ds_tile(std::false_type{});
       tmem_st16(scol, pk);
       tmem_st_wait();
       tc_fence_before_sync();

@@ -22,12 +22,16 @@
 //     same reference, so the result is exact in exact arithmetic.
 //
 // Warp roles (352 threads): warps 0-3 softmax for tile 0, warps 4-7 for tile 1
-// (thread = query row = TMEM lane), warp 8 TMA producer (Q once, then K and V
-// in separate rings), warp 9 issues tile 0's MMAs and owns the TMEM
-// allocation, warp 10 issues tile 1's MMAs.  Each MMA warp orders its own
-// tile's S / P aliasing; splitting the issue over two warps halves the serial
-// barrier-wait and commit overhead per key tile, which otherwise exceeds the
-// tensor time of a 64-key step.
+// (thread = query row = TMEM lane), warp 8 TMA producer (Q once, then K_j and
+// V_j together into one ring stage), warp 9 issues tile 0's MMAs and owns the
+// TMEM allocation, warp 10 issues tile 1's MMAs.  Each MMA warp orders its
+// own tile's S / P aliasing; splitting the issue over two warps halves the
+// serial barrier-wait and commit overhead per key tile, which otherwise
+// exceeds the tensor time of a 64-key step.
+//
+// The softmax works on packed pairs (.f32x2 fma / add) and takes the row
+// maximum with three-input max, which keeps its instruction count, and so its
+// share of the issue slots of the sub-partitions the MMA warps run on, low.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -42,18 +46,16 @@ struct Fwd2Geom {
   static constexpr int Q_BYTES = NCH * BQ * 128;
   static constexpr int KV_BYTES = NCH * BK * 128;
   static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * Q_BYTES;
-  static constexpr int NKV = AVAIL / KV_BYTES;
-  static constexpr int KSTAGES = (NKV + 1) / 2 > 4 ? 4 : (NKV + 1) / 2;
-  static constexpr int VSTAGES = (NKV - KSTAGES) > 4 ? 4 : (NKV - KSTAGES);
-  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int STAGES = AVAIL / (2 * KV_BYTES) > 6 ? 6 : AVAIL / (2 * KV_BYTES);  // K_j + V_j each
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + STAGES * 2 * KV_BYTES;
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_THREADS = 352;
   static constexpr float TAU = 8.0f;
   __host__ __device__ static constexpr int o_col(int t) { return t * 128; }
   __host__ __device__ static constexpr int s_col(int t, int b) { return 256 + t * 128 + b * 64; }
   static_assert(D <= 128, "two O accumulators need D <= 128");
-  // S for key tile j+2 is issued while K_j may still be in use
-  static_assert(KSTAGES >= 3 && VSTAGES >= 2, "shared memory budget");
+  // S for key tile j+2 is issued while K_j / V_j may still be in use
+  static_assert(STAGES >= 3, "shared memory budget");
 };
 
 template <int D, bool BF16, bool CAUSAL>
@@ -62,19 +64,18 @@ __global__ void __launch_bounds__(352, 1)
                      const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Gm = Fwd2Geom<D>;
   using E = Elem<BF16>;
-  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2][2],
-      bar_pready[2][2], bar_odone[2], bar_done;
+  __shared__ uint64_t bar_q, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2][2], bar_pready[2][2], bar_odone[2],
+      bar_done;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;  // tile t at sQ + t * Q_BYTES
-  const uint32_t sK0 = sQ + 2 * Gm::Q_BYTES;
-  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
+  const uint32_t sK0 = sQ + 2 * Gm::Q_BYTES;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
 
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
@@ -89,15 +90,11 @@ __global__ void __launch_bounds__(352, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
-    // K_j / V_j are free once both tiles' MMAs that read them completed:
-    // one commit from each MMA warp.
-    for (int s = 0; s < KST; ++s) {
-      mbar_init(smem_u32(&bar_kfull[s]), 1);
-      mbar_init(smem_u32(&bar_kempty[s]), 2);
-    }
-    for (int s = 0; s < VST; ++s) {
-      mbar_init(smem_u32(&bar_vfull[s]), 1);
-      mbar_init(smem_u32(&bar_vempty[s]), 2);
+    // A stage (K_j, V_j) is free once both tiles' MMAs that read it
+    // completed: one commit from each MMA warp, after its P_t V_j.
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(smem_u32(&bar_kvfull[s]), 1);
+      mbar_init(smem_u32(&bar_kvempty[s]), 2);
     }
     for (int t = 0; t < 2; ++t) {
       for (int bb = 0; bb < 2; ++bb) {
@@ -132,22 +129,19 @@ __global__ void __launch_bounds__(352, 1)
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sQ + t * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0 + t * BQ, bh);
     for (int j = 0; j < n_kv; ++j) {
-      const int ks = j % KST, vs = j % VST;
-      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 31);
+      const int s = j % ST;
+      if (j >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (j / ST - 1) & 1, g, kDevTimeoutBase + 31);
       __syncwarp();
-      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
-      for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
-      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 32);
-      __syncwarp();
-      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
-      for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+      const uint32_t bar = smem_u32(&bar_kvfull[s]);
+      const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
+      mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
+      for (int c = 0; c < NCH; ++c) {
+        tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
+        tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
+      }
     }
-    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
-    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+    for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kvfull[j % ST]), (j / ST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
     // ---------------- MMA issuers: warp 9 for tile 0, warp 10 for tile 1 ----------------
@@ -155,35 +149,35 @@ __global__ void __launch_bounds__(352, 1)
     constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
     constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
     const uint64_t dQd = make_sdesc_sw128(sQ + t * Gm::Q_BYTES, 16, 1024);  // this tile's Q, K-major
-    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);                   // K stage 0, K-major
-    const uint64_t dVm = make_sdesc_sw128(sV0, BK * 128, 1024);             // V stage 0, MN-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);                         // K stage 0, K-major
+    const uint64_t dVm = make_sdesc_sw128(sK0 + Gm::KV_BYTES, BK * 128, 1024);    // V stage 0, MN-major
     mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 33);
     __syncwarp();
     tc_fence_after_sync();
+    // S_t of key tile j; the wait on the stage also covers V_j for P_t V_j
     auto issue_s = [&](int j) {
-      const int ks = j % KST;
-      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 34);
+      const int s = j % ST;
+      mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 34);
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-        const uint32_t ko = ks * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        const uint32_t ko = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
         mma_ss_w(tmem + Gm::s_col(t, j & 1), sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_sfull[t][j & 1]));
-      mma_commit_w(smem_u32(&bar_kempty[ks]));
     };
     auto issue_pv = [&](int j) {
-      const int vs = j % VST;
+      const int s = j % ST;
       mbar_wait(smem_u32(&bar_pready[t][j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 35);
-      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 36);
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk)
         mma_ts_w(tmem + Gm::o_col(t), tmem + Gm::s_col(t, j & 1) + kk * 8,
-                 sdesc_add(dVm, vs * Gm::KV_BYTES + kk * 2048), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_w(smem_u32(&bar_vempty[vs]));
+                 sdesc_add(dVm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+      // this thread's S_t(j) and P_t V_j are the last reads of the stage
+      mma_commit_w(smem_u32(&bar_kvempty[s]));
       // A rescale on the last key tile needs this product done; earlier
       // rescales use the next tile's S barrier, which covers it.
       if (j == n_kv - 2) mma_commit_w(smem_u32(&bar_odone[t]));
@@ -231,9 +225,8 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i]));
 #pragma unroll
-      for (int i = 8; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i])));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      for (int i = 8; i < 32; ++i) mx[i & 7] = fmax3(mx[i & 7], __uint_as_float(ra[i]), __uint_as_float(rb[i]));
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
       const float m_new = fmaxf(m, mt);
       if (__any_sync(0xffffffffu, m_new > m + Gm::TAU)) {
         const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
@@ -260,20 +253,28 @@ __global__ void __launch_bounds__(352, 1)
           }
         }
       }
-      float sa = 0.f, sb = 0.f;
+      // P = exp2(S * scale_log2 - m), two elements per packed instruction
+      uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
       uint32_t pa[16], pb[16];
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m, -m);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float a0 = ex2_approx(fmaf(__uint_as_float(ra[2 * i]), sl2, -m));
-        const float a1 = ex2_approx(fmaf(__uint_as_float(ra[2 * i + 1]), sl2, -m));
-        const float b0 = ex2_approx(fmaf(__uint_as_float(rb[2 * i]), sl2, -m));
-        const float b1 = ex2_approx(fmaf(__uint_as_float(rb[2 * i + 1]), sl2, -m));
-        sa += a0 + a1;
-        sb += b0 + b1;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), sl2x2, nm2), x0, x1);
+        const float a0 = ex2_approx(x0), a1 = ex2_approx(x1);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])), sl2x2, nm2), x0, x1);
+        const float b0 = ex2_approx(x0), b1 = ex2_approx(x1);
+        sa2 = f2_add(sa2, f2_pack(a0, a1));
+        sb2 = f2_add(sb2, f2_pack(b0, b1));
         pa[i] = E::pack(a0, a1);
         pb[i] = E::pack(b0, b1);
       }
-      l += sa + sb;
+      {
+        float s0, s1, s2, s3;
+        f2_unpack(sa2, s0, s1);
+        f2_unpack(sb2, s2, s3);
+        l += (s0 + s1) + (s2 + s3);
+      }
       // P: keys 0..31 -> columns 0..15, keys 32..63 -> columns 16..31 of S_t
       tmem_st16(s_col, pa);
       tmem_st16(s_col + 16, pb);

@@ -356,4 +356,66 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed pairs of fp32 values (sm_100-family .f32x2 arithmetic: one
+// instruction, two lanes, each rounded as the scalar operation).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for two values on the FMA pipe instead of the MUFU unit.  Method:
+// range reduction to x = n + f with n = round(x) and |f| <= 1/2 (adding
+// 1.5 * 2^23 rounds x to an integer held in the low mantissa bits), then a
+// degree-3 polynomial for 2^f whose coefficients minimise the maximum
+// relative error on [-1/2, 1/2] (fitted by a Remez exchange; max relative
+// error 7.5e-5, below the 2^-9 half-ulp of bf16 and the 2^-11 of fp16 that P
+// is rounded to), and the exponent n added to the result's exponent field.
+// Inputs below -126 are clamped there (the result is then < 1.2e-38).
+// Used where the MUFU unit is shared with a warp that issues tensor-core
+// instructions: MUFU traffic on a sub-partition delays that warp's issue.
+__device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& y1) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+  const uint64_t rnd = f2_pack(kRound, kRound);
+  const uint64_t t = f2_add(x, rnd);
+  const uint64_t f = f2_sub(x, f2_sub(t, rnd));
+  uint64_t p = f2_fma(f, f2_pack(0x1.c3f76p-5f, 0x1.c3f76p-5f), f2_pack(0x1.f0de1ap-3f, 0x1.f0de1ap-3f));
+  p = f2_fma(p, f, f2_pack(0x1.62f31ap-1f, 0x1.62f31ap-1f));
+  p = f2_fma(p, f, f2_pack(0x1.fff692p-1f, 0x1.fff692p-1f));
+  float p0, p1, t0, t1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(t, t0, t1);
+  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
+
 }  // namespace gbattn
