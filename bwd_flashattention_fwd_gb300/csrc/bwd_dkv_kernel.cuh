@@ -67,11 +67,11 @@ struct DkvGeom {
   // element pairs (of 16 per thread and query tile) whose exponentials use
   // the polynomial on the MMA warp's sub-partition
 #ifndef GBATTN_DKV_POLY_PAIRS
-  static constexpr int POLY_PAIRS = 8;
+  static constexpr int POLY_PAIRS = 10;
 #else
   static constexpr int POLY_PAIRS = GBATTN_DKV_POLY_PAIRS;
 #endif
-  static_assert(POLY_PAIRS == 0 || 16 % POLY_PAIRS == 0, "polynomial share");
+  static_assert(POLY_PAIRS >= 0 && POLY_PAIRS <= 16, "polynomial share");
   static_assert(MODE != kDkvBoth || D <= 128, "dK and dV together need D <= 128");
   static_assert((NEED_DS ? DPT_COL + 2 * BQ : ST_COL + 2 * BQ) <= TMEM_COLS, "tensor memory budget");
 };
@@ -259,15 +259,15 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
       const uint64_t* dlt_row = reinterpret_cast<const uint64_t*>(&dlt_s[s][half * 32]);
       const int qc0 = q0 + half * 32;
       uint32_t pk[16], dk[16];
-      auto pds_tile = [&](auto poly_tag) {
-        constexpr bool POLY = decltype(poly_tag)::value;
-        constexpr int EVERY = Gm::POLY_PAIRS > 0 ? 16 / Gm::POLY_PAIRS : 1;
+      // NPOLY of the 16 pairs, spread evenly, use the polynomial
+      auto pds_tile = [&](auto npoly_tag) {
+        constexpr int NPOLY = decltype(npoly_tag)::value;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c0 = 2 * i;
           float x0, x1, p0, p1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), sl2x2, nlse_row[i]), x0, x1);
-          if (POLY && i % EVERY == EVERY - 1) {
+          if ((i + 1) * NPOLY / 16 > i * NPOLY / 16) {
             ex2_poly2(x0, x1, p0, p1);
           } else {
             p0 = ex2_approx(x0);
@@ -286,10 +286,10 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
           }
         }
       };
-      if (Gm::POLY_PAIRS > 0 && quad == 1)  // sub-partition of the MMA warp
-        pds_tile(std::true_type{});
+      if (quad == 1)  // sub-partition of the MMA warp
+        pds_tile(std::integral_constant<int, Gm::POLY_PAIRS>{});
       else
-        pds_tile(std::false_type{});
+        pds_tile(std::integral_constant<int, 0>{});
       if (Gm::NEED_DV) tmem_st16(scol, pk);
       if (Gm::NEED_DS) tmem_st16(dcol, dk);
       tmem_st_wait();

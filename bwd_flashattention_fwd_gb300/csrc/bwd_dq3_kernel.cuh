@@ -11,18 +11,23 @@
 // tensor memory and every MMA reads its A operand from there: S = Q K^T and
 // dP = dO V^T read only the K / V tile from shared memory, dQ += dS K reads dS
 // from tensor memory.  Tensor memory (512 columns): dQ (D), Q and dO (D/2
-// columns of 16-bit pairs each), two S and two dP buffers of 64 columns; dS
-// (16-bit pairs) is written back over the S columns its warpgroup has read.
-// S / dP of key tile j+1 run while the row threads work on tile j.  Two warps
-// issue the MMAs (S / dP, and dQ); MMAs of different threads are not ordered,
-// so the S warp waits on a "buffer free" barrier, committed after the dQ MMA
-// that read a buffer's dS, before it writes that buffer again.
+// columns of 16-bit pairs each), one S buffer and three dP buffers of 64
+// columns; dS (16-bit pairs) is written back over the dP columns its warp
+// has read.  Two warps issue the MMAs, each in an order that needs no
+// completion round trip (tcgen05 MMAs of one issuing thread execute in issue
+// order):
+//   * the S warp issues S(j+1) as soon as every row thread has loaded S(j)
+//     into registers ("S free" barrier), so it runs while the rows compute;
+//   * the dQ warp issues dQ(j) += dS(j) K_j and then dP(j+3) into dP buffer
+//     j mod 3, behind the MMA that reads dS(j) from it; three buffers keep
+//     dP two tiles ahead of the row threads.
 //
 // Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each 64-key
 // tile, and copies D/2 columns of its rows of Q and dO into tensor memory;
 // warp 8 TMA producer (K_j and V_j together into one ring stage); warp 9
-// issues S / dP and owns the TMEM allocation; warp 10 issues dQ += dS K.
+// issues S = Q K^T and owns the TMEM allocation; warp 10 issues dQ += dS K
+// and dP = dO V^T.
 // MMA issue competes with MUFU instructions issued on the same SM
 // sub-partition, so the row warps on sub-partitions 1 and 2 evaluate part of
 // their exponentials with a polynomial on the FMA pipe (ex2_poly2).
@@ -43,7 +48,8 @@ struct Dq3Geom {
   static constexpr int AVAIL = kMaxDynSmem - 512 - 1024;
   static constexpr int STAGES = AVAIL / (2 * KV_BYTES) > 6 ? 6 : AVAIL / (2 * KV_BYTES);  // K_j + V_j each
   static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * KV_BYTES;
-  static constexpr int DQ_COL = 0, Q_COL = 128, DO_COL = 192, S_COL = 256, DP_COL = 384;  // S/dP: 2 x 64
+  static constexpr int DQ_COL = 0, Q_COL = 128, DO_COL = 192, S_COL = 256, DP_COL = 320;  // dP: 3 x 64
+  static constexpr int NDP = 3;  // dP buffers
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_COMPUTE_WARPS = 8;
   static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
@@ -52,15 +58,21 @@ struct Dq3Geom {
   static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
   static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
-  static_assert(STAGES >= 2, "S of tile j+1 is issued while K_j is still in use");
+  static_assert(STAGES >= NDP + 1, "dP of tile j+3 is issued while K_j is still in use");
   // element pairs (of 16 per thread and key tile) whose exponentials use the
-  // polynomial on the MMA warps' sub-partitions
-#ifndef GBATTN_DQ_POLY_PAIRS
-  static constexpr int POLY_PAIRS = 8;
+  // polynomial, on the sub-partition of the S warp (1) and of the dQ / dP
+  // warp (2)
+#ifndef GBATTN_DQ_POLY_Q1
+  static constexpr int POLY_Q1 = 0;
 #else
-  static constexpr int POLY_PAIRS = GBATTN_DQ_POLY_PAIRS;
+  static constexpr int POLY_Q1 = GBATTN_DQ_POLY_Q1;
 #endif
-  static_assert(POLY_PAIRS == 0 || 16 % POLY_PAIRS == 0, "polynomial share");
+#ifndef GBATTN_DQ_POLY_Q2
+  static constexpr int POLY_Q2 = 8;
+#else
+  static constexpr int POLY_Q2 = GBATTN_DQ_POLY_Q2;
+#endif
+  static_assert(POLY_Q1 >= 0 && POLY_Q1 <= 16 && POLY_Q2 >= 0 && POLY_Q2 <= 16, "polynomial share");
 };
 
 template <int D, bool BF16, bool CAUSAL>
@@ -72,8 +84,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2], bar_dsready[2], bar_pfree[2],
-      bar_dqdone;
+  constexpr int NDP = Gm::NDP;
+  __shared__ uint64_t bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_sfree, bar_dpfull[NDP],
+      bar_dsready[NDP], bar_dqdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -96,12 +109,13 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     mbar_init(smem_u32(&bar_qready), Gm::NCT);
     for (int s = 0; s < ST; ++s) {
       mbar_init(smem_u32(&bar_kvfull[s]), 1);
-      mbar_init(smem_u32(&bar_kvempty[s]), 2);  // S / dP (S warp) and dQ (dQ warp) read the stage
+      mbar_init(smem_u32(&bar_kvempty[s]), 2);  // S (S warp) and dP, dQ (dQ warp) read the stage
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_sfull[i]), 1);
+    mbar_init(smem_u32(&bar_sfull), 1);
+    mbar_init(smem_u32(&bar_sfree), Gm::NCT);
+    for (int i = 0; i < NDP; ++i) {
+      mbar_init(smem_u32(&bar_dpfull[i]), 1);
       mbar_init(smem_u32(&bar_dsready[i]), Gm::NCT);
-      mbar_init(smem_u32(&bar_pfree[i]), 1);
     }
     mbar_init(smem_u32(&bar_dqdone), 1);
     fence_mbar_init();
@@ -139,57 +153,69 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       mbar_wait_drain(smem_u32(&bar_kvfull[j % ST]), (j / ST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == Gm::S_MMA_WARP) {
-    // ---------------- S / dP issuer (A operands Q and dO from tensor memory) ----------------
+    // ---------------- S = Q K^T issuer (A operand Q from tensor memory) ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
-    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);                  // K stage 0, K-major
-    const uint64_t dVk = make_sdesc_sw128(sK0 + Gm::KV_BYTES, 16, 1024);   // V stage 0, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
     mbar_wait(smem_u32(&bar_qready), 0, g, kDevTimeoutBase + 63);
     __syncwarp();
     tc_fence_after_sync();
     for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST, buf = j & 1;
-      // the dQ MMA of key tile j-2 has read this buffer's dS
-      if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 64);
+      const int s = j % ST;
+      // every row thread has loaded S(j-1) from the buffer
+      if (j >= 1) mbar_wait(smem_u32(&bar_sfree), (j - 1) & 1, g, kDevTimeoutBase + 64);
       mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 65);
       __syncwarp();
+      tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-        mma_ts_w(tmem + Gm::S_COL + buf * BK, tmem + Gm::Q_COL + kk * 8, sdesc_add(dKk, ko), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+        mma_ts_w(tmem + Gm::S_COL, tmem + Gm::Q_COL + kk * 8, sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
       }
+      mma_commit_w(smem_u32(&bar_sfull));
+      mma_commit_w(smem_u32(&bar_kvempty[s]));
+    }
+    __syncwarp();
+  } else if (warp == Gm::DQ_MMA_WARP) {
+    // ---------------- dQ += dS K and dP = dO V^T issuer ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
+    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dVk = make_sdesc_sw128(sK0 + Gm::KV_BYTES, 16, 1024);  // V stage 0, K-major
+    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);           // K stage 0, MN-major
+    mbar_wait(smem_u32(&bar_qready), 0, g, kDevTimeoutBase + 66);
+    __syncwarp();
+    tc_fence_after_sync();
+    auto issue_dp = [&](int j) {
+      const int s = j % ST, buf = j % NDP;
+      mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 67);
+      __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t vo = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
         mma_ts_w(tmem + Gm::DP_COL + buf * BK, tmem + Gm::DO_COL + kk * 8, sdesc_add(dVk, vo), IDESC_S,
                  kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(smem_u32(&bar_sfull[buf]));
-      mma_commit_w(smem_u32(&bar_kvempty[s]));
-    }
-    __syncwarp();
-  } else if (warp == Gm::DQ_MMA_WARP) {
-    // ---------------- dQ += dS K issuer ----------------
-    constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
-    const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
+      mma_commit_w(smem_u32(&bar_dpfull[buf]));
+    };
+    for (int j = 0; j < NDP && j < n_kv; ++j) issue_dp(j);
     for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST, buf = j & 1;
-      // dS of tile j implies its S MMA completed, so K_j is in shared memory
-      mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 68);
+      const int s = j % ST, buf = j % NDP;
+      mbar_wait(smem_u32(&bar_dsready[buf]), (j / NDP) & 1, g, kDevTimeoutBase + 68);
       __syncwarp();
       tc_fence_after_sync();
       // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
-      // pairs in columns 32h..32h+15 of the S buffer.
+      // pairs in columns 32h..32h+15 of the dP buffer.
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
-        const uint32_t acol = Gm::S_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
+        const uint32_t acol = Gm::DP_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
         mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
                  (j > 0 || kk > 0) ? 1u : 0u);
       }
-      mma_commit_w(smem_u32(&bar_pfree[buf]));
+      // this warp's dP(j) and dQ(j) are its last reads of the stage
       mma_commit_w(smem_u32(&bar_kvempty[s]));
+      // dP(j+3) overwrites the buffer behind dQ(j), which reads its dS
+      if (j + NDP < n_kv) issue_dp(j + NDP);
     }
-    // Every S / dP MMA completed before the last dS was ready, so this commit
+    // Every S MMA completed before the last dS was ready, so this commit
     // covers all MMAs of the CTA.
     mma_commit_w(smem_u32(&bar_dqdone));
     mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
@@ -253,27 +279,31 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
     const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
     for (int j = 0; j < n_kv; ++j) {
-      const int buf = j & 1;
-      mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 69);
+      const int buf = j % NDP;
+      mbar_wait(smem_u32(&bar_sfull), j & 1, g, kDevTimeoutBase + 69);
+      mbar_wait(smem_u32(&bar_dpfull[buf]), (j / NDP) & 1, g, kDevTimeoutBase + 71);
       __syncwarp();
       tc_fence_after_sync();
       const int kc0 = j * BK + half * 32;  // first key of this thread's columns
       const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
-      const uint32_t scol = tmem + lrow + Gm::S_COL + buf * BK + half * 32;
+      const uint32_t dcol = tmem + lrow + Gm::DP_COL + buf * BK + half * 32;
       uint32_t sr[32], dr[32];
-      tmem_ld32(scol, sr);
-      tmem_ld32(tmem + lrow + Gm::DP_COL + buf * BK + half * 32, dr);
+      tmem_ld32(tmem + lrow + Gm::S_COL + half * 32, sr);
+      tmem_ld32(dcol, dr);
       tmem_ld_wait(sr);
       reg_fence(dr);
+      // S(j) is in registers: the S warp may overwrite the buffer
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_sfree));
       uint32_t pk[16];
-      auto ds_tile = [&](auto poly_tag) {
-        constexpr bool POLY = decltype(poly_tag)::value;
-        constexpr int EVERY = Gm::POLY_PAIRS > 0 ? 16 / Gm::POLY_PAIRS : 1;
+      // NPOLY of the 16 pairs, spread evenly, use the polynomial
+      auto ds_tile = [&](auto npoly_tag) {
+        constexpr int NPOLY = decltype(npoly_tag)::value;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1, p0, p1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, nlse2), x0, x1);
-          if (POLY && i % EVERY == EVERY - 1) {
+          if ((i + 1) * NPOLY / 16 > i * NPOLY / 16) {
             ex2_poly2(x0, x1, p0, p1);
           } else {
             p0 = ex2_approx(x0);
@@ -289,11 +319,13 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
           pk[i] = E::pack(ds0, ds1);
         }
       };
-      if (Gm::POLY_PAIRS > 0 && (quad == 1 || quad == 2))  // sub-partitions of MMA warps 9 and 10
-        ds_tile(std::true_type{});
+      if (quad == 1)  // sub-partition of the S / dP warp (9)
+        ds_tile(std::integral_constant<int, Gm::POLY_Q1>{});
+      else if (quad == 2)  // sub-partition of the dQ warp (10)
+        ds_tile(std::integral_constant<int, Gm::POLY_Q2>{});
       else
-        ds_tile(std::false_type{});
-      tmem_st16(scol, pk);
+        ds_tile(std::integral_constant<int, 0>{});
+      tmem_st16(dcol, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_dsready[buf]));
