@@ -62,7 +62,7 @@ def load_peaks() -> dict:
 KERNEL_FILES = {
     "fwd": "fwd2_kernel.cuh",
     "delta": "delta_kernel.cuh",
-    "bwd_dkv": "bwd_dkv_kernel.cuh",
+    "bwd_dkv": "bwd_dkv2_kernel.cuh",
     "bwd_dq": "bwd_dq3_kernel.cuh",
 }
 

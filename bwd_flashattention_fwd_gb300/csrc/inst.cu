@@ -3,6 +3,7 @@
 // four translation units compile in parallel.
 #include "launch.h"
 
+#include "bwd_dkv2_kernel.cuh"
 #include "bwd_dkv_kernel.cuh"
 #include "bwd_dq3_kernel.cuh"
 #include "bwd_dq_kernel.cuh"
@@ -134,6 +135,26 @@ int dkv_impl(const AttnArgs& a) {
                 tq, tk, tv, tdo, p);
 }
 
+// D <= 128: K held in tensor memory as the A operand of S^T (bwd_dkv2_kernel.cuh).
+template <bool BF16, bool CAUSAL>
+int dkv2_impl(const AttnArgs& a) {
+  constexpr int DD = kD <= 128 ? kD : 128;
+  using Gm = Dkv2Geom<DD>;
+  CUtensorMap tq, tv, tdo;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+    return kLaunchBadMap;
+  BwdParams p = bwd_params(a);
+  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+  p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
+  const dim3 grid(a.B * a.Hkv, p.n_ktiles);
+  auto kern = attn_bwd_dkv2_kernel<DD, BF16, CAUSAL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+    return kLaunchCudaError;
+  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, a.k, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
 // D <= 128: Q and dO held in tensor memory as MMA A operands (bwd_dq3_kernel.cuh).
 template <bool BF16, bool CAUSAL>
 int dq3_impl(const AttnArgs& a) {
@@ -172,7 +193,7 @@ int dq_impl(const AttnArgs& a) {
 template <bool BF16, bool CAUSAL>
 int dkv_all(const AttnArgs& a) {
   if constexpr (kD <= 128) {
-    return dkv_impl<BF16, CAUSAL, kDkvBoth>(a);
+    return dkv2_impl<BF16, CAUSAL>(a);
   } else {
     const int r = dkv_impl<BF16, CAUSAL, kDkvDvOnly>(a);
     return r == kLaunchOk ? dkv_impl<BF16, CAUSAL, kDkvDkOnly>(a) : r;
