@@ -51,7 +51,14 @@ struct Dq3Geom {
   static constexpr int DQ_COL = 0, Q_COL = 128, DO_COL = 192, S_COL = 256, DP_COL = 320;  // dP: 3 x 64
   static constexpr int NDP = 3;  // dP buffers
   static constexpr int TMEM_COLS = 512;
+#ifndef GBATTN_DQ_ROW_WARPS
   static constexpr int NUM_COMPUTE_WARPS = 8;
+#else
+  static constexpr int NUM_COMPUTE_WARPS = GBATTN_DQ_ROW_WARPS;
+#endif
+  static constexpr int NG = NUM_COMPUTE_WARPS / 4;  // row warps per TMEM lane quadrant
+  static constexpr int KC = BK / NG;                 // key columns per row warp
+  static_assert(NUM_COMPUTE_WARPS == 8 || NUM_COMPUTE_WARPS == 16, "row warps");
   static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
   static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
   static constexpr int S_MMA_WARP = NUM_COMPUTE_WARPS + 1;
@@ -202,11 +209,11 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       mbar_wait(smem_u32(&bar_dsready[buf]), (j / NDP) & 1, g, kDevTimeoutBase + 68);
       __syncwarp();
       tc_fence_after_sync();
-      // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
-      // pairs in columns 32h..32h+15 of the dP buffer.
+      // A operand: 16 keys per K step; keys KC*h..KC*h+KC-1 of row-warp
+      // group h sit as pairs in columns KC*h..KC*h+KC/2-1 of the dP buffer.
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
-        const uint32_t acol = Gm::DP_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
+        const uint32_t acol = Gm::DP_COL + buf * BK + (16 * kk / Gm::KC) * Gm::KC + (16 * kk % Gm::KC) / 2;
         mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
                  (j > 0 || kk > 0) ? 1u : 0u);
       }
@@ -222,23 +229,25 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ---------------- row threads ----------------
-    const int quad = warp & 3;   // TMEM lane quadrant (query rows)
-    const int half = warp >> 2;  // key columns 32*half .. +31 of each tile
+    constexpr int NG = Gm::NG, KC = Gm::KC;
+    const int quad = warp & 3;  // TMEM lane quadrant (query rows)
+    const int grp = warp >> 2;  // key columns KC*grp .. +KC-1 of each tile
     const int r = quad * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
     const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
     // Q and dO rows into tensor memory: this warp copies columns
-    // [half*D/2, (half+1)*D/2) of its 32 rows (zeros past Lq), as 16-bit pairs.
+    // [grp*D/NG, (grp+1)*D/NG) of its 32 rows (zeros past Lq), as 16-bit pairs.
     {
-      constexpr int HALF = D / 2;  // elements per thread per tensor
-      constexpr int NV = HALF / 8;  // 16-byte loads per thread per tensor
+      constexpr int EW = D / NG;   // elements per thread per tensor
+      constexpr int NV = EW / 8;   // 16-byte loads per thread per tensor
+      constexpr int PC = EW / 2;   // packed columns per thread per tensor
       const uint4* qrow =
-          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(q) + row * D + half * HALF);
+          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(q) + row * D + grp * EW);
       const uint4* orow =
-          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(dO) + row * D + half * HALF);
-      uint32_t qa[HALF / 2], oa[HALF / 2];
+          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(dO) + row * D + grp * EW);
+      uint32_t qa[PC], oa[PC];
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u), y = make_uint4(0u, 0u, 0u, 0u);
@@ -249,26 +258,37 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
         oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
       }
-      // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
+      const uint32_t qcol = tmem + lrow + Gm::Q_COL + grp * PC, ocol = tmem + lrow + Gm::DO_COL + grp * PC;
+      // PC packed columns (4 .. 32) in pieces of 16, 8 and 4
 #pragma unroll
-      for (int c = 0; c + 16 <= HALF / 2; c += 16) {
-        uint32_t t16[16];
+      for (int c = 0; c + 16 <= PC; c += 16) {
+        uint32_t t[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t16[i] = qa[c + i];
-        tmem_st16(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t16);
+        for (int i = 0; i < 16; ++i) t[i] = qa[c + i];
+        tmem_st16(qcol + c, t);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t16[i] = oa[c + i];
-        tmem_st16(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t16);
+        for (int i = 0; i < 16; ++i) t[i] = oa[c + i];
+        tmem_st16(ocol + c, t);
       }
-      if constexpr ((HALF / 2) % 16 == 8) {
-        constexpr int c = HALF / 2 - 8;
-        uint32_t t8[8];
+      if constexpr (PC % 16 >= 8) {
+        constexpr int c = PC / 16 * 16;
+        uint32_t t[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t8[i] = qa[c + i];
-        tmem_st8(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t8);
+        for (int i = 0; i < 8; ++i) t[i] = qa[c + i];
+        tmem_st8(qcol + c, t);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t8[i] = oa[c + i];
-        tmem_st8(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t8);
+        for (int i = 0; i < 8; ++i) t[i] = oa[c + i];
+        tmem_st8(ocol + c, t);
+      }
+      if constexpr (PC % 8 == 4) {
+        constexpr int c = PC / 8 * 8;
+        uint32_t t[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i] = qa[c + i];
+        tmem_st4(qcol + c, t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i] = oa[c + i];
+        tmem_st4(ocol + c, t);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -284,26 +304,31 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       mbar_wait(smem_u32(&bar_dpfull[buf]), (j / NDP) & 1, g, kDevTimeoutBase + 71);
       __syncwarp();
       tc_fence_after_sync();
-      const int kc0 = j * BK + half * 32;  // first key of this thread's columns
+      const int kc0 = j * BK + grp * KC;  // first key of this thread's columns
       const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
-      const uint32_t dcol = tmem + lrow + Gm::DP_COL + buf * BK + half * 32;
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lrow + Gm::S_COL + half * 32, sr);
-      tmem_ld32(dcol, dr);
+      const uint32_t dcol = tmem + lrow + Gm::DP_COL + buf * BK + grp * KC;
+      uint32_t sr[KC], dr[KC];
+      if constexpr (KC == 32) {
+        tmem_ld32(tmem + lrow + Gm::S_COL + grp * KC, sr);
+        tmem_ld32(dcol, dr);
+      } else {
+        tmem_ld16(tmem + lrow + Gm::S_COL + grp * KC, sr);
+        tmem_ld16(dcol, dr);
+      }
       tmem_ld_wait(sr);
       reg_fence(dr);
       // S(j) is in registers: the S warp may overwrite the buffer
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_sfree));
-      uint32_t pk[16];
-      // NPOLY of the 16 pairs, spread evenly, use the polynomial
+      uint32_t pk[KC / 2];
+      // NPOLY of the KC/2 pairs, spread evenly, use the polynomial
       auto ds_tile = [&](auto npoly_tag) {
-        constexpr int NPOLY = decltype(npoly_tag)::value;
+        constexpr int NPOLY = decltype(npoly_tag)::value * KC / 32;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < KC / 2; ++i) {
           float x0, x1, p0, p1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, nlse2), x0, x1);
-          if ((i + 1) * NPOLY / 16 > i * NPOLY / 16) {
+          if ((i + 1) * NPOLY / (KC / 2) > i * NPOLY / (KC / 2)) {
             ex2_poly2(x0, x1, p0, p1);
           } else {
             p0 = ex2_approx(x0);
@@ -319,13 +344,16 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
           pk[i] = E::pack(ds0, ds1);
         }
       };
-      if (quad == 1)  // sub-partition of the S / dP warp (9)
+      if (quad == 1)  // sub-partition of the S warp
         ds_tile(std::integral_constant<int, Gm::POLY_Q1>{});
-      else if (quad == 2)  // sub-partition of the dQ warp (10)
+      else if (quad == 2)  // sub-partition of the dQ / dP warp
         ds_tile(std::integral_constant<int, Gm::POLY_Q2>{});
       else
         ds_tile(std::integral_constant<int, 0>{});
-      tmem_st16(dcol, pk);
+      if constexpr (KC == 32)
+        tmem_st16(dcol, pk);
+      else
+        tmem_st8(dcol, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_dsready[buf]));
@@ -335,7 +363,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     tc_fence_after_sync();
     typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
 #pragma unroll 1
-    for (int c = half; c < D / 32; c += 2) {
+    for (int c = grp; c < D / 32; c += NG) {
       uint32_t rr[32];
       tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
       tmem_ld_wait(rr);
