@@ -73,6 +73,8 @@ attn_status_t check_common(int B, int Hq, int Lq, int D, attn_dtype_t dtype) {
   // grid limits: B*H CTAs along x, 64-row tiles along y
   if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if ((Lq + 63) / 64 > 65535) return ATTN_ERR_UNSUPPORTED;
+  // work items of the persistent dQ kernel (128-row query tiles x heads)
+  if (static_cast<long long>(B) * Hq * ((Lq + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 

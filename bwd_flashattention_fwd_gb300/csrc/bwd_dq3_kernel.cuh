@@ -7,7 +7,7 @@
 //
 // Shared-memory bandwidth (128 B per clock per SM) is what limits an MMA
 // whose two operands both come from shared memory at N = 64.  Q and dO do not
-// change over the CTA's key loop, so the row threads copy them once into
+// change over a query tile's key loop, so the row threads copy them into
 // tensor memory and every MMA reads its A operand from there: S = Q K^T and
 // dP = dO V^T read only the K / V tile from shared memory, dQ += dS K reads dS
 // from tensor memory.  Tensor memory (512 columns): dQ (D), Q and dO (D/2
@@ -22,15 +22,23 @@
 //     j mod 3, behind the MMA that reads dS(j) from it; three buffers keep
 //     dP two tiles ahead of the row threads.
 //
+// Persistent: one CTA per SM walks a list of (query tile, head) work items,
+// heaviest query tiles first, dealt to the CTAs in alternating (snake) order
+// so every CTA gets a similar amount of work.  While a CTA works on item i,
+// its producer warp prefetches item i+1's Q and dO tiles into shared memory
+// with TMA, so starting the next item costs a shared-to-tensor-memory copy
+// instead of a global-memory round trip.  Barrier phases count key tiles and
+// items over the CTA's whole life.
+//
 // Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each 64-key
 // tile, and copies D/2 columns of its rows of Q and dO into tensor memory;
-// warp 8 TMA producer (K_j and V_j together into one ring stage); warp 9
-// issues S = Q K^T and owns the TMEM allocation; warp 10 issues dQ += dS K
-// and dP = dO V^T.
-// MMA issue competes with MUFU instructions issued on the same SM
-// sub-partition, so the row warps on sub-partitions 1 and 2 evaluate part of
-// their exponentials with a polynomial on the FMA pipe (ex2_poly2).
+// warp 8 TMA producer (Q/dO tiles, and K_j and V_j together into one ring
+// stage); warp 9 issues S = Q K^T and owns the TMEM allocation; warp 10
+// issues dQ += dS K and dP = dO V^T.  MMA issue competes with MUFU
+// instructions issued on the same SM sub-partition, so the row warps on the
+// dQ warp's sub-partition evaluate part of their exponentials with a
+// polynomial on the FMA pipe (ex2_poly2).
 #pragma once
 
 #include <type_traits>
@@ -45,27 +53,19 @@ struct Dq3Geom {
   static constexpr int BK = 64;
   static constexpr int NCH = n_chunks(D);
   static constexpr int KV_BYTES = NCH * BK * 128;
-  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024;
+  static constexpr int QB_BYTES = NCH * BQ * 128;  // one prefetched Q or dO tile
+  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * QB_BYTES;
   static constexpr int STAGES = AVAIL / (2 * KV_BYTES) > 6 ? 6 : AVAIL / (2 * KV_BYTES);  // K_j + V_j each
-  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * KV_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + 2 * QB_BYTES + STAGES * 2 * KV_BYTES;
   static constexpr int DQ_COL = 0, Q_COL = 128, DO_COL = 192, S_COL = 256, DP_COL = 320;  // dP: 3 x 64
   static constexpr int NDP = 3;  // dP buffers
   static constexpr int TMEM_COLS = 512;
-#ifndef GBATTN_DQ_ROW_WARPS
   static constexpr int NUM_COMPUTE_WARPS = 8;
-#else
-  static constexpr int NUM_COMPUTE_WARPS = GBATTN_DQ_ROW_WARPS;
-#endif
-  static constexpr int NG = NUM_COMPUTE_WARPS / 4;  // row warps per TMEM lane quadrant
-  static constexpr int KC = BK / NG;                 // key columns per row warp
-  static_assert(NUM_COMPUTE_WARPS == 8 || NUM_COMPUTE_WARPS == 16, "row warps");
   static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
   static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
   static constexpr int S_MMA_WARP = NUM_COMPUTE_WARPS + 1;
   static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
-  static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
-  static_assert(STAGES >= NDP + 1, "dP of tile j+3 is issued while K_j is still in use");
   // element pairs (of 16 per thread and key tile) whose exponentials use the
   // polynomial, on the sub-partition of the S warp (1) and of the dQ / dP
   // warp (2)
@@ -80,39 +80,76 @@ struct Dq3Geom {
   static constexpr int POLY_Q2 = GBATTN_DQ_POLY_Q2;
 #endif
   static_assert(POLY_Q1 >= 0 && POLY_Q1 <= 16 && POLY_Q2 >= 0 && POLY_Q2 <= 16, "polynomial share");
+  static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
+  static_assert(STAGES >= NDP + 1, "dP of tile j+3 is issued while K_j is still in use");
 };
+
+// Position in a ring of N slots whose barriers flip phase once per lap:
+// slot index and the parity of the current lap (cheaper than dividing a
+// running tile count).
+template <int N>
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == N) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Work item w of the list (heaviest query tiles first): query tile and
+// (batch, head) index.
+struct Dq3Item {
+  int qt, bh;
+};
+__device__ __forceinline__ Dq3Item dq3_item(int w, int BH, int n_qtiles) {
+  const int t = w / BH;
+  return {n_qtiles - 1 - t, w - t * BH};
+}
+// Item of this CTA's round r (snake order over the CTAs), or -1 past the end.
+__device__ __forceinline__ int dq3_round_item(int r, int n_items) {
+  const int nc = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int w = r * nc + ((r & 1) ? nc - 1 - c : c);
+  return w < n_items ? w : -1;
+}
 
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
-    attn_bwd_dq3_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const void* __restrict__ q, const void* __restrict__ dO, const BwdParams p) {
+    attn_bwd_dq3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const BwdParams p) {
   using Gm = Dq3Geom<D>;
   using E = Elem<BF16>;
-  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NDP = Gm::NDP;
 
   extern __shared__ uint8_t smem_raw[];
-  constexpr int NDP = Gm::NDP;
-  __shared__ uint64_t bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_sfree, bar_dpfull[NDP],
-      bar_dsready[NDP], bar_dqdone;
+  __shared__ uint64_t bar_qbfull, bar_qbfree, bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_sfree,
+      bar_dpfull[NDP], bar_dsready[NDP], bar_dqdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sK0 = sbase;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
+  const uint32_t sQb = sbase;                // prefetched Q tile
+  const uint32_t sDOb = sQb + Gm::QB_BYTES;  // prefetched dO tile
+  const uint32_t sK0 = sDOb + Gm::QB_BYTES;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
 
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq, hq = bh - b * p.Hq;
-  const int hk = hq / p.G;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
-  const int q0 = qt * BQ;
-  const int q_hi = min(q0 + BQ, p.Lq);
-  const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
-  const int n_kv = (kv_end + BK - 1) / BK;
+  const int BH = p.B * p.Hq;
+  const int n_items = p.n_qtiles * BH;
+  // key tiles of query tile qt
+  auto n_kv_of = [&](int qt) {
+    const int q_hi = min(qt * BQ + BQ, p.Lq);
+    const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
+    return (kv_end + BK - 1) / BK;
+  };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    mbar_init(smem_u32(&bar_qbfull), 1);
+    mbar_init(smem_u32(&bar_qbfree), Gm::NCT);
     mbar_init(smem_u32(&bar_qready), Gm::NCT);
     for (int s = 0; s < ST; ++s) {
       mbar_init(smem_u32(&bar_kvfull[s]), 1);
@@ -139,47 +176,90 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   if (warp == Gm::PRODUCER_WARP) {
     // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
     if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
     }
     __syncwarp();
-    const int zkv = b * p.Hkv + hk;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST;
-      if (j >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (j / ST - 1) & 1, g, kDevTimeoutBase + 61);
-      __syncwarp();
-      const uint32_t bar = smem_u32(&bar_kvfull[s]);
-      const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
-      mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
+    auto load_q = [&](int w) {
+      const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
+      mbar_arrive_expect_tx_w(smem_u32(&bar_qbfull), 2 * Gm::QB_BYTES);
       for (int c = 0; c < NCH; ++c) {
-        tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
-        tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
+        tma_load_3d_w(sQb + c * BQ * 128, &tmQ, smem_u32(&bar_qbfull), c * 64, it.qt * BQ, it.bh);
+        tma_load_3d_w(sDOb + c * BQ * 128, &tmdO, smem_u32(&bar_qbfull), c * 64, it.qt * BQ, it.bh);
+      }
+    };
+    RingPos<ST> kv;  // stage of the next key tile
+    bool wrapped = false;  // the ring has been filled once: stages must be freed first
+    int r = 0;
+    int w = dq3_round_item(0, n_items);
+    if (w >= 0) load_q(w);
+    for (; w >= 0; ++r) {
+      const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
+      const int b = it.bh / p.Hq, hq = it.bh - b * p.Hq;
+      const int zkv = b * p.Hkv + hq / p.G;
+      const int n_kv = n_kv_of(it.qt);
+      for (int j = 0; j < n_kv; ++j, kv.next()) {
+        const int s = kv.slot;
+        if (kv.slot == 0 && kv.phase == 1) wrapped = true;
+        if (wrapped) mbar_wait(smem_u32(&bar_kvempty[s]), kv.phase ^ 1u, g, kDevTimeoutBase + 61);
+        __syncwarp();
+        const uint32_t bar = smem_u32(&bar_kvfull[s]);
+        const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
+        mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
+        for (int c = 0; c < NCH; ++c) {
+          tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
+          tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
+        }
+      }
+      // The row threads copied this item's Q / dO out of the buffer when the
+      // item started: prefetch the next item's.
+      w = dq3_round_item(r + 1, n_items);
+      if (w >= 0) {
+        mbar_wait(smem_u32(&bar_qbfree), r & 1, g, kDevTimeoutBase + 72);
+        __syncwarp();
+        load_q(w);
       }
     }
-    for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_kvfull[j % ST]), (j / ST) & 1, p.limit_ns);
+    // the last ST issued stages (fewer if the ring never wrapped)
+    for (int u = 0; u < ST; ++u) {
+      kv.slot = kv.slot == 0 ? ST - 1 : kv.slot - 1;
+      if (kv.slot == ST - 1) {
+        if (!wrapped && kv.phase == 0) break;  // before the first stage issued
+        kv.phase ^= 1u;
+      }
+      mbar_wait_drain(smem_u32(&bar_kvfull[kv.slot]), kv.phase, p.limit_ns);
+    }
     __syncwarp();
   } else if (warp == Gm::S_MMA_WARP) {
     // ---------------- S = Q K^T issuer (A operand Q from tensor memory) ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BK, BF16, false, false);
     const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
-    mbar_wait(smem_u32(&bar_qready), 0, g, kDevTimeoutBase + 63);
-    __syncwarp();
-    tc_fence_after_sync();
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST;
-      // every row thread has loaded S(j-1) from the buffer
-      if (j >= 1) mbar_wait(smem_u32(&bar_sfree), (j - 1) & 1, g, kDevTimeoutBase + 64);
-      mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 65);
-      __syncwarp();
-      tc_fence_after_sync();
+    RingPos<ST> kv;       // stage of the next key tile
+    uint32_t sphase = 0;  // parity of the S buffer's next use
+    bool first = true;
+    for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
+      const int n_kv = n_kv_of(dq3_item(w, BH, p.n_qtiles).qt);
+      // this item's Q is in tensor memory
+      mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 63);
+      for (int j = 0; j < n_kv; ++j, kv.next()) {
+        const int s = kv.slot;
+        // every row thread has loaded the previous S from the buffer
+        if (!first) mbar_wait(smem_u32(&bar_sfree), sphase ^ 1u, g, kDevTimeoutBase + 64);
+        first = false;
+        sphase ^= 1u;
+        mbar_wait(smem_u32(&bar_kvfull[s]), kv.phase, g, kDevTimeoutBase + 65);
+        __syncwarp();
+        tc_fence_after_sync();
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ko = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-        mma_ts_w(tmem + Gm::S_COL, tmem + Gm::Q_COL + kk * 8, sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+          mma_ts_w(tmem + Gm::S_COL, tmem + Gm::Q_COL + kk * 8, sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(smem_u32(&bar_sfull));
+        mma_commit_w(smem_u32(&bar_kvempty[s]));
       }
-      mma_commit_w(smem_u32(&bar_sfull));
-      mma_commit_w(smem_u32(&bar_kvempty[s]));
     }
     __syncwarp();
   } else if (warp == Gm::DQ_MMA_WARP) {
@@ -188,13 +268,14 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
     const uint64_t dVk = make_sdesc_sw128(sK0 + Gm::KV_BYTES, 16, 1024);  // V stage 0, K-major
     const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);           // K stage 0, MN-major
-    mbar_wait(smem_u32(&bar_qready), 0, g, kDevTimeoutBase + 66);
-    __syncwarp();
-    tc_fence_after_sync();
-    auto issue_dp = [&](int j) {
-      const int s = j % ST, buf = j % NDP;
-      mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 67);
+    RingPos<ST> kv, kv_dp;  // stages of the next dQ and the next dP key tile
+    RingPos<NDP> db, db_dp;  // dP buffers of the next dQ and the next dP
+    // dP of the next key tile to load into its dP buffer
+    auto issue_dp = [&]() {
+      const int s = kv_dp.slot, buf = db_dp.slot;
+      mbar_wait(smem_u32(&bar_kvfull[s]), kv_dp.phase, g, kDevTimeoutBase + 67);
       __syncwarp();
+      tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t vo = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
@@ -202,172 +283,172 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
                  kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_dpfull[buf]));
+      kv_dp.next();
+      db_dp.next();
     };
-    for (int j = 0; j < NDP && j < n_kv; ++j) issue_dp(j);
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST, buf = j % NDP;
-      mbar_wait(smem_u32(&bar_dsready[buf]), (j / NDP) & 1, g, kDevTimeoutBase + 68);
-      __syncwarp();
-      tc_fence_after_sync();
-      // A operand: 16 keys per K step; keys KC*h..KC*h+KC-1 of row-warp
-      // group h sit as pairs in columns KC*h..KC*h+KC/2-1 of the dP buffer.
+    for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
+      const int n_kv = n_kv_of(dq3_item(w, BH, p.n_qtiles).qt);
+      // this item's dO is in tensor memory
+      mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 66);
+      for (int j = 0; j < NDP && j < n_kv; ++j) issue_dp();
+      for (int j = 0; j < n_kv; ++j, kv.next(), db.next()) {
+        const int s = kv.slot, buf = db.slot;
+        mbar_wait(smem_u32(&bar_dsready[buf]), db.phase, g, kDevTimeoutBase + 68);
+        __syncwarp();
+        tc_fence_after_sync();
+        // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
+        // pairs in columns 32h..32h+15 of the dP buffer.
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk) {
-        const uint32_t acol = Gm::DP_COL + buf * BK + (16 * kk / Gm::KC) * Gm::KC + (16 * kk % Gm::KC) / 2;
-        mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t acol = Gm::DP_COL + buf * BK + (kk >> 1) * 32 + (kk & 1) * 8;
+          mma_ts_w(tmem + Gm::DQ_COL, tmem + acol, sdesc_add(dKm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_DQ,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        // this warp's dP(t) and dQ(t) are its last reads of the stage
+        mma_commit_w(smem_u32(&bar_kvempty[s]));
+        // dP three tiles ahead overwrites the buffer behind dQ, which reads its dS
+        if (j + NDP < n_kv) issue_dp();
       }
-      // this warp's dP(j) and dQ(j) are its last reads of the stage
-      mma_commit_w(smem_u32(&bar_kvempty[s]));
-      // dP(j+3) overwrites the buffer behind dQ(j), which reads its dS
-      if (j + NDP < n_kv) issue_dp(j + NDP);
+      // Every S MMA of the item completed before its last dS was ready, so
+      // this commit covers all of the item's MMAs.
+      mma_commit_w(smem_u32(&bar_dqdone));
     }
-    // Every S MMA completed before the last dS was ready, so this commit
-    // covers all MMAs of the CTA.
-    mma_commit_w(smem_u32(&bar_dqdone));
-    mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
     __syncwarp();
   } else {
     // ---------------- row threads ----------------
-    constexpr int NG = Gm::NG, KC = Gm::KC;
-    const int quad = warp & 3;  // TMEM lane quadrant (query rows)
-    const int grp = warp >> 2;  // key columns KC*grp .. +KC-1 of each tile
-    const int r = quad * 32 + lane;
-    const int qi = q0 + r;
+    const int quad = warp & 3;   // TMEM lane quadrant (query rows)
+    const int half = warp >> 2;  // key columns 32*half .. +31 of each tile
+    const int rr_ = quad * 32 + lane;  // row of the query tile
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
-    // Q and dO rows into tensor memory: this warp copies columns
-    // [grp*D/NG, (grp+1)*D/NG) of its 32 rows (zeros past Lq), as 16-bit pairs.
-    {
-      constexpr int EW = D / NG;   // elements per thread per tensor
-      constexpr int NV = EW / 8;   // 16-byte loads per thread per tensor
-      constexpr int PC = EW / 2;   // packed columns per thread per tensor
-      const uint4* qrow =
-          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(q) + row * D + grp * EW);
-      const uint4* orow =
-          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(dO) + row * D + grp * EW);
-      uint32_t qa[PC], oa[PC];
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    constexpr int HALF = D / 2;  // elements of a Q / dO row this thread copies
+    uint32_t sphase = 0;  // parity of the S buffer's next fill
+    RingPos<NDP> db;      // dP buffer of the next key tile
+    for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
+      const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
+      const int q0 = it.qt * BQ;
+      const int qi = q0 + rr_;
+      const int n_kv = n_kv_of(it.qt);
+      const size_t row = static_cast<size_t>(it.bh) * p.Lq + qi;
+      // Q and dO rows from the prefetch buffer (TMA layout: 64-column chunks
+      // of 128-byte rows, 16-byte units swizzled by row % 8; zeros past Lq
+      // and past D) into tensor memory: this warp copies elements
+      // [half*D/2, (half+1)*D/2) of its 32 rows as 16-bit pairs.  The
+      // previous item's MMAs are complete: its dQ was read out after the
+      // item's final commit.
+      mbar_wait(smem_u32(&bar_qbfull), r & 1, g, kDevTimeoutBase + 73);
+      {
+        uint32_t qa[HALF / 2], oa[HALF / 2];
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        uint4 x = make_uint4(0u, 0u, 0u, 0u), y = make_uint4(0u, 0u, 0u, 0u);
-        if (qi < p.Lq) {
-          x = qrow[v];
-          y = orow[v];
+        for (int v = 0; v < HALF / 8; ++v) {
+          const int e = half * HALF + 8 * v;  // first element of this 16-byte unit
+          const uint32_t off = (e / 64) * (BQ * 128) + rr_ * 128 + ((((e % 64) / 8) ^ (rr_ & 7)) * 16);
+          const uint4 x = ld_shared_v4(sQb + off), y = ld_shared_v4(sDOb + off);
+          qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
+          oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
         }
-        qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
-        oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
+        // the producer may refill the buffer once every row thread has read it
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bar_qbfree));
+        // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
+#pragma unroll
+        for (int c = 0; c + 16 <= HALF / 2; c += 16) {
+          uint32_t t16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t16[i] = qa[c + i];
+          tmem_st16(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t16[i] = oa[c + i];
+          tmem_st16(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t16);
+        }
+        if constexpr ((HALF / 2) % 16 == 8) {
+          constexpr int c = HALF / 2 - 8;
+          uint32_t t8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = qa[c + i];
+          tmem_st8(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = oa[c + i];
+          tmem_st8(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t8);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(smem_u32(&bar_qready));
       }
-      const uint32_t qcol = tmem + lrow + Gm::Q_COL + grp * PC, ocol = tmem + lrow + Gm::DO_COL + grp * PC;
-      // PC packed columns (4 .. 32) in pieces of 16, 8 and 4
+      const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
+      const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
+      const uint64_t nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
+      const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
+      for (int j = 0; j < n_kv; ++j, db.next()) {
+        const int buf = db.slot;
+        mbar_wait(smem_u32(&bar_sfull), sphase, g, kDevTimeoutBase + 69);
+        sphase ^= 1u;
+        mbar_wait(smem_u32(&bar_dpfull[buf]), db.phase, g, kDevTimeoutBase + 71);
+        __syncwarp();
+        tc_fence_after_sync();
+        const int kc0 = j * BK + half * 32;  // first key of this thread's columns
+        const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
+        const uint32_t dcol = tmem + lrow + Gm::DP_COL + buf * BK + half * 32;
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lrow + Gm::S_COL + half * 32, sr);
+        tmem_ld32(dcol, dr);
+        tmem_ld_wait(sr);
+        reg_fence(dr);
+        // S(t) is in registers: the S warp may overwrite the buffer
+        tc_fence_before_sync();
+        mbar_arrive(smem_u32(&bar_sfree));
+        uint32_t pk[16];
+        // NPOLY of the 16 pairs, spread evenly, use the polynomial
+        auto ds_tile = [&](auto npoly_tag) {
+          constexpr int NPOLY = decltype(npoly_tag)::value;
 #pragma unroll
-      for (int c = 0; c + 16 <= PC; c += 16) {
-        uint32_t t[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) t[i] = qa[c + i];
-        tmem_st16(qcol + c, t);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) t[i] = oa[c + i];
-        tmem_st16(ocol + c, t);
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1, p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, nlse2), x0,
+                      x1);
+            if ((i + 1) * NPOLY / 16 > i * NPOLY / 16) {
+              ex2_poly2(x0, x1, p0, p1);
+            } else {
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
+            if (need_mask) {
+              if (kc0 + 2 * i > lim) p0 = 0.f;
+              if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
+            }
+            const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])), dlt2);
+            float ds0, ds1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
+            pk[i] = E::pack(ds0, ds1);
+          }
+        };
+        if (quad == 1)  // sub-partition of the S warp
+          ds_tile(std::integral_constant<int, Gm::POLY_Q1>{});
+        else if (quad == 2)  // sub-partition of the dQ / dP warp
+          ds_tile(std::integral_constant<int, Gm::POLY_Q2>{});
+        else
+          ds_tile(std::integral_constant<int, 0>{});
+        tmem_st16(dcol, pk);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(smem_u32(&bar_dsready[buf]));
       }
-      if constexpr (PC % 16 >= 8) {
-        constexpr int c = PC / 16 * 16;
-        uint32_t t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = qa[c + i];
-        tmem_st8(qcol + c, t);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = oa[c + i];
-        tmem_st8(ocol + c, t);
-      }
-      if constexpr (PC % 8 == 4) {
-        constexpr int c = PC / 8 * 8;
-        uint32_t t[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) t[i] = qa[c + i];
-        tmem_st4(qcol + c, t);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) t[i] = oa[c + i];
-        tmem_st4(ocol + c, t);
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_qready));
-    }
-    const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
-    const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
-    const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
-    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
-    for (int j = 0; j < n_kv; ++j) {
-      const int buf = j % NDP;
-      mbar_wait(smem_u32(&bar_sfull), j & 1, g, kDevTimeoutBase + 69);
-      mbar_wait(smem_u32(&bar_dpfull[buf]), (j / NDP) & 1, g, kDevTimeoutBase + 71);
+      // epilogue of the item: every MMA of the item is complete
+      mbar_wait(smem_u32(&bar_dqdone), r & 1, g, kDevTimeoutBase + 70);
       __syncwarp();
       tc_fence_after_sync();
-      const int kc0 = j * BK + grp * KC;  // first key of this thread's columns
-      const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
-      const uint32_t dcol = tmem + lrow + Gm::DP_COL + buf * BK + grp * KC;
-      uint32_t sr[KC], dr[KC];
-      if constexpr (KC == 32) {
-        tmem_ld32(tmem + lrow + Gm::S_COL + grp * KC, sr);
-        tmem_ld32(dcol, dr);
-      } else {
-        tmem_ld16(tmem + lrow + Gm::S_COL + grp * KC, sr);
-        tmem_ld16(dcol, dr);
-      }
-      tmem_ld_wait(sr);
-      reg_fence(dr);
-      // S(j) is in registers: the S warp may overwrite the buffer
-      tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_sfree));
-      uint32_t pk[KC / 2];
-      // NPOLY of the KC/2 pairs, spread evenly, use the polynomial
-      auto ds_tile = [&](auto npoly_tag) {
-        constexpr int NPOLY = decltype(npoly_tag)::value * KC / 32;
-#pragma unroll
-        for (int i = 0; i < KC / 2; ++i) {
-          float x0, x1, p0, p1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, nlse2), x0, x1);
-          if ((i + 1) * NPOLY / (KC / 2) > i * NPOLY / (KC / 2)) {
-            ex2_poly2(x0, x1, p0, p1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-          }
-          if (need_mask) {
-            if (kc0 + 2 * i > lim) p0 = 0.f;
-            if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
-          }
-          const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])), dlt2);
-          float ds0, ds1;
-          f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
-          pk[i] = E::pack(ds0, ds1);
-        }
-      };
-      if (quad == 1)  // sub-partition of the S warp
-        ds_tile(std::integral_constant<int, Gm::POLY_Q1>{});
-      else if (quad == 2)  // sub-partition of the dQ / dP warp
-        ds_tile(std::integral_constant<int, Gm::POLY_Q2>{});
-      else
-        ds_tile(std::integral_constant<int, 0>{});
-      if constexpr (KC == 32)
-        tmem_st16(dcol, pk);
-      else
-        tmem_st8(dcol, pk);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_dsready[buf]));
-    }
-    mbar_wait(smem_u32(&bar_dqdone), 0, g, kDevTimeoutBase + 70);
-    __syncwarp();
-    tc_fence_after_sync();
-    typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
+      typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
 #pragma unroll 1
-    for (int c = grp; c < D / 32; c += NG) {
-      uint32_t rr[32];
-      tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
-      tmem_ld_wait(rr);
-      if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+      for (int c = half; c < D / 32; c += 2) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+      }
+      // The next item's first dQ MMA overwrites these columns; it is issued
+      // after this thread's next dS arrival, which follows these loads.
+      tc_fence_before_sync();
     }
   }
 

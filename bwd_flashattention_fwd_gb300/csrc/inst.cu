@@ -160,17 +160,21 @@ template <bool BF16, bool CAUSAL>
 int dq3_impl(const AttnArgs& a) {
   constexpr int DD = kD <= 128 ? kD : 128;
   using Gm = Dq3Geom<DD>;
-  CUtensorMap tk, tv;
-  if (!make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
-  const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  // persistent: one CTA per SM (fewer when there are fewer work items)
+  const long long n_items = static_cast<long long>(p.n_qtiles) * a.B * a.Hq;
+  const int sms = a.num_sms > 0 ? a.num_sms : 1;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   auto kern = attn_bwd_dq3_kernel<DD, BF16, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
     return kLaunchCudaError;
-  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tk, tv, a.q, a.dO, p);
+  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tdo, tk, tv, p);
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
