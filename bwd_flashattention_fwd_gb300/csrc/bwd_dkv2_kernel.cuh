@@ -144,12 +144,13 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     __syncwarp();
     mbar_arrive_expect_tx_w(smem_u32(&bar_v), Gm::V_BYTES);
     for (int c = 0; c < NCH; ++c) tma_load_3d_w(sV + c * BK * 128, &tmV, smem_u32(&bar_v), c * 64, k0, bhk);
-    for (int it = 0; it < n_iter; ++it) {
-      const int s = it % ST, u = it / ST;
-      if (u > 0) mbar_wait(smem_u32(&bar_stempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 81);
+    RingPos<ST> st;                  // stage of iteration it
+    int gi = 0, qtile = qt_start;    // query head in the group and query tile of iteration it
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot;
+      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 81);
       __syncwarp();
-      const int gi = it / nq;
-      const int q0 = (qt_start + (it - gi * nq)) * BQ;
+      const int q0 = qtile * BQ;
       const int zq = b * p.Hq + hk * p.G + gi;
       mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
       for (int c = 0; c < NCH; ++c) {
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
         dlt_s[s][c] = qi < p.Lq ? p.delta[row] : 0.f;
       }
       mbar_arrive(smem_u32(&bar_stfull[s]));
+      if (++qtile == p.n_qtiles) qtile = qt_start, ++gi;
     }
     mbar_wait_drain(smem_u32(&bar_v), 0, p.limit_ns);
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
@@ -176,11 +178,12 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     mbar_wait(smem_u32(&bar_kready), 0, g, kDevTimeoutBase + 82);
     __syncwarp();
     tc_fence_after_sync();
-    for (int it = 0; it < n_iter; ++it) {
-      const int s = it % ST;
+    RingPos<ST> st;  // stage of iteration it
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot;
       // every row thread has loaded S^T(it-1) from the buffer
       if (it >= 1) mbar_wait(smem_u32(&bar_sfree), (it - 1) & 1, g, kDevTimeoutBase + 83);
-      mbar_wait(smem_u32(&bar_stfull[s]), (it / ST) & 1, g, kDevTimeoutBase + 84);
+      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 84);
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -202,9 +205,10 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     const uint64_t dOm = make_sdesc_sw128(sdO0, BQ * 128, 1024);    // dO stage 0, MN-major
     mbar_wait(smem_u32(&bar_v), 0, g, kDevTimeoutBase + 85);
     __syncwarp();
+    RingPos<ST> st, st_dp;  // stages of the next dV / dK and of the next dP^T iteration
     auto issue_dp = [&](int it) {
-      const int s = it % ST, buf = it & 1;
-      mbar_wait(smem_u32(&bar_stfull[s]), (it / ST) & 1, g, kDevTimeoutBase + 86);
+      const int s = st_dp.slot, buf = it & 1;
+      mbar_wait(smem_u32(&bar_stfull[s]), st_dp.phase, g, kDevTimeoutBase + 86);
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -214,10 +218,11 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
         mma_ss_w(tmem + Gm::DPT_COL + buf * BQ, sdesc_add(dV, vo), sdesc_add(dOk, qo), IDESC_S, kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_dpfull[buf]));
+      st_dp.next();
     };
     for (int it = 0; it < 2 && it < n_iter; ++it) issue_dp(it);
-    for (int it = 0; it < n_iter; ++it) {
-      const int s = it % ST, buf = it & 1;
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot, buf = it & 1;
       mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 87);
       __syncwarp();
       tc_fence_after_sync();
@@ -285,11 +290,13 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_kready));
     }
-    for (int it = 0; it < n_iter; ++it) {
-      const int s = it % ST, buf = it & 1;
-      const int gi = it / nq;
-      const int q0 = (qt_start + (it - gi * nq)) * BQ;
-      mbar_wait(smem_u32(&bar_stfull[s]), (it / ST) & 1, g, kDevTimeoutBase + 88);
+    RingPos<ST> st;             // stage of iteration it
+    int qtile = qt_start;       // query tile of iteration it
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot, buf = it & 1;
+      const int q0 = qtile * BQ;
+      if (++qtile == p.n_qtiles) qtile = qt_start;
+      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 88);
       mbar_wait(smem_u32(&bar_sfull), it & 1, g, kDevTimeoutBase + 89);
       mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 90);
       __syncwarp();

@@ -84,21 +84,6 @@ struct Dq3Geom {
   static_assert(STAGES >= NDP + 1, "dP of tile j+3 is issued while K_j is still in use");
 };
 
-// Position in a ring of N slots whose barriers flip phase once per lap:
-// slot index and the parity of the current lap (cheaper than dividing a
-// running tile count).
-template <int N>
-struct RingPos {
-  int slot = 0;
-  uint32_t phase = 0;
-  __device__ __forceinline__ void next() {
-    if (++slot == N) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 // Work item w of the list (heaviest query tiles first): query tile and
 // (batch, head) index.
 struct Dq3Item {

@@ -128,9 +128,10 @@ __global__ void __launch_bounds__(352, 1)
     for (int t = 0; t < 2; ++t)
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sQ + t * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0 + t * BQ, bh);
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST;
-      if (j >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (j / ST - 1) & 1, g, kDevTimeoutBase + 31);
+    RingPos<ST> st;  // stage of key tile j
+    for (int j = 0; j < n_kv; ++j, st.next()) {
+      const int s = st.slot;
+      if (j >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 31);
       __syncwarp();
       const uint32_t bar = smem_u32(&bar_kvfull[s]);
       const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
@@ -154,10 +155,12 @@ __global__ void __launch_bounds__(352, 1)
     mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 33);
     __syncwarp();
     tc_fence_after_sync();
+    RingPos<ST> st_s, st_pv;  // stages of the next S_t and of the next P_t V
     // S_t of key tile j; the wait on the stage also covers V_j for P_t V_j
     auto issue_s = [&](int j) {
-      const int s = j % ST;
-      mbar_wait(smem_u32(&bar_kvfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 34);
+      const int s = st_s.slot;
+      mbar_wait(smem_u32(&bar_kvfull[s]), st_s.phase, g, kDevTimeoutBase + 34);
+      st_s.next();
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -168,7 +171,8 @@ __global__ void __launch_bounds__(352, 1)
       mma_commit_w(smem_u32(&bar_sfull[t][j & 1]));
     };
     auto issue_pv = [&](int j) {
-      const int s = j % ST;
+      const int s = st_pv.slot;
+      st_pv.next();
       mbar_wait(smem_u32(&bar_pready[t][j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 35);
       __syncwarp();
       tc_fence_after_sync();

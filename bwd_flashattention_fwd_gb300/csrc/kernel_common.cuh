@@ -94,4 +94,19 @@ __device__ __forceinline__ void store_row32(void* dst, const uint32_t (&r)[32], 
   }
 }
 
+// Position in a ring of N slots whose barriers flip phase once per lap:
+// slot index and the parity of the current lap (cheaper than dividing a
+// running tile count).
+template <int N>
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == N) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 }  // namespace gbattn
