@@ -32,6 +32,13 @@
 // The softmax works on packed pairs (.f32x2 fma / add) and takes the row
 // maximum with three-input max, which keeps its instruction count, and so its
 // share of the issue slots of the sub-partitions the MMA warps run on, low.
+//
+// Persistent: one CTA per SM walks a list of (256-row query pair, head) work
+// items, heaviest first, dealt to the CTAs in alternating (snake) order.  As
+// soon as an item's last S MMAs have completed, the producer loads the next
+// item's Q into the (then unused) Q buffer, and the MMA warps compute the next
+// item's first S tiles while the softmax warps write out the current item's O
+// and lse.  Barrier phases count key tiles and items over the CTA's life.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -67,8 +74,8 @@ __global__ void __launch_bounds__(352, 1)
   constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2][2], bar_pready[2][2], bar_odone[2],
-      bar_done;
+  __shared__ uint64_t bar_q, bar_qfree, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2][2], bar_pready[2][2],
+      bar_odone[2], bar_done;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -77,19 +84,29 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t sQ = sbase;  // tile t at sQ + t * Q_BYTES
   const uint32_t sK0 = sQ + 2 * Gm::Q_BYTES;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
 
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq, hq = bh - b * p.Hq;
-  const int hk = hq / p.G;
-  const int pt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest first; n_qtiles counts 256-row pairs
-  const int q0 = pt * 2 * BQ;
-  const int q_hi = min(q0 + 2 * BQ, p.Lq);
-  const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
-  const int n_kv = (kv_end + BK - 1) / BK;
+  // work items: w -> (query pair pt, head bh), heaviest query pairs first;
+  // n_qtiles counts 256-row pairs
+  const int BH = p.B * p.Hq;
+  const int n_items = p.n_qtiles * BH;
+  auto item_pt = [&](int w) { return p.n_qtiles - 1 - w / BH; };
+  auto item_bh = [&](int w) { return w - (w / BH) * BH; };
+  // item of this CTA's round r (snake order over the CTAs), or -1
+  auto round_item = [&](int r) {
+    const int nc = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int w = r * nc + ((r & 1) ? nc - 1 - c : c);
+    return w < n_items ? w : -1;
+  };
+  auto n_kv_of = [&](int pt) {
+    const int q_hi = min(pt * 2 * BQ + 2 * BQ, p.Lq);
+    const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
+    return (kv_end + BK - 1) / BK;
+  };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
+    mbar_init(smem_u32(&bar_qfree), 2);  // one commit per MMA warp after its item's last S
     // A stage (K_j, V_j) is free once both tiles' MMAs that read it
     // completed: one commit from each MMA warp, after its P_t V_j.
     for (int s = 0; s < ST; ++s) {
@@ -123,26 +140,40 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&tmV);
     }
     __syncwarp();
-    const int zkv = b * p.Hkv + hk;
-    mbar_arrive_expect_tx_w(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
-    for (int t = 0; t < 2; ++t)
-      for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sQ + t * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0 + t * BQ, bh);
-    RingPos<ST> st;  // stage of key tile j
-    for (int j = 0; j < n_kv; ++j, st.next()) {
-      const int s = st.slot;
-      if (j >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 31);
+    RingPos<ST> st;  // stage of the next key tile
+    int issued = 0;  // key tiles issued (all items)
+    for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
+      const int pt = item_pt(w), bh = item_bh(w);
+      const int b = bh / p.Hq, hq = bh - b * p.Hq;
+      const int zkv = b * p.Hkv + hq / p.G;
+      const int q0 = pt * 2 * BQ;
+      const int n_kv = n_kv_of(pt);
+      // the previous item's S MMAs, the only readers of Q, are complete
+      if (r > 0) mbar_wait(smem_u32(&bar_qfree), (r - 1) & 1, g, kDevTimeoutBase + 30);
       __syncwarp();
-      const uint32_t bar = smem_u32(&bar_kvfull[s]);
-      const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
-      mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
-        tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
+      mbar_arrive_expect_tx_w(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < NCH; ++c)
+          tma_load_3d_w(sQ + t * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0 + t * BQ, bh);
+      for (int j = 0; j < n_kv; ++j, st.next(), ++issued) {
+        const int s = st.slot;
+        if (issued >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 31);
+        __syncwarp();
+        const uint32_t bar = smem_u32(&bar_kvfull[s]);
+        const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
+        mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
+        for (int c = 0; c < NCH; ++c) {
+          tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
+          tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
+        }
       }
     }
-    for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_kvfull[j % ST]), (j / ST) & 1, p.limit_ns);
+    // the last ST issued stages
+    for (int u = 0; u < ST && u < issued; ++u) {
+      if (st.slot == 0) st.phase ^= 1u;
+      st.slot = (st.slot == 0 ? ST : st.slot) - 1;
+      mbar_wait_drain(smem_u32(&bar_kvfull[st.slot]), st.phase, p.limit_ns);
+    }
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
     // ---------------- MMA issuers: warp 9 for tile 0, warp 10 for tile 1 ----------------
@@ -152,33 +183,35 @@ __global__ void __launch_bounds__(352, 1)
     const uint64_t dQd = make_sdesc_sw128(sQ + t * Gm::Q_BYTES, 16, 1024);  // this tile's Q, K-major
     const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);                         // K stage 0, K-major
     const uint64_t dVm = make_sdesc_sw128(sK0 + Gm::KV_BYTES, BK * 128, 1024);    // V stage 0, MN-major
-    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 33);
-    __syncwarp();
-    tc_fence_after_sync();
     RingPos<ST> st_s, st_pv;  // stages of the next S_t and of the next P_t V
-    // S_t of key tile j; the wait on the stage also covers V_j for P_t V_j
-    auto issue_s = [&](int j) {
-      const int s = st_s.slot;
+    int ts = 0, tp = 0;       // key tiles (all items) of the next S_t and of the next P_t V
+    // S_t of the next key tile; the wait on the stage also covers V_j for P_t V_j
+    auto issue_s = [&]() {
+      const int s = st_s.slot, bb = ts & 1;
       mbar_wait(smem_u32(&bar_kvfull[s]), st_s.phase, g, kDevTimeoutBase + 34);
       st_s.next();
+      ++ts;
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
         const uint32_t ko = 2 * s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-        mma_ss_w(tmem + Gm::s_col(t, j & 1), sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
+        mma_ss_w(tmem + Gm::s_col(t, bb), sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
       }
-      mma_commit_w(smem_u32(&bar_sfull[t][j & 1]));
+      mma_commit_w(smem_u32(&bar_sfull[t][bb]));
     };
-    auto issue_pv = [&](int j) {
-      const int s = st_pv.slot;
+    // P_t V_j of key tile j of an item with n_kv key tiles
+    auto issue_pv = [&](int j, int n_kv) {
+      const int s = st_pv.slot, bb = tp & 1;
+      const uint32_t ph = (tp >> 1) & 1;
       st_pv.next();
-      mbar_wait(smem_u32(&bar_pready[t][j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 35);
+      ++tp;
+      mbar_wait(smem_u32(&bar_pready[t][bb]), ph, g, kDevTimeoutBase + 35);
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk)
-        mma_ts_w(tmem + Gm::o_col(t), tmem + Gm::s_col(t, j & 1) + kk * 8,
+        mma_ts_w(tmem + Gm::o_col(t), tmem + Gm::s_col(t, bb) + kk * 8,
                  sdesc_add(dVm, 2 * s * Gm::KV_BYTES + kk * 2048), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
       // this thread's S_t(j) and P_t V_j are the last reads of the stage
       mma_commit_w(smem_u32(&bar_kvempty[s]));
@@ -186,120 +219,147 @@ __global__ void __launch_bounds__(352, 1)
       // rescales use the next tile's S barrier, which covers it.
       if (j == n_kv - 2) mma_commit_w(smem_u32(&bar_odone[t]));
     };
-    for (int j = 0; j < 2 && j < n_kv; ++j) issue_s(j);
-    for (int j = 0; j < n_kv; ++j) {
-      issue_pv(j);
-      if (j + 2 < n_kv) issue_s(j + 2);
+    int r = 0;
+    for (int w = round_item(0); w >= 0; w = round_item(++r)) {
+      const int n_kv = n_kv_of(item_pt(w));
+      // this item's Q is in shared memory
+      mbar_wait(smem_u32(&bar_q), r & 1, g, kDevTimeoutBase + 33);
+      __syncwarp();
+      tc_fence_after_sync();
+      for (int j = 0; j < 2 && j < n_kv; ++j) {
+        issue_s();
+        if (j == n_kv - 1) mma_commit_w(smem_u32(&bar_qfree));  // last read of this item's Q
+      }
+      for (int j = 0; j < n_kv; ++j) {
+        issue_pv(j, n_kv);
+        if (j + 2 < n_kv) {
+          issue_s();
+          if (j + 2 == n_kv - 1) mma_commit_w(smem_u32(&bar_qfree));
+        }
+      }
+      mma_commit_w(smem_u32(&bar_done));
     }
-    mma_commit_w(smem_u32(&bar_done));
-    mbar_wait_drain(smem_u32(&bar_done), 0, p.limit_ns);
+    if (r > 0) mbar_wait_drain(smem_u32(&bar_done), (r - 1) & 1, p.limit_ns);
     __syncwarp();
   } else {
     // ---------------- softmax warpgroups ----------------
     const int t = warp >> 2;  // query tile
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;
-    const int q0t = q0 + t * BQ;
-    const int qi = q0t + r;
+    const int rt = quad * 32 + lane;  // row of the query tile
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t o_col = tmem + lrow + Gm::o_col(t);
     const float sl2 = p.scale_log2;
-    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;  // last visible key
-    float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < n_kv; ++j) {
-      const int bb = j & 1;
-      const uint32_t s_col = tmem + lrow + Gm::s_col(t, bb);
-      mbar_wait(smem_u32(&bar_sfull[t][bb]), (j >> 1) & 1, g, kDevTimeoutBase + 37);
-      __syncwarp();
-      tc_fence_after_sync();
-      uint32_t ra[32], rb[32];
-      tmem_ld32(s_col, ra);
-      tmem_ld32(s_col + 32, rb);
-      tmem_ld_wait(ra);
-      reg_fence(rb);
-      const int k0 = j * BK;
-      if ((CAUSAL && (k0 + BK - 1 > q0t + p.off)) || (k0 + BK > p.Lk)) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (k0 + i > lim) ra[i] = __float_as_uint(-INFINITY);
-          if (k0 + 32 + i > lim) rb[i] = __float_as_uint(-INFINITY);
-        }
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i]));
-#pragma unroll
-      for (int i = 8; i < 32; ++i) mx[i & 7] = fmax3(mx[i & 7], __uint_as_float(ra[i]), __uint_as_float(rb[i]));
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-      const float m_new = fmaxf(m, mt);
-      if (__any_sync(0xffffffffu, m_new > m + Gm::TAU)) {
-        const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
-        m = m_new;
-        l *= alpha;
-        if (j > 0) {
-          // O_t holds P V up to key tile j-1 once that MMA is done.  S_t of
-          // key tile j+1 was issued right after it, so its barrier covers it;
-          // on the last key tile a dedicated commit does.
-          if (j + 1 < n_kv)
-            mbar_wait(smem_u32(&bar_sfull[t][(j + 1) & 1]), ((j + 1) >> 1) & 1, g, kDevTimeoutBase + 39);
-          else
-            mbar_wait(smem_u32(&bar_odone[t]), 0, g, kDevTimeoutBase + 40);
-          __syncwarp();
-          tc_fence_after_sync();
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(o_col + c * 32, rr);
-            tmem_ld_wait(rr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st32(o_col + c * 32, rr);
+    int ts = 0;             // key tiles (all items) seen so far
+    uint32_t odone_ph = 0;  // parity of the next item-end product barrier
+    int r = 0;
+    for (int w = round_item(0); w >= 0; w = round_item(++r)) {
+      const int bh = item_bh(w);
+      const int q0t = item_pt(w) * 2 * BQ + t * BQ;
+      const int qi = q0t + rt;
+      const int n_kv = n_kv_of(item_pt(w));
+      const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;  // last visible key
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_kv; ++j) {
+        const int T = ts + j;
+        const int bb = T & 1;
+        const uint32_t s_col = tmem + lrow + Gm::s_col(t, bb);
+        mbar_wait(smem_u32(&bar_sfull[t][bb]), (T >> 1) & 1, g, kDevTimeoutBase + 37);
+        __syncwarp();
+        tc_fence_after_sync();
+        uint32_t ra[32], rb[32];
+        tmem_ld32(s_col, ra);
+        tmem_ld32(s_col + 32, rb);
+        tmem_ld_wait(ra);
+        reg_fence(rb);
+        const int k0 = j * BK;
+        if ((CAUSAL && (k0 + BK - 1 > q0t + p.off)) || (k0 + BK > p.Lk)) {
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (k0 + i > lim) ra[i] = __float_as_uint(-INFINITY);
+            if (k0 + 32 + i > lim) rb[i] = __float_as_uint(-INFINITY);
           }
         }
+        float mx[8];
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i]));
+  #pragma unroll
+        for (int i = 8; i < 32; ++i) mx[i & 7] = fmax3(mx[i & 7], __uint_as_float(ra[i]), __uint_as_float(rb[i]));
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+        const float m_new = fmaxf(m, mt);
+        if (__any_sync(0xffffffffu, m_new > m + Gm::TAU)) {
+          const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+          m = m_new;
+          l *= alpha;
+          if (j > 0) {
+            // O_t holds P V up to key tile j-1 once that MMA is done.  S_t of
+            // key tile j+1 was issued right after it, so its barrier covers it;
+            // on the last key tile a dedicated commit does.
+            if (j + 1 < n_kv)
+              mbar_wait(smem_u32(&bar_sfull[t][(T + 1) & 1]), ((T + 1) >> 1) & 1, g, kDevTimeoutBase + 39);
+            else
+              mbar_wait(smem_u32(&bar_odone[t]), odone_ph, g, kDevTimeoutBase + 40);
+            __syncwarp();
+            tc_fence_after_sync();
+  #pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t rr[32];
+              tmem_ld32(o_col + c * 32, rr);
+              tmem_ld_wait(rr);
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+              tmem_st32(o_col + c * 32, rr);
+            }
+          }
+        }
+        // P = exp2(S * scale_log2 - m), two elements per packed instruction
+        uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
+        uint32_t pa[16], pb[16];
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m, -m);
+  #pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), sl2x2, nm2), x0, x1);
+          const float a0 = ex2_approx(x0), a1 = ex2_approx(x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])), sl2x2, nm2), x0, x1);
+          const float b0 = ex2_approx(x0), b1 = ex2_approx(x1);
+          sa2 = f2_add(sa2, f2_pack(a0, a1));
+          sb2 = f2_add(sb2, f2_pack(b0, b1));
+          pa[i] = E::pack(a0, a1);
+          pb[i] = E::pack(b0, b1);
+        }
+        {
+          float s0, s1, s2, s3;
+          f2_unpack(sa2, s0, s1);
+          f2_unpack(sb2, s2, s3);
+          l += (s0 + s1) + (s2 + s3);
+        }
+        // P: keys 0..31 -> columns 0..15, keys 32..63 -> columns 16..31 of S_t
+        tmem_st16(s_col, pa);
+        tmem_st16(s_col + 16, pb);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(smem_u32(&bar_pready[t][bb]));
       }
-      // P = exp2(S * scale_log2 - m), two elements per packed instruction
-      uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
-      uint32_t pa[16], pb[16];
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m, -m);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), sl2x2, nm2), x0, x1);
-        const float a0 = ex2_approx(x0), a1 = ex2_approx(x1);
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])), sl2x2, nm2), x0, x1);
-        const float b0 = ex2_approx(x0), b1 = ex2_approx(x1);
-        sa2 = f2_add(sa2, f2_pack(a0, a1));
-        sb2 = f2_add(sb2, f2_pack(b0, b1));
-        pa[i] = E::pack(a0, a1);
-        pb[i] = E::pack(b0, b1);
+      ts += n_kv;
+      if (n_kv >= 2) odone_ph ^= 1u;
+      // ---------------- epilogue ----------------
+      mbar_wait(smem_u32(&bar_done), r & 1, g, kDevTimeoutBase + 38);
+      __syncwarp();
+      tc_fence_after_sync();
+      const float inv_l = 1.f / l;
+      typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
+  #pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(o_col + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
       }
-      {
-        float s0, s1, s2, s3;
-        f2_unpack(sa2, s0, s1);
-        f2_unpack(sb2, s2, s3);
-        l += (s0 + s1) + (s2 + s3);
-      }
-      // P: keys 0..31 -> columns 0..15, keys 32..63 -> columns 16..31 of S_t
-      tmem_st16(s_col, pa);
-      tmem_st16(s_col + 16, pb);
-      tmem_st_wait();
+      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
+      // the next item's first P V overwrites O_t after this warpgroup's next
+      // P arrival, which follows these loads
       tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_pready[t][bb]));
     }
-    // ---------------- epilogue ----------------
-    mbar_wait(smem_u32(&bar_done), 0, g, kDevTimeoutBase + 38);
-    __syncwarp();
-    tc_fence_after_sync();
-    const float inv_l = 1.f / l;
-    typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t rr[32];
-      tmem_ld32(o_col + c * 32, rr);
-      tmem_ld_wait(rr);
-      if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
-    }
-    if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
   }
 
   tc_fence_before_sync();

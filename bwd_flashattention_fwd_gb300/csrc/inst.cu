@@ -60,7 +60,7 @@ int launch(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, con
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
-// D <= 128: two 128-row query tiles per CTA (fwd2_kernel.cuh).
+// D <= 128: two 128-row query tiles per work item, persistent CTAs (fwd2_kernel.cuh).
 template <bool BF16, bool CAUSAL>
 int fwd2_impl(const AttnArgs& a) {
   using Gm = Fwd2Geom<(kD <= 128 ? kD : 128)>;
@@ -77,7 +77,10 @@ int fwd2_impl(const AttnArgs& a) {
   p.n_qtiles = (a.Lq + 2 * Gm::BQ - 1) / (2 * Gm::BQ);  // 256-row pairs of tiles
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.limit_ns = a.limit_ns;
-  const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  // persistent: one CTA per SM (fewer when there are fewer work items)
+  const long long n_items = static_cast<long long>(p.n_qtiles) * a.B * a.Hq;
+  const int sms = a.num_sms > 0 ? a.num_sms : 1;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   return launch(attn_fwd2_kernel<(kD <= 128 ? kD : 128), BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
                 a.stream, tq, tk, tv, p);
 }
