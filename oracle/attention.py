@@ -32,9 +32,17 @@ softmax, no log2 tricks), for every batch b and query head hq:
   where the sums over g run over the G = Hq / Hkv query heads that share KV
   head hk = hq // G (consecutive query heads share one KV head).
 
+* Block-sparse attention (page 1, section "Sparse Block Masks": an optional
+  uint8 mask with one entry per (query tile, key tile) pair; a zero entry
+  skips the pair): key j is visible to query i only if, in addition,
+  block_mask[i // blk, j // blk] != 0.  The kernels fix blk = 128.  A query
+  row that then sees no key (the pages are silent on this case) has P = 0,
+  O = 0 and LSE = +inf, so its dQ is 0 and it adds nothing to dK and dV.
+
 Layouts: q, o, do, dq are [B, Hq, Lq, D]; k, v, dk, dv are [B, Hkv, Lk, D];
-lse and delta are [B, Hq, Lq].  All arrays are float64 numpy arrays; callers
-decode fp16/bf16 inputs to float64 exactly before calling.
+lse and delta are [B, Hq, Lq]; block_mask is [ceil(Lq/blk), ceil(Lk/blk)],
+shared by all batches and heads.  All arrays are float64 numpy arrays;
+callers decode fp16/bf16 inputs to float64 exactly before calling.
 """
 
 from __future__ import annotations
@@ -42,19 +50,42 @@ from __future__ import annotations
 import numpy as np
 
 LOG2E = 1.0 / np.log(2.0)
+MASK_BLOCK = 128  # rows and columns covered by one block-mask entry in the kernels
 
 
-def visible(Lq: int, Lk: int, causal: bool) -> np.ndarray:
+def visible(Lq: int, Lk: int, causal: bool, block_mask=None, blk: int = MASK_BLOCK) -> np.ndarray:
     """Boolean [Lq, Lk]: True where key j is visible to query i.
 
     Bottom-right causal alignment: j <= i + (Lk - Lq) (page 2, "Ragged causal
-    inputs").  Non-causal attention sees every key.
+    inputs").  Non-causal attention sees every key.  With a block mask, key j
+    is visible only where block_mask[i // blk, j // blk] != 0 (page 1, "Sparse
+    Block Masks").
     """
     if not causal:
-        return np.ones((Lq, Lk), dtype=bool)
-    i = np.arange(Lq)[:, None]
-    j = np.arange(Lk)[None, :]
-    return j <= i + (Lk - Lq)
+        vis = np.ones((Lq, Lk), dtype=bool)
+    else:
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lk)[None, :]
+        vis = j <= i + (Lk - Lq)
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        if bm.shape != (-(-Lq // blk), -(-Lk // blk)):
+            raise ValueError("block mask shape must be [ceil(Lq/blk), ceil(Lk/blk)]")
+        vis = vis & bm[np.arange(Lq)[:, None] // blk, np.arange(Lk)[None, :] // blk]
+    return vis
+
+
+def _softmax_rows(S: np.ndarray, mask: np.ndarray):
+    """Masked softmax of each row: (P, LSE_natural).  A row with no visible
+    entry gets P = 0 and LSE = +inf."""
+    has = mask.any(axis=1, keepdims=True)
+    S = np.where(mask, S, -np.inf)
+    m = np.where(has, S.max(axis=1, keepdims=True, initial=-np.inf), 0.0)
+    E = np.where(mask, np.exp(np.where(mask, S, 0.0) - m), 0.0)
+    l = E.sum(axis=1, keepdims=True)
+    P = np.where(has, E / np.where(has, l, 1.0), 0.0)
+    lse = np.where(has, m + np.log(np.where(has, l, 1.0)), np.inf)[:, 0]
+    return P, lse
 
 
 def _group(Hq: int, Hkv: int) -> int:
@@ -63,24 +94,20 @@ def _group(Hq: int, Hkv: int) -> int:
     return Hq // Hkv
 
 
-def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float, causal: bool):
+def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float, causal: bool, block_mask=None,
+                 blk: int = MASK_BLOCK):
     """One (b, hq) head: returns (P, O, LSE_natural) with P the full [Lq, Lk]
     probability matrix (page 3, section 3: S = scale*QK^T + mask,
     P = softmax(S), O = PV; L = m + log l)."""
     Lq, Lk = qh.shape[0], kh.shape[0]
-    mask = visible(Lq, Lk, causal)
+    mask = visible(Lq, Lk, causal, block_mask, blk)
     S = scale * (qh @ kh.T)
-    S = np.where(mask, S, -np.inf)
-    m = S.max(axis=1, keepdims=True)
-    E = np.where(mask, np.exp(S - m), 0.0)
-    l = E.sum(axis=1, keepdims=True)
-    P = E / l
+    P, lse = _softmax_rows(S, mask)
     O = P @ vh
-    lse = (m + np.log(l))[:, 0]
     return P, O, lse
 
 
-def forward(q, k, v, scale: float, causal: bool):
+def forward(q, k, v, scale: float, causal: bool, block_mask=None, blk: int = MASK_BLOCK):
     """Returns (o, lse2, lse_nat): o [B,Hq,Lq,D]; lse2 = base-2 LSE [B,Hq,Lq]."""
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
@@ -90,7 +117,7 @@ def forward(q, k, v, scale: float, causal: bool):
     for b in range(B):
         for hq in range(Hq):
             hk = hq // G
-            _, o[b, hq], lse[b, hq] = head_forward(q[b, hq], k[b, hk], v[b, hk], scale, causal)
+            _, o[b, hq], lse[b, hq] = head_forward(q[b, hq], k[b, hk], v[b, hk], scale, causal, block_mask, blk)
     return o, lse * LOG2E, lse
 
 
@@ -99,12 +126,12 @@ def delta(o, do):
     return (o * do).sum(axis=-1)
 
 
-def head_backward(qh, kh, vh, oh, doh, scale: float, causal: bool):
+def head_backward(qh, kh, vh, oh, doh, scale: float, causal: bool, block_mask=None, blk: int = MASK_BLOCK):
     """One (b, hq) head: returns (dq, dk_part, dv_part) where the dk/dv parts
     are this query head's contribution to its KV head (page 1, "Background",
     backward pass: dP = dO V^T, dS = scale * P * (dP - delta), dQ = dS K,
     dK = dS^T Q, dV = P^T dO)."""
-    P, _, _ = head_forward(qh, kh, vh, scale, causal)
+    P, _, _ = head_forward(qh, kh, vh, scale, causal, block_mask, blk)
     dP = doh @ vh.T
     dlt = delta(oh, doh)[:, None]
     dS = P * (dP - dlt)
@@ -114,7 +141,7 @@ def head_backward(qh, kh, vh, oh, doh, scale: float, causal: bool):
     return dq, dk, dv
 
 
-def backward(q, k, v, o, do, scale: float, causal: bool):
+def backward(q, k, v, o, do, scale: float, causal: bool, block_mask=None, blk: int = MASK_BLOCK):
     """Returns (dq, dk, dv) with the GQA group sums folded into dk and dv."""
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
@@ -125,7 +152,8 @@ def backward(q, k, v, o, do, scale: float, causal: bool):
     for b in range(B):
         for hq in range(Hq):
             hk = hq // G
-            a, bk, bv = head_backward(q[b, hq], k[b, hk], v[b, hk], o[b, hq], do[b, hq], scale, causal)
+            a, bk, bv = head_backward(q[b, hq], k[b, hk], v[b, hk], o[b, hq], do[b, hq], scale, causal, block_mask,
+                                      blk)
             dq[b, hq] = a
             dk[b, hk] += bk
             dv[b, hk] += bv

@@ -236,9 +236,136 @@ def pin_sampled_helpers(o):
         assert np.allclose(dvs, dv[1, 0, keys], atol=1e-13)
 
 
+def _rand_mask(rng, nqb, nkb, density=0.6):
+    return (rng.random((nqb, nkb)) < density).astype(np.uint8)
+
+
+def pin_block_mask_all_ones(o):
+    """A block mask of ones changes nothing (page 1, "Sparse Block Masks":
+    only zero entries skip a tile pair)."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, Lq, Lk, D = 1, 2, 1, 7, 9, 4
+    q, k, v, do = (_rand(B, Hq, Lq, D, rng=rng), _rand(B, Hkv, Lk, D, rng=rng),
+                   _rand(B, Hkv, Lk, D, rng=rng), _rand(B, Hq, Lq, D, rng=rng))
+    for causal in (True, False):
+        ones = np.ones((-(-Lq // 3), -(-Lk // 3)), dtype=np.uint8)
+        out, lse2, _ = o.forward(q, k, v, 0.5, causal)
+        outm, lse2m, _ = o.forward(q, k, v, 0.5, causal, ones, 3)
+        assert np.array_equal(out, outm) and np.array_equal(lse2, lse2m)
+        g = o.backward(q, k, v, out, do, 0.5, causal)
+        gm = o.backward(q, k, v, out, do, 0.5, causal, ones, 3)
+        assert all(np.array_equal(x, y) for x, y in zip(g, gm))
+
+
+def pin_block_mask_block_diagonal(o):
+    """With a block-diagonal mask every diagonal block is an attention problem
+    of its own: its rows and keys match the unmasked definition on the block's
+    sub-arrays (square blocks, so causal alignment is the same inside)."""
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, L, D, blk = 1, 2, 1, 6, 4, 2
+    q, k, v, do = (_rand(B, Hq, L, D, rng=rng), _rand(B, Hkv, L, D, rng=rng),
+                   _rand(B, Hkv, L, D, rng=rng), _rand(B, Hq, L, D, rng=rng))
+    eye = np.eye(L // blk, dtype=np.uint8)
+    for causal in (True, False):
+        out, lse2, _ = o.forward(q, k, v, 0.7, causal, eye, blk)
+        dq, dk, dv = o.backward(q, k, v, out, do, 0.7, causal, eye, blk)
+        for t in range(L // blk):
+            r = slice(t * blk, (t + 1) * blk)
+            ob, lb, _ = o.forward(q[:, :, r], k[:, :, r], v[:, :, r], 0.7, causal)
+            gb = o.backward(q[:, :, r], k[:, :, r], v[:, :, r], ob, do[:, :, r], 0.7, causal)
+            assert np.allclose(out[:, :, r], ob, atol=1e-13) and np.allclose(lse2[:, :, r], lb, atol=1e-13)
+            assert np.allclose(dq[:, :, r], gb[0], atol=1e-13)
+            assert np.allclose(dk[:, :, r], gb[1], atol=1e-13) and np.allclose(dv[:, :, r], gb[2], atol=1e-13)
+
+
+def pin_block_mask_torch_sdpa(o):
+    """Against PyTorch's CPU fp64 attention and autograd with the explicit
+    element mask causal AND block_mask[i // blk, j // blk] (every row keeps a
+    visible key; non-square block grids catch a transposed mask)."""
+    rng = np.random.default_rng(13)
+    for causal, Lq, Lk, blk in [(True, 7, 11, 3), (False, 9, 5, 2), (True, 10, 10, 4)]:
+        B, Hq, Hkv, D = 1, 4, 2, 8
+        G = Hq // Hkv
+        nqb, nkb = -(-Lq // blk), -(-Lk // blk)
+        while True:
+            bm = _rand_mask(rng, nqb, nkb)
+            vis = o.visible(Lq, Lk, causal, bm, blk) if o is A else A.visible(Lq, Lk, causal, bm, blk)
+            if vis.any(axis=1).all():
+                break
+        q, k, v, do = (_rand(B, Hq, Lq, D, rng=rng), _rand(B, Hkv, Lk, D, rng=rng),
+                       _rand(B, Hkv, Lk, D, rng=rng), _rand(B, Hq, Lq, D, rng=rng))
+        scale = 1.0 / math.sqrt(D)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        kr, vr = tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1)
+        tmask = torch.tensor(vis)
+        to = torch.nn.functional.scaled_dot_product_attention(tq, kr, vr, attn_mask=tmask, scale=scale)
+        to.backward(torch.tensor(do))
+        scores = ((tq.detach() @ kr.detach().transpose(-1, -2)) * scale).masked_fill(~tmask, float("-inf"))
+        tlse2 = torch.logsumexp(scores, dim=-1) / math.log(2.0)
+        out, lse2, _ = o.forward(q, k, v, scale, causal, bm, blk)
+        dq, dk, dv = o.backward(q, k, v, out, do, scale, causal, bm, blk)
+        assert np.allclose(out, to.detach().numpy(), atol=1e-12)
+        assert np.allclose(lse2, tlse2.numpy(), atol=1e-12)
+        assert np.allclose(dq, tq.grad.numpy(), atol=1e-12)
+        assert np.allclose(dk, tk.grad.numpy(), atol=1e-12)
+        assert np.allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
+def pin_block_mask_empty_rows(o):
+    """Query rows whose every key block is masked: O = 0, LSE = +inf, dQ = 0,
+    and dK, dV equal the problem without those rows (non-causal, so dropping
+    rows moves no causal offset)."""
+    rng = np.random.default_rng(14)
+    B, Hq, Hkv, Lq, Lk, D, blk = 1, 2, 1, 6, 6, 4, 2
+    q, k, v, do = (_rand(B, Hq, Lq, D, rng=rng), _rand(B, Hkv, Lk, D, rng=rng),
+                   _rand(B, Hkv, Lk, D, rng=rng), _rand(B, Hq, Lq, D, rng=rng))
+    bm = np.ones((3, 3), dtype=np.uint8)
+    bm[1] = 0  # query rows 2, 3 see nothing
+    out, lse2, _ = o.forward(q, k, v, 0.6, False, bm, blk)
+    dq, dk, dv = o.backward(q, k, v, out, do, 0.6, False, bm, blk)
+    assert np.array_equal(out[:, :, 2:4], np.zeros_like(out[:, :, 2:4]))
+    assert np.all(np.isposinf(lse2[:, :, 2:4]))
+    assert np.array_equal(dq[:, :, 2:4], np.zeros_like(dq[:, :, 2:4]))
+    keep = [0, 1, 4, 5]
+    ok, lk, _ = o.forward(q[:, :, keep], k, v, 0.6, False)
+    gk = o.backward(q[:, :, keep], k, v, ok, do[:, :, keep], 0.6, False)
+    assert np.allclose(out[:, :, keep], ok, atol=1e-13) and np.allclose(lse2[:, :, keep], lk, atol=1e-13)
+    assert np.allclose(dq[:, :, keep], gk[0], atol=1e-13)
+    assert np.allclose(dk, gk[1], atol=1e-13) and np.allclose(dv, gk[2], atol=1e-13)
+
+
+def pin_block_mask_finite_differences(o):
+    """Central differences of L = sum(dO * O) match the gradients under a block
+    mask that also empties a query block."""
+    rng = np.random.default_rng(15)
+    h = 1e-6
+    B, Hq, Hkv, Lq, Lk, D, blk = 1, 2, 1, 6, 8, 3, 2
+    bm = np.array([[1, 0, 1, 1], [0, 0, 0, 0], [1, 1, 0, 1]], dtype=np.uint8)
+    for causal in (True, False):
+        q, k, v, do = (_rand(B, Hq, Lq, D, rng=rng), _rand(B, Hkv, Lk, D, rng=rng),
+                       _rand(B, Hkv, Lk, D, rng=rng), _rand(B, Hq, Lq, D, rng=rng))
+        out, _, _ = o.forward(q, k, v, 0.5, causal, bm, blk)
+        grads = o.backward(q, k, v, out, do, 0.5, causal, bm, blk)
+
+        def loss(q_, k_, v_):
+            return float((o.forward(q_, k_, v_, 0.5, causal, bm, blk)[0] * do).sum())
+
+        for which, x in enumerate((q, k, v)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p, args_m = [q, k, v], [q, k, v]
+                args_p[which], args_m[which] = xp, xm
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert np.allclose(grads[which], num, atol=1e-7, rtol=1e-6), (which, causal)
+
+
 PINS = [pin_rows_sum_to_one, pin_zero_query, pin_causal_diagonal, pin_delta_identity,
         pin_gqa_is_repeated_mha, pin_finite_differences, pin_torch_sdpa, pin_brute_force_loops,
-        pin_sampled_helpers]
+        pin_sampled_helpers, pin_block_mask_all_ones, pin_block_mask_block_diagonal,
+        pin_block_mask_torch_sdpa, pin_block_mask_empty_rows, pin_block_mask_finite_differences]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -292,15 +419,32 @@ def _mutant(**overrides):
     return m
 
 
-def _top_left_visible(Lq, Lk, causal):
-    if not causal:
-        return np.ones((Lq, Lk), dtype=bool)
-    return np.arange(Lk)[None, :] <= np.arange(Lq)[:, None]
+def _top_left_visible(Lq, Lk, causal, block_mask=None, blk=A.MASK_BLOCK):
+    vis = np.ones((Lq, Lk), dtype=bool) if not causal else np.arange(Lk)[None, :] <= np.arange(Lq)[:, None]
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        vis = vis & bm[np.arange(Lq)[:, None] // blk, np.arange(Lk)[None, :] // blk]
+    return vis
+
+
+def _mask_transposed_visible(Lq, Lk, causal, block_mask=None, blk=A.MASK_BLOCK):
+    # reads the block mask as [key block, query block]
+    vis = A.visible(Lq, Lk, causal)
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        kb, qb = np.arange(Lk)[None, :] // blk, np.arange(Lq)[:, None] // blk
+        ok = (kb < bm.shape[0]) & (qb < bm.shape[1])
+        vis = vis & ok & bm[np.minimum(kb, bm.shape[0] - 1), np.minimum(qb, bm.shape[1] - 1)]
+    return vis
+
+
+def _mask_ignored_visible(Lq, Lk, causal, block_mask=None, blk=A.MASK_BLOCK):
+    return A.visible(Lq, Lk, causal)
 
 
 def _mk_head_backward(change):
-    def head_backward(qh, kh, vh, oh, doh, scale, causal, _m=None):
-        P, _, _ = A.head_forward(qh, kh, vh, scale, causal)
+    def head_backward(qh, kh, vh, oh, doh, scale, causal, block_mask=None, blk=A.MASK_BLOCK):
+        P, _, _ = A.head_forward(qh, kh, vh, scale, causal, block_mask, blk)
         dP = doh @ vh.T
         dlt = (oh * doh).sum(axis=-1)[:, None]
         if change == "drop_delta":
@@ -321,20 +465,27 @@ def _mk_head_backward(change):
     return head_backward
 
 
-def _bad_forward_lse_natural(q, k, v, scale, causal):
-    o, lse2, lse = A.forward(q, k, v, scale, causal)
+def _bad_forward_lse_natural(q, k, v, scale, causal, block_mask=None, blk=A.MASK_BLOCK):
+    o, lse2, lse = A.forward(q, k, v, scale, causal, block_mask, blk)
     return o, lse, lse
 
 
-def _bad_gqa_forward(q, k, v, scale, causal):
+def _bad_gqa_forward(q, k, v, scale, causal, block_mask=None, blk=A.MASK_BLOCK):
     # query head hq reads KV head hq % Hkv instead of hq // G
     Hq, Hkv = q.shape[1], k.shape[1]
     idx = [h % Hkv for h in range(Hq)]
-    return A.forward(q, k[:, idx], v[:, idx], scale, causal)
+    return A.forward(q, k[:, idx], v[:, idx], scale, causal, block_mask, blk)
 
 
-def _bad_scale_forward(q, k, v, scale, causal):
-    return A.forward(q, k, v, 1.0, causal)
+def _bad_scale_forward(q, k, v, scale, causal, block_mask=None, blk=A.MASK_BLOCK):
+    return A.forward(q, k, v, 1.0, causal, block_mask, blk)
+
+
+def _masked_rows_uniform_softmax_rows(S, mask):
+    # a row with no visible key spreads its probability over every key
+    has = mask.any(axis=1, keepdims=True)
+    mask = np.where(has, mask, True)
+    return A._softmax_rows(S, mask)
 
 
 MUTANTS = {
@@ -348,6 +499,9 @@ MUTANTS = {
     "gqa_modulo_mapping": dict(forward=_bad_gqa_forward),
     "scale_ignored": dict(forward=_bad_scale_forward),
     "delta_zero": dict(delta=lambda o_, do_: np.zeros(o_.shape[:-1])),
+    "block_mask_transposed": dict(visible=_mask_transposed_visible),
+    "block_mask_ignored": dict(visible=_mask_ignored_visible),
+    "masked_row_uniform": dict(_softmax_rows=_masked_rows_uniform_softmax_rows),
 }
 
 
