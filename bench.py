@@ -7,11 +7,17 @@ is credited TFLOP/s: 3.5 x the forward FLOPs (4*B*Hq*Lq*Lk*D, halved for
 causal) over the summed device time of the step's kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--block-mask none|window:W|random:P]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload on its own GPU (weak scaling); the value is all ranks' work
 over the slowest rank's time.  `--impl reference` times the fp64 CPU oracle on
 the host cores instead, on a bounded sample of the same workload.
+
+With `--block-mask` the step runs the block-sparse entry points
+(attn_fwd_masked, attn_bwd_delta, attn_bwd_masked) and the metric credits
+3.5 x 4*D FLOPs per (query, key) pair the mask and the causal rule leave
+visible.
 """
 
 from __future__ import annotations
@@ -34,9 +40,10 @@ import torch  # noqa: E402
 
 from bwd_flashattention_fwd_gb300 import flops as F  # noqa: E402
 from bwd_flashattention_fwd_gb300 import replicas  # noqa: E402
-from bwd_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+from bwd_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, block_mask, make_inputs  # noqa: E402
 
 METRIC = "fwd+bwd attention TFLOP/s, causal GQA L=8192 D=128 bf16; % of BF16 TC peak"
+METRIC_MASKED = "block-sparse fwd+bwd attention TFLOP/s (3.5 x 4*D FLOPs per visible pair), GQA D=128 bf16"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "qwen3_8b_gqa_l8192_d128"
 L2_FLUSH_BYTES = 256 << 20
@@ -86,7 +93,7 @@ def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None).  Line format:
     `<kernel> <workload> <bytes_per_launch> <source_hash>`."""
-    if not os.path.exists(TRAFFIC_FILE):
+    if kernel not in KERNEL_FILES or not os.path.exists(TRAFFIC_FILE):
         return None
     cur = kernel_source_hash(kernel)
     with open(TRAFFIC_FILE) as f:
@@ -268,22 +275,34 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sc, causal = w.scale, w.causal
+    bm_np = block_mask(args.block_mask, w.Lq, w.Lk, seed=w.seed)
+    bm = None if bm_np is None else torch.from_numpy(bm_np).to(dev)
+
+    if bm is None:
+        phase_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
+        calls = (
+            lambda: gbattn.attn_fwd(q, k, v, o, lse, sc, causal, stream),
+            lambda: gbattn.attn_bwd_delta(o, do, dlt, stream),
+            lambda: gbattn.attn_bwd_dkv(q, k, v, do, lse, dlt, dk, dv, sc, causal, stream),
+            lambda: gbattn.attn_bwd_dq(q, k, v, do, lse, dlt, dq, sc, causal, stream),
+        )
+    else:
+        # attn_bwd_masked launches the dK/dV kernel, then the dQ kernel
+        phase_names = ("fwd", "delta", "bwd")
+        calls = (
+            lambda: gbattn.attn_fwd_masked(q, k, v, o, lse, bm, sc, causal, stream),
+            lambda: gbattn.attn_bwd_delta(o, do, dlt, stream),
+            lambda: gbattn.attn_bwd_masked(q, k, v, o, do, lse, dlt, bm, dq, dk, dv, sc, causal, stream),
+        )
+    n_ev = len(calls) + 1
 
     def step(ev=None):
+        for j, c in enumerate(calls):
+            if ev is not None:
+                ev[j].record(stream)
+            c()
         if ev is not None:
-            ev[0].record(stream)
-        gbattn.attn_fwd(q, k, v, o, lse, sc, causal, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        gbattn.attn_bwd_delta(o, do, dlt, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        gbattn.attn_bwd_dkv(q, k, v, do, lse, dlt, dk, dv, sc, causal, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        gbattn.attn_bwd_dq(q, k, v, do, lse, dlt, dq, sc, causal, stream)
-        if ev is not None:
-            ev[4].record(stream)
+            ev[-1].record(stream)
 
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
@@ -292,7 +311,7 @@ def run_ours(args):
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     clocks = ClockSampler(physical_gpu_index(local_rank))
     replicas.barrier(dev)
     torch.cuda.synchronize(dev)
@@ -308,15 +327,19 @@ def run_ours(args):
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during the timed steps")
 
-    phase_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
     per_phase = {n: [] for n in phase_names}
     step_ms = []
     for ev in events:
         for j, n in enumerate(phase_names):
             per_phase[n].append(ev[j].elapsed_time(ev[j + 1]))
-        step_ms.append(ev[0].elapsed_time(ev[4]))
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
     local_s = sum(step_ms) / 1e3
-    credited = F.credited_fwd_bwd(w.B, w.Hq, w.Lq, w.Lk, w.D, w.causal)
+    if bm is None:
+        pairs = F.visible_pairs(w.Lq, w.Lk, w.causal)
+        credited = F.credited_fwd_bwd(w.B, w.Hq, w.Lq, w.Lk, w.D, w.causal)
+    else:
+        pairs = F.visible_pairs_masked(w.Lq, w.Lk, w.causal, bm_np)
+        credited = 3.5 * 4.0 * w.D * w.B * w.Hq * pairs
     value_flops, _, max_s = replicas.aggregate_throughput(credited * args.steps, local_s, dev)
     value = value_flops / 1e12
     peaks = load_peaks()
@@ -324,18 +347,20 @@ def run_ours(args):
 
     # roofline per kernel (algorithmic work / average launch time)
     kernels = {}
-    for n in ("fwd", "bwd_dkv", "bwd_dq"):
-        fl = F.kernel_flops(n, w.B, w.Hq, w.Lq, w.Lk, w.D, w.causal)
+    mm_phases = [n for n in phase_names if n != "delta"]
+    for n in mm_phases:
+        fl = F.kernel_flops_pairs(n, w.B, w.Hq, w.D, pairs)
         ach = fl / (avg[n] * 1e-3) / 1e12
         kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
                       "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
-                      "avg_ms": avg[n], "algorithmic": fl, "traffic": recorded_traffic(n, w.name)}
+                      "avg_ms": avg[n], "algorithmic": fl,
+                      "traffic": recorded_traffic(n, w.name) if bm is None else None}
     db = F.delta_bytes(w.B, w.Hq, w.Lq, w.D)
     ach = db / (avg["delta"] * 1e-3) / 1e9
     kernels["delta"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": ach / peaks["hbm_gbs"], "avg_ms": avg["delta"], "algorithmic": db,
                         "traffic": recorded_traffic("delta", w.name)}
-    dominant = max(("fwd", "bwd_dkv", "bwd_dq"), key=lambda n: avg[n])
+    dominant = max(mm_phases, key=lambda n: avg[n])
     roof = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
     roof["peak_kind"] = f"bf16 dense, sustained ({peaks['source']})"
@@ -343,17 +368,22 @@ def run_ours(args):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, dev, stream, gbattn, credited)
+        e2e = run_e2e(args, w, dev, stream, gbattn, credited, bm)
 
     n_dkv = 1 if w.D <= 128 else 2
+    extra = {}
+    if bm is not None:
+        extra = {"block_mask": args.block_mask, "mask_blocks_kept": int(bm_np.sum()),
+                 "mask_blocks": int(bm_np.size), "visible_pairs_per_head": pairs}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "metric": METRIC if bm is None else METRIC_MASKED, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, {
             "l2": "flushed between steps (256 MiB write outside the step events); inputs 384 MiB",
             "parallelism": "replicas" if ws > 1 else "single GPU",
             "timing": "CUDA events on the launching stream, sum over steps",
+            **extra,
         }),
         "pct_of_bf16_peak": 100.0 * value / ws / peaks["bf16_tflops"],
         "pct_of_bf16_peak_sustained": 100.0 * value / ws / peaks["bf16_tflops_sustained"],
@@ -377,7 +407,7 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(args, w, dev, stream, gbattn, credited):
+def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
     """Same metric through attn_fwd / attn_bwd_delta / attn_bwd with pinned
     host buffers: every step copies q, k, v, dO in and o, lse, dq, dk, dv out.
     Steps are pipelined over two sets of device buffers and three streams
@@ -419,10 +449,16 @@ def run_e2e(args, w, dev, stream, gbattn, credited):
         if i >= 2:
             stream.wait_event(ev_out[i - 2])  # buffer set b's outputs reached the host
         q, k, v, do = s_["in"]
-        gbattn.attn_fwd(q, k, v, s_["o"], s_["lse"], w.scale, w.causal, stream)
-        gbattn.attn_bwd_delta(s_["o"], do, s_["dlt"], stream)
-        gbattn.attn_bwd(q, k, v, s_["o"], do, s_["lse"], s_["dlt"], s_["dq"], s_["dk"], s_["dv"], w.scale, w.causal,
-                        stream)
+        if bm is None:
+            gbattn.attn_fwd(q, k, v, s_["o"], s_["lse"], w.scale, w.causal, stream)
+            gbattn.attn_bwd_delta(s_["o"], do, s_["dlt"], stream)
+            gbattn.attn_bwd(q, k, v, s_["o"], do, s_["lse"], s_["dlt"], s_["dq"], s_["dk"], s_["dv"], w.scale,
+                            w.causal, stream)
+        else:
+            gbattn.attn_fwd_masked(q, k, v, s_["o"], s_["lse"], bm, w.scale, w.causal, stream)
+            gbattn.attn_bwd_delta(s_["o"], do, s_["dlt"], stream)
+            gbattn.attn_bwd_masked(q, k, v, s_["o"], do, s_["lse"], s_["dlt"], bm, s_["dq"], s_["dk"], s_["dv"],
+                                   w.scale, w.causal, stream)
         ev_comp[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[i])
@@ -457,6 +493,8 @@ def main(argv=None) -> int:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--block-mask", default="none",
+                    help="block-sparse pattern: none, window:W (W key blocks of 128), random:P")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")

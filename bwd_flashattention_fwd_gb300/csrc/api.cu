@@ -201,6 +201,52 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
   return finish(dispatch_bwd(a));
 }
 
+// Block-sparse variants: the same calls with a [ceil(Lq/128), ceil(Lk/128)]
+// uint8 block mask on the device; head dimensions up to 128.
+extern "C" attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                                         const uint8_t* block_mask, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                                         float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !block_mask) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  if (D > 128) return ATTN_ERR_UNSUPPORTED;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse, a.block_mask = block_mask;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dispatch_fwd(a));
+}
+
+extern "C" attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                                         const void* dO, const float* lse, const float* delta,
+                                         const uint8_t* block_mask, void* dq, void* dk, void* dv, int B, int Hq,
+                                         int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                         cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !delta || !block_mask || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  if (D > 128) return ATTN_ERR_UNSUPPORTED;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta, a.block_mask = block_mask;
+  a.dq = dq, a.dk = dk, a.dv = dv;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dispatch_bwd(a));
+}
+
 // The two halves of attn_bwd, for callers that run them on separate streams.
 namespace {
 attn_status_t bwd_part(bool dq_part, const void* q, const void* k, const void* v, const void* dO,

@@ -31,6 +31,13 @@
 // same SM sub-partition, so the row warps on the sub-partitions of warps 9
 // and 10 evaluate part of their exponentials with a polynomial on the FMA
 // pipe (ex2_poly2).
+//
+// MASKED: block-sparse variant ("feat(attention): complete Flash Attention
+// VJP implementation", section "Sparse Block Masks": the dK/dV kernel skips
+// the query blocks whose mask entry is zero).  The CTA's 128 keys are one
+// mask block and a query tile half of a 128-row block; skipped query tiles
+// are neither loaded nor computed, and every warp walks the same list of kept
+// tiles.  A key tile with no kept query tile writes dK = dV = 0.
 #pragma once
 
 #include <type_traits>
@@ -77,7 +84,7 @@ struct Dkv2Geom {
   static_assert(POLY_Q1 >= 0 && POLY_Q1 <= 16 && POLY_Q2 >= 0 && POLY_Q2 <= 16, "polynomial share");
 };
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     attn_bwd_dkv2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ k, const BwdParams p) {
@@ -104,8 +111,11 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   const int kt = blockIdx.y;
   const int k0 = kt * BK;
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
-  const int nq = p.n_qtiles - qt_start;
-  const int n_iter = p.G * nq;
+  static_assert(BK == kMaskBlock && 2 * BQ == kMaskBlock, "key tile = mask block, query tile = half a block");
+  // query tile qt is computed (block mask)
+  auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
+  // (query head, computed query tile) iterations; every warp counts them itself
+  const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -145,7 +155,8 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     mbar_arrive_expect_tx_w(smem_u32(&bar_v), Gm::V_BYTES);
     for (int c = 0; c < NCH; ++c) tma_load_3d_w(sV + c * BK * 128, &tmV, smem_u32(&bar_v), c * 64, k0, bhk);
     RingPos<ST> st;                  // stage of iteration it
-    int gi = 0, qtile = qt_start;    // query head in the group and query tile of iteration it
+    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
+    int gi = 0, qtile = qw.first(qt_start);  // query head in the group and query tile of iteration it
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 81);
@@ -166,7 +177,8 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
         dlt_s[s][c] = qi < p.Lq ? p.delta[row] : 0.f;
       }
       mbar_arrive(smem_u32(&bar_stfull[s]));
-      if (++qtile == p.n_qtiles) qtile = qt_start, ++gi;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
     }
     mbar_wait_drain(smem_u32(&bar_v), 0, p.limit_ns);
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
@@ -291,11 +303,13 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       mbar_arrive(smem_u32(&bar_kready));
     }
     RingPos<ST> st;             // stage of iteration it
-    int qtile = qt_start;       // query tile of iteration it
+    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
+    int qtile = qw.first(qt_start);  // query tile of iteration it
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot, buf = it & 1;
       const int q0 = qtile * BQ;
-      if (++qtile == p.n_qtiles) qtile = qt_start;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start);
       mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 88);
       mbar_wait(smem_u32(&bar_sfull), it & 1, g, kDevTimeoutBase + 89);
       mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 90);
@@ -362,11 +376,18 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
 #pragma unroll 1
     for (int c = half; c < D / 32; c += 2) {
       uint32_t rr[32];
-      tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
-      tmem_ld_wait(rr);
+      if (n_iter > 0) {
+        tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept query tile: dK = dV = 0
+      }
       if (kj < p.Lk) store_row32<BF16>(dkrow + c * 32, rr, p.scale);
-      tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
-      tmem_ld_wait(rr);
+      if (n_iter > 0) {
+        tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+      }
       if (kj < p.Lk) store_row32<BF16>(dvrow + c * 32, rr, 1.f);
     }
   }

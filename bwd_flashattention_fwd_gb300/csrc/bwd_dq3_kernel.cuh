@@ -39,6 +39,13 @@
 // instructions issued on the same SM sub-partition, so the row warps on the
 // dQ warp's sub-partition evaluate part of their exponentials with a
 // polynomial on the FMA pipe (ex2_poly2).
+//
+// MASKED: block-sparse variant ("feat(attention): complete Flash Attention
+// VJP implementation", section "Sparse Block Masks": the dQ kernel skips the
+// key blocks whose mask entry is zero).  A query tile is one 128-row mask
+// block and a key tile half of a 128-key block; skipped key tiles are neither
+// loaded nor computed, and every warp walks the same list of kept tiles.  A
+// query tile with no kept key tile writes dQ = 0.
 #pragma once
 
 #include <type_traits>
@@ -100,7 +107,7 @@ __device__ __forceinline__ int dq3_round_item(int r, int n_items) {
   return w < n_items ? w : -1;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     attn_bwd_dq3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -129,6 +136,11 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
     return (kv_end + BK - 1) / BK;
   };
+  static_assert(BQ == kMaskBlock && 2 * BK == kMaskBlock, "query tile = mask block, key tile = half a block");
+  // key tile j of query tile qt is computed (block mask)
+  auto keep = [&](int qt, int j) { return !MASKED || mask_keep(p.bmask, p.nkb, qt, j >> 1); };
+  // number of computed key tiles of query tile qt (warp-collective)
+  auto n_kept = [&](int qt) { return count_kept<MASKED>([&](int j) { return keep(qt, j); }, 0, n_kv_of(qt)); };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -185,7 +197,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       const int b = it.bh / p.Hq, hq = it.bh - b * p.Hq;
       const int zkv = b * p.Hkv + hq / p.G;
       const int n_kv = n_kv_of(it.qt);
-      for (int j = 0; j < n_kv; ++j, kv.next()) {
+      auto kw = kept_walk<MASKED>([&](int j) { return keep(it.qt, j); }, n_kv);
+      for (int j = kw.first(0); j < n_kv; j = kw.next(j)) {
         const int s = kv.slot;
         if (kv.slot == 0 && kv.phase == 1) wrapped = true;
         if (wrapped) mbar_wait(smem_u32(&bar_kvempty[s]), kv.phase ^ 1u, g, kDevTimeoutBase + 61);
@@ -197,6 +210,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
           tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
           tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
         }
+        kv.next();
       }
       // The row threads copied this item's Q / dO out of the buffer when the
       // item started: prefetch the next item's.
@@ -225,10 +239,10 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     uint32_t sphase = 0;  // parity of the S buffer's next use
     bool first = true;
     for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
-      const int n_kv = n_kv_of(dq3_item(w, BH, p.n_qtiles).qt);
+      const int nk = n_kept(dq3_item(w, BH, p.n_qtiles).qt);
       // this item's Q is in tensor memory
       mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 63);
-      for (int j = 0; j < n_kv; ++j, kv.next()) {
+      for (int j = 0; j < nk; ++j, kv.next()) {
         const int s = kv.slot;
         // every row thread has loaded the previous S from the buffer
         if (!first) mbar_wait(smem_u32(&bar_sfree), sphase ^ 1u, g, kDevTimeoutBase + 64);
@@ -272,11 +286,11 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       db_dp.next();
     };
     for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
-      const int n_kv = n_kv_of(dq3_item(w, BH, p.n_qtiles).qt);
+      const int nk = n_kept(dq3_item(w, BH, p.n_qtiles).qt);
       // this item's dO is in tensor memory
       mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 66);
-      for (int j = 0; j < NDP && j < n_kv; ++j) issue_dp();
-      for (int j = 0; j < n_kv; ++j, kv.next(), db.next()) {
+      for (int j = 0; j < NDP && j < nk; ++j) issue_dp();
+      for (int j = 0; j < nk; ++j, kv.next(), db.next()) {
         const int s = kv.slot, buf = db.slot;
         mbar_wait(smem_u32(&bar_dsready[buf]), db.phase, g, kDevTimeoutBase + 68);
         __syncwarp();
@@ -292,7 +306,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         // this warp's dP(t) and dQ(t) are its last reads of the stage
         mma_commit_w(smem_u32(&bar_kvempty[s]));
         // dP three tiles ahead overwrites the buffer behind dQ, which reads its dS
-        if (j + NDP < n_kv) issue_dp();
+        if (j + NDP < nk) issue_dp();
       }
       // Every S MMA of the item completed before its last dS was ready, so
       // this commit covers all of the item's MMAs.
@@ -315,6 +329,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       const int q0 = it.qt * BQ;
       const int qi = q0 + rr_;
       const int n_kv = n_kv_of(it.qt);
+      const int nk = n_kept(it.qt);
       const size_t row = static_cast<size_t>(it.bh) * p.Lq + qi;
       // Q and dO rows from the prefetch buffer (TMA layout: 64-column chunks
       // of 128-byte rows, 16-byte units swizzled by row % 8; zeros past Lq
@@ -365,11 +380,14 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
       const uint64_t nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
       const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
-      for (int j = 0; j < n_kv; ++j, db.next()) {
+      auto kw = kept_walk<MASKED>([&](int j) { return keep(it.qt, j); }, n_kv);
+      for (int j = kw.first(0); j < n_kv; j = kw.next(j)) {
         const int buf = db.slot;
+        const uint32_t dph = db.phase;
+        db.next();
         mbar_wait(smem_u32(&bar_sfull), sphase, g, kDevTimeoutBase + 69);
         sphase ^= 1u;
-        mbar_wait(smem_u32(&bar_dpfull[buf]), db.phase, g, kDevTimeoutBase + 71);
+        mbar_wait(smem_u32(&bar_dpfull[buf]), dph, g, kDevTimeoutBase + 71);
         __syncwarp();
         tc_fence_after_sync();
         const int kc0 = j * BK + half * 32;  // first key of this thread's columns
@@ -427,8 +445,13 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
 #pragma unroll 1
       for (int c = half; c < D / 32; c += 2) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
-        tmem_ld_wait(rr);
+        if (nk > 0) {
+          tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+          tmem_ld_wait(rr);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept key tile: dQ = 0
+        }
         if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
       }
       // The next item's first dQ MMA overwrites these columns; it is issued

@@ -39,6 +39,14 @@
 // item's Q into the (then unused) Q buffer, and the MMA warps compute the next
 // item's first S tiles while the softmax warps write out the current item's O
 // and lse.  Barrier phases count key tiles and items over the CTA's life.
+//
+// MASKED: block-sparse variant ("feat(attention): complete Flash Attention
+// VJP implementation", section "Sparse Block Masks"; the forward applies the
+// same mask so that the saved lse matches the gradients).  Each 128-row query
+// tile is one mask block and each key tile half of a 128-key block.  A key
+// tile that both query tiles of the item mask is neither loaded nor computed;
+// one that only one of them masks is computed and set to -inf for that tile.
+// A row that sees no key gets O = 0 and lse = +inf.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -65,7 +73,7 @@ struct Fwd2Geom {
   static_assert(STAGES >= 3, "shared memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -101,6 +109,16 @@ __global__ void __launch_bounds__(352, 1)
     const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
     return (kv_end + BK - 1) / BK;
   };
+  static_assert(BQ == kMaskBlock && 2 * BK == kMaskBlock, "query tile = mask block, key tile = half a block");
+  const int nqb = (p.Lq + kMaskBlock - 1) / kMaskBlock;
+  // key tile j is visible to query tile t of pair pt as far as the block mask goes
+  auto keep_t = [&](int pt, int t, int j) {
+    return !MASKED || (2 * pt + t < nqb && mask_keep(p.bmask, p.nkb, 2 * pt + t, j >> 1));
+  };
+  // key tile j is computed for the pair (either query tile keeps it)
+  auto keep = [&](int pt, int j) { return !MASKED || keep_t(pt, 0, j) || keep_t(pt, 1, j); };
+  // computed key tiles of pair pt (warp-collective)
+  auto n_kept = [&](int pt) { return count_kept<MASKED>([&](int j) { return keep(pt, j); }, 0, n_kv_of(pt)); };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -155,7 +173,8 @@ __global__ void __launch_bounds__(352, 1)
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < NCH; ++c)
           tma_load_3d_w(sQ + t * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0 + t * BQ, bh);
-      for (int j = 0; j < n_kv; ++j, st.next(), ++issued) {
+      auto kw = kept_walk<MASKED>([&](int j) { return keep(pt, j); }, n_kv);
+      for (int j = kw.first(0); j < n_kv; j = kw.next(j)) {
         const int s = st.slot;
         if (issued >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 31);
         __syncwarp();
@@ -166,6 +185,8 @@ __global__ void __launch_bounds__(352, 1)
           tma_load_3d_w(dK + c * BK * 128, &tmK, bar, c * 64, j * BK, zkv);
           tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, j * BK, zkv);
         }
+        st.next();
+        ++issued;
       }
     }
     // the last ST issued stages
@@ -221,7 +242,7 @@ __global__ void __launch_bounds__(352, 1)
     };
     int r = 0;
     for (int w = round_item(0); w >= 0; w = round_item(++r)) {
-      const int n_kv = n_kv_of(item_pt(w));
+      const int n_kv = n_kept(item_pt(w));  // computed key tiles of the item
       // this item's Q is in shared memory
       mbar_wait(smem_u32(&bar_q), r & 1, g, kDevTimeoutBase + 33);
       __syncwarp();
@@ -237,6 +258,7 @@ __global__ void __launch_bounds__(352, 1)
           if (j + 2 == n_kv - 1) mma_commit_w(smem_u32(&bar_qfree));
         }
       }
+      if (n_kv == 0) mma_commit_w(smem_u32(&bar_qfree));  // nothing reads this item's Q
       mma_commit_w(smem_u32(&bar_done));
     }
     if (r > 0) mbar_wait_drain(smem_u32(&bar_done), (r - 1) & 1, p.limit_ns);
@@ -256,11 +278,15 @@ __global__ void __launch_bounds__(352, 1)
       const int bh = item_bh(w);
       const int q0t = item_pt(w) * 2 * BQ + t * BQ;
       const int qi = q0t + rt;
-      const int n_kv = n_kv_of(item_pt(w));
+      const int pt = item_pt(w);
+      const int n_kv = n_kv_of(pt);
+      const int nk = n_kept(pt);
       const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;  // last visible key
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < n_kv; ++j) {
-        const int T = ts + j;
+      auto kw = kept_walk<MASKED>([&](int j) { return keep(pt, j); }, n_kv);
+      for (int j = kw.first(0), kc = 0; j < n_kv; j = kw.next(j), ++kc) {
+        const int k = MASKED ? kc : j;  // computed key tiles before this one
+        const int T = ts + k;
         const int bb = T & 1;
         const uint32_t s_col = tmem + lrow + Gm::s_col(t, bb);
         mbar_wait(smem_u32(&bar_sfull[t][bb]), (T >> 1) & 1, g, kDevTimeoutBase + 37);
@@ -273,16 +299,20 @@ __global__ void __launch_bounds__(352, 1)
         reg_fence(rb);
         const int k0 = j * BK;
         if ((CAUSAL && (k0 + BK - 1 > q0t + p.off)) || (k0 + BK > p.Lk)) {
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (k0 + i > lim) ra[i] = __float_as_uint(-INFINITY);
             if (k0 + 32 + i > lim) rb[i] = __float_as_uint(-INFINITY);
           }
         }
+        if (MASKED && !keep_t(pt, t, j)) {  // the other query tile needs this key tile
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ra[i] = rb[i] = __float_as_uint(-INFINITY);
+        }
         float mx[8];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(ra[i]), __uint_as_float(rb[i]));
-  #pragma unroll
+#pragma unroll
         for (int i = 8; i < 32; ++i) mx[i & 7] = fmax3(mx[i & 7], __uint_as_float(ra[i]), __uint_as_float(rb[i]));
         const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
         const float m_new = fmaxf(m, mt);
@@ -290,22 +320,22 @@ __global__ void __launch_bounds__(352, 1)
           const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
           m = m_new;
           l *= alpha;
-          if (j > 0) {
-            // O_t holds P V up to key tile j-1 once that MMA is done.  S_t of
-            // key tile j+1 was issued right after it, so its barrier covers it;
-            // on the last key tile a dedicated commit does.
-            if (j + 1 < n_kv)
+          if (k > 0) {
+            // O_t holds P V up to the previous key tile once that MMA is done.
+            // S_t of the next key tile was issued right after it, so its
+            // barrier covers it; on the last key tile a dedicated commit does.
+            if (k + 1 < nk)
               mbar_wait(smem_u32(&bar_sfull[t][(T + 1) & 1]), ((T + 1) >> 1) & 1, g, kDevTimeoutBase + 39);
             else
               mbar_wait(smem_u32(&bar_odone[t]), odone_ph, g, kDevTimeoutBase + 40);
             __syncwarp();
             tc_fence_after_sync();
-  #pragma unroll 1
+#pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t rr[32];
               tmem_ld32(o_col + c * 32, rr);
               tmem_ld_wait(rr);
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
               tmem_st32(o_col + c * 32, rr);
             }
@@ -314,8 +344,10 @@ __global__ void __launch_bounds__(352, 1)
         // P = exp2(S * scale_log2 - m), two elements per packed instruction
         uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
         uint32_t pa[16], pb[16];
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m, -m);
-  #pragma unroll
+        // (a row that has seen no key yet keeps m = -inf and gets P = 0)
+        const float mu = (MASKED && m == -INFINITY) ? 0.f : m;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
+#pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), sl2x2, nm2), x0, x1);
@@ -340,22 +372,29 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_before_sync();
         mbar_arrive(smem_u32(&bar_pready[t][bb]));
       }
-      ts += n_kv;
-      if (n_kv >= 2) odone_ph ^= 1u;
+      ts += nk;
+      if (nk >= 2) odone_ph ^= 1u;
       // ---------------- epilogue ----------------
       mbar_wait(smem_u32(&bar_done), r & 1, g, kDevTimeoutBase + 38);
       __syncwarp();
       tc_fence_after_sync();
-      const float inv_l = 1.f / l;
+      const bool empty = MASKED && !(l > 0.f);  // the row saw no key: O = 0, lse = +inf
+      const float inv_l = empty ? 0.f : 1.f / l;
       typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
-  #pragma unroll 1
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(o_col + c * 32, rr);
-        tmem_ld_wait(rr);
+        if (!MASKED || nk > 0) {  // same for the whole CTA: tcgen05.ld is warp-collective
+          tmem_ld32(o_col + c * 32, rr);
+          tmem_ld_wait(rr);
+        }
+        if (MASKED && (nk == 0 || empty)) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
         if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
       }
-      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
+      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
       // the next item's first P V overwrites O_t after this warpgroup's next
       // P arrival, which follows these loads
       tc_fence_before_sync();

@@ -61,7 +61,7 @@ int launch(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, con
 }
 
 // D <= 128: two 128-row query tiles per work item, persistent CTAs (fwd2_kernel.cuh).
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool MASKED>
 int fwd2_impl(const AttnArgs& a) {
   using Gm = Fwd2Geom<(kD <= 128 ? kD : 128)>;
   CUtensorMap tq, tk, tv;
@@ -75,19 +75,23 @@ int fwd2_impl(const AttnArgs& a) {
   p.B = a.B, p.Hq = a.Hq, p.Hkv = a.Hkv, p.Lq = a.Lq, p.Lk = a.Lk, p.G = a.Hq / a.Hkv;
   p.off = a.Lk - a.Lq;
   p.n_qtiles = (a.Lq + 2 * Gm::BQ - 1) / (2 * Gm::BQ);  // 256-row pairs of tiles
+  p.bmask = a.block_mask;
+  p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.limit_ns = a.limit_ns;
   // persistent: one CTA per SM (fewer when there are fewer work items)
   const long long n_items = static_cast<long long>(p.n_qtiles) * a.B * a.Hq;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  return launch(attn_fwd2_kernel<(kD <= 128 ? kD : 128), BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
-                a.stream, tq, tk, tv, p);
+  return launch(attn_fwd2_kernel<(kD <= 128 ? kD : 128), BF16, CAUSAL, MASKED>, grid, Gm::NUM_THREADS,
+                Gm::SMEM_BYTES, a.stream, tq, tk, tv, p);
 }
 
 template <bool BF16, bool CAUSAL>
 int fwd_impl(const AttnArgs& a) {
-  if constexpr (kD <= 128) return fwd2_impl<BF16, CAUSAL>(a);
+  if constexpr (kD <= 128) {
+    return a.block_mask ? fwd2_impl<BF16, CAUSAL, true>(a) : fwd2_impl<BF16, CAUSAL, false>(a);
+  } else {
   using Gm = FwdGeom<kD>;
   CUtensorMap tq, tk, tv;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) ||
@@ -105,6 +109,7 @@ int fwd_impl(const AttnArgs& a) {
   const dim3 grid(a.B * a.Hq, p.n_qtiles);
   return launch(attn_fwd_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
                 tv, p);
+  }
 }
 
 BwdParams bwd_params(const AttnArgs& a) {
@@ -120,6 +125,8 @@ BwdParams bwd_params(const AttnArgs& a) {
   p.scale = a.scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.limit_ns = a.limit_ns;
+  p.bmask = a.block_mask;
+  p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
   return p;
 }
 
@@ -139,7 +146,7 @@ int dkv_impl(const AttnArgs& a) {
 }
 
 // D <= 128: K held in tensor memory as the A operand of S^T (bwd_dkv2_kernel.cuh).
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool MASKED>
 int dkv2_impl(const AttnArgs& a) {
   constexpr int DD = kD <= 128 ? kD : 128;
   using Gm = Dkv2Geom<DD>;
@@ -151,7 +158,7 @@ int dkv2_impl(const AttnArgs& a) {
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
   const dim3 grid(a.B * a.Hkv, p.n_ktiles);
-  auto kern = attn_bwd_dkv2_kernel<DD, BF16, CAUSAL>;
+  auto kern = attn_bwd_dkv2_kernel<DD, BF16, CAUSAL, MASKED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
     return kLaunchCudaError;
   kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, a.k, p);
@@ -159,7 +166,7 @@ int dkv2_impl(const AttnArgs& a) {
 }
 
 // D <= 128: Q and dO held in tensor memory as MMA A operands (bwd_dq3_kernel.cuh).
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool MASKED>
 int dq3_impl(const AttnArgs& a) {
   constexpr int DD = kD <= 128 ? kD : 128;
   using Gm = Dq3Geom<DD>;
@@ -174,7 +181,7 @@ int dq3_impl(const AttnArgs& a) {
   const long long n_items = static_cast<long long>(p.n_qtiles) * a.B * a.Hq;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  auto kern = attn_bwd_dq3_kernel<DD, BF16, CAUSAL>;
+  auto kern = attn_bwd_dq3_kernel<DD, BF16, CAUSAL, MASKED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
     return kLaunchCudaError;
   kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tdo, tk, tv, p);
@@ -183,7 +190,9 @@ int dq3_impl(const AttnArgs& a) {
 
 template <bool BF16, bool CAUSAL>
 int dq_impl(const AttnArgs& a) {
-  if constexpr (kD <= 128) return dq3_impl<BF16, CAUSAL>(a);
+  if constexpr (kD <= 128) {
+    return a.block_mask ? dq3_impl<BF16, CAUSAL, true>(a) : dq3_impl<BF16, CAUSAL, false>(a);
+  } else {
   using Gm = DqGeom<kD>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
@@ -195,12 +204,13 @@ int dq_impl(const AttnArgs& a) {
   const dim3 grid(a.B * a.Hq, p.n_qtiles);
   return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
                 tv, tdo, p);
+  }
 }
 
 template <bool BF16, bool CAUSAL>
 int dkv_all(const AttnArgs& a) {
   if constexpr (kD <= 128) {
-    return dkv2_impl<BF16, CAUSAL>(a);
+    return a.block_mask ? dkv2_impl<BF16, CAUSAL, true>(a) : dkv2_impl<BF16, CAUSAL, false>(a);
   } else {
     const int r = dkv_impl<BF16, CAUSAL, kDkvDvOnly>(a);
     return r == kLaunchOk ? dkv_impl<BF16, CAUSAL, kDkvDkOnly>(a) : r;

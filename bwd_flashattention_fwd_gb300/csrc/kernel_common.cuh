@@ -20,6 +20,7 @@ enum : int {
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxDynSmem = 232448;                       // 227 KB per CTA on sm_103a
 constexpr int kSmemReserve = 4096;                        // static shared memory
+constexpr int kMaskBlock = 128;  // query rows and keys covered by one block-mask entry
 
 struct FwdParams {
   void* o;
@@ -30,6 +31,9 @@ struct FwdParams {
   int n_qtiles;
   float scale_log2;
   uint64_t limit_ns;
+  // block-sparse variant: uint8 [ceil(Lq/128), ceil(Lk/128)], row-major
+  const uint8_t* bmask;
+  int nkb;  // ceil(Lk / 128): row length of the mask
 };
 
 struct BwdParams {
@@ -44,7 +48,62 @@ struct BwdParams {
   int n_qtiles, n_ktiles;  // in units of the launching kernel's own tiles
   float scale, scale_log2;
   uint64_t limit_ns;
+  // block-sparse variant: uint8 [ceil(Lq/128), ceil(Lk/128)], row-major
+  const uint8_t* bmask;
+  int nkb;  // ceil(Lk / 128): row length of the mask
 };
+
+// Block-mask entry (query block qb, key block kb); nonzero keeps the pair.
+__device__ __forceinline__ bool mask_keep(const uint8_t* m, int nkb, int qb, int kb) {
+  return __ldg(m + static_cast<size_t>(qb) * nkb + kb) != 0;
+}
+
+// Walks the indices x in [lo, hi) for which keep(x) holds, in increasing
+// order, testing 32 candidates per ballot.  Warp-collective: every lane calls
+// first() and next() together and gets the same x; hi ends the walk.  Without
+// a mask every index is kept and the walk is a plain count.
+template <bool MASKED, class Keep>
+struct KeptWalk {
+  Keep keep;
+  int hi;
+  int base = 0;
+  uint32_t bits = 0u;
+  __device__ __forceinline__ int first(int lo) {
+    if (!MASKED) return lo;
+    base = lo - 32;
+    bits = 0u;
+    return next(lo - 1);
+  }
+  __device__ __forceinline__ int next(int x) {
+    if (!MASKED) return x + 1;
+    while (bits == 0u) {
+      base += 32;
+      if (base >= hi) return hi;
+      const int y = base + static_cast<int>(threadIdx.x & 31u);
+      bits = __ballot_sync(0xffffffffu, y < hi && keep(y));
+    }
+    const int i = __ffs(static_cast<int>(bits)) - 1;
+    bits &= bits - 1u;
+    return base + i;
+  }
+};
+
+template <bool MASKED, class Keep>
+__device__ __forceinline__ KeptWalk<MASKED, Keep> kept_walk(Keep keep, int hi) {
+  return KeptWalk<MASKED, Keep>{keep, hi};
+}
+
+// Number of x in [lo, hi) with keep(x) (warp-collective).
+template <bool MASKED, class Keep>
+__device__ __forceinline__ int count_kept(Keep keep, int lo, int hi) {
+  if (!MASKED) return hi - lo;
+  int c = 0;
+  for (int b = lo; b < hi; b += 32) {
+    const int y = b + static_cast<int>(threadIdx.x & 31u);
+    c += __popc(__ballot_sync(0xffffffffu, y < hi && keep(y)));
+  }
+  return c;
+}
 
 template <bool BF16>
 struct Elem;

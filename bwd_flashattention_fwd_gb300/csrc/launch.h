@@ -37,6 +37,8 @@ struct AttnArgs {
   uint64_t limit_ns = 0;
   int num_sms = 0;
   EncodeTiledFn encode = nullptr;
+  // block-sparse variant: uint8 [ceil(Lq/128), ceil(Lk/128)] on the device, or null
+  const uint8_t* block_mask = nullptr;
 };
 
 // Launch results: 0 = launched, 1 = tensor-map encoding rejected the

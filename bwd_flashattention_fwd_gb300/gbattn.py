@@ -24,7 +24,7 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc",
+EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc", "attn_fwd_masked", "attn_bwd_masked",
             "attn_last_device_status", "attn_status_string")
 
 _lib = None
@@ -59,6 +59,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd_dkv.restype = ci
     lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.attn_bwd_noalloc.restype = ci
+    lib.attn_fwd_masked.argtypes = [vp] * 6 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_fwd_masked.restype = ci
+    lib.attn_bwd_masked.argtypes = [vp] * 11 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd_masked.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -154,6 +158,28 @@ def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, scale: float, causal: bool
                                          _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D, float(scale),
                                          int(bool(causal)), _dtype_code(q), _stream_handle(stream))
     return _check(st, "attn_bwd_noalloc", check)
+
+
+def attn_fwd_masked(q, k, v, o, lse, block_mask, scale: float, causal: bool, stream=None,
+                    check: bool = True) -> int:
+    """attn_fwd with a uint8 block mask [ceil(Lq/128), ceil(Lk/128)] on the device."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(block_mask), B, Hq,
+                                        Hkv, Lq, Lk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                                        _stream_handle(stream))
+    return _check(st, "attn_fwd_masked", check)
+
+
+def attn_bwd_masked(q, k, v, o, dO, lse, delta, block_mask, dq, dk, dv, scale: float, causal: bool, stream=None,
+                    check: bool = True) -> int:
+    """attn_bwd with the block mask of attn_fwd_masked."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
+                                        _ptr(block_mask), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D,
+                                        float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_bwd_masked", check)
 
 
 def attn_last_device_status(stream=None) -> int:

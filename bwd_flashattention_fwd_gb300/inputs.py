@@ -88,3 +88,30 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu"):
 def to_f64(t: torch.Tensor) -> np.ndarray:
     """Exact decode of a 16-bit (or fp32) tensor to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def block_mask(spec: str, Lq: int, Lk: int, seed: int = 0, blk: int = 128):
+    """A block-mask pattern of shape [ceil(Lq/blk), ceil(Lk/blk)] (uint8,
+    nonzero = the block pair is kept), or None for "none".
+
+    "window:W"  each query block keeps the W key blocks ending at the block
+                that holds its bottom-right-aligned diagonal (a sliding
+                window of W*blk keys, the pattern the pages name first);
+    "random:P"  each block pair kept with probability P (seeded).
+    """
+    if spec in (None, "", "none"):
+        return None
+    kind, _, arg = spec.partition(":")
+    nqb, nkb = -(-Lq // blk), -(-Lk // blk)
+    if kind == "window":
+        width = int(arg)
+        if width < 1:
+            raise ValueError("window width must be at least one block")
+        # key block holding the last key that row qb*blk + blk-1 may see
+        diag = np.minimum(nkb - 1, (np.minimum(Lq, (np.arange(nqb) + 1) * blk) - 1 + Lk - Lq) // blk)
+        kb = np.arange(nkb)[None, :]
+        return ((kb <= diag[:, None]) & (kb > diag[:, None] - width)).astype(np.uint8)
+    if kind == "random":
+        rng = np.random.default_rng(seed)
+        return (rng.random((nqb, nkb)) < float(arg)).astype(np.uint8)
+    raise ValueError(f"unknown block-mask pattern {spec!r}")

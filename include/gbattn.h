@@ -33,6 +33,7 @@
 #define GBATTN_H_
 
 #include <cuda_runtime_api.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -109,6 +110,32 @@ attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const voi
 attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                            const float* delta, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk,
                            int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Block-sparse attention ("feat(attention): complete Flash Attention VJP
+ * implementation", section "Sparse Block Masks": a uint8 entry per (query
+ * tile, key tile) pair; a zero entry skips the pair).  These two calls are
+ * attn_fwd and attn_bwd with a block mask on top of the causal mask:
+ *   block_mask: DEVICE pointer, uint8, row-major [ceil(Lq/128), ceil(Lk/128)],
+ *     shared by every batch and head; entry (qb, kb) != 0 keeps the pairs of
+ *     query rows [128 qb, 128 qb + 128) and keys [128 kb, 128 kb + 128), 0
+ *     removes them.  Owned by the caller, read only.
+ *   Key tiles (forward, dQ) and query tiles (dK/dV) that the mask removes are
+ *   neither loaded nor computed.  A query row left with no visible key gets
+ *   O = 0 and lse = +inf (the pages do not define this case); its dQ is 0 and
+ *   it adds nothing to dK and dV.  Feed attn_bwd_masked the lse of
+ *   attn_fwd_masked with the same mask; delta comes from attn_bwd_delta.
+ *   D in {64, 96, 128}; D = 256 returns ATTN_ERR_UNSUPPORTED.  Other arguments
+ *   and errors as for attn_fwd / attn_bwd; a null block_mask is
+ *   ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const uint8_t* block_mask, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                              float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, const float* delta, const uint8_t* block_mask, void* dq,
+                              void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int D, float scale,
+                              int causal, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
  * attn_bwd for callers that cannot allocate device memory.  (The pages have no

@@ -99,3 +99,28 @@ def test_status_strings(lib):
 def test_binding_raises_on_error(lib):
     with pytest.raises(gbattn.AttnError):
         gbattn._check(gbattn.ATTN_ERR_UNSUPPORTED, "attn_fwd", True)
+
+
+def fwd_masked(lib, mask=FAKE, D=128, Lq=300, Lk=300):
+    return lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, mask, 1, 4, 2, Lq, Lk, D, ctypes.c_float(0.1), 1, 1,
+                               None)
+
+
+def bwd_masked(lib, ptrs=None, D=128, Lq=300, Lk=300):
+    ptrs = ptrs or [FAKE] * 11
+    return lib.attn_bwd_masked(*ptrs, 1, 4, 2, Lq, Lk, D, ctypes.c_float(0.1), 1, 1, None)
+
+
+def test_masked_rejects_on_host(lib):
+    # the block mask is required (the unmasked calls serve a mask of all ones)
+    assert fwd_masked(lib, mask=None) == gbattn.ATTN_ERR_INVALID_ARG
+    # the mask is a byte array: any address is accepted for it, but not for the tensors
+    assert fwd_masked(lib, D=256) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_masked(lib, D=80) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_masked(lib, Lq=301, Lk=300) == gbattn.ATTN_ERR_INVALID_ARG
+    for i in range(11):
+        ptrs = [FAKE] * 11
+        ptrs[i] = None
+        assert bwd_masked(lib, ptrs) == gbattn.ATTN_ERR_INVALID_ARG
+    assert bwd_masked(lib, D=256) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert bwd_masked(lib, Lq=301, Lk=300) == gbattn.ATTN_ERR_INVALID_ARG

@@ -30,3 +30,13 @@ def test_kernel_flops_and_delta_bytes():
     assert F.kernel_flops("fwd", 1, 2, 4, 4, 8, True) == 2 * 8 * 2 * 2 * 10
     assert F.kernel_flops("bwd_dkv", 1, 1, 3, 3, 4, False) == 2 * 4 * 4 * 9
     assert F.delta_bytes(2, 3, 5, 64) == 2 * 30 * 64 * 2 + 4 * 30
+
+
+@pytest.mark.parametrize("Lq,Lk,causal,seed", [(300, 300, True, 1), (300, 900, True, 2), (500, 260, False, 3),
+                                               (1031, 1031, True, 4), (257, 129, False, 5)])
+def test_visible_pairs_masked_brute_force(Lq, Lk, causal, seed):
+    rng = np.random.default_rng(seed)
+    bm = (rng.random((-(-Lq // 128), -(-Lk // 128))) < 0.5).astype(np.uint8)
+    assert F.visible_pairs_masked(Lq, Lk, causal, bm) == int(A.visible(Lq, Lk, causal, bm).sum())
+    ones = np.ones_like(bm)
+    assert F.visible_pairs_masked(Lq, Lk, causal, ones) == F.visible_pairs(Lq, Lk, causal)
