@@ -7,7 +7,7 @@ is credited TFLOP/s: 3.5 x the forward FLOPs (4*B*Hq*Lq*Lk*D, halved for
 causal) over the summed device time of the step's kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--block-mask none|window:W|random:P]
+                    [--block-mask none|window:W|random:P] [--kv-capacity N]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload on its own GPU (weak scaling); the value is all ranks' work
@@ -17,7 +17,9 @@ the host cores instead, on a bounded sample of the same workload.
 With `--block-mask` the step runs the block-sparse entry points
 (attn_fwd_masked, attn_bwd_delta, attn_bwd_masked) and the metric credits
 3.5 x 4*D FLOPs per (query, key) pair the mask and the causal rule leave
-visible.
+visible.  With `--kv-capacity N` k and v are the first Lk rows of each head
+of an N-row cache whose other rows hold large stale values, and the step runs
+attn_fwd_ex / attn_bwd_ex.
 """
 
 from __future__ import annotations
@@ -277,8 +279,18 @@ def run_ours(args):
     sc, causal = w.scale, w.causal
     bm_np = block_mask(args.block_mask, w.Lq, w.Lk, seed=w.seed)
     bm = None if bm_np is None else torch.from_numpy(bm_np).to(dev)
+    kv_cap = args.kv_capacity
+    if kv_cap:
+        if kv_cap < w.Lk:
+            raise SystemExit(f"--kv-capacity {kv_cap} is below Lk = {w.Lk}")
+        caches = []
+        for t in (k, v):
+            c = torch.full((w.B, w.Hkv, kv_cap, w.D), 3.0e4, dtype=t.dtype, device=dev)
+            c[:, :, :w.Lk].copy_(t)
+            caches.append(c)
+        k, v = caches[0][:, :, :w.Lk], caches[1][:, :, :w.Lk]
 
-    if bm is None:
+    if bm is None and not kv_cap:
         phase_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
         calls = (
             lambda: gbattn.attn_fwd(q, k, v, o, lse, sc, causal, stream),
@@ -287,12 +299,13 @@ def run_ours(args):
             lambda: gbattn.attn_bwd_dq(q, k, v, do, lse, dlt, dq, sc, causal, stream),
         )
     else:
-        # attn_bwd_masked launches the dK/dV kernel, then the dQ kernel
+        # attn_bwd_ex launches the dK/dV kernel, then the dQ kernel
         phase_names = ("fwd", "delta", "bwd")
         calls = (
-            lambda: gbattn.attn_fwd_masked(q, k, v, o, lse, bm, sc, causal, stream),
+            lambda: gbattn.attn_fwd_ex(q, k, v, o, lse, sc, causal, block_mask=bm, stream=stream),
             lambda: gbattn.attn_bwd_delta(o, do, dlt, stream),
-            lambda: gbattn.attn_bwd_masked(q, k, v, o, do, lse, dlt, bm, dq, dk, dv, sc, causal, stream),
+            lambda: gbattn.attn_bwd_ex(q, k, v, o, do, lse, dlt, dq, dk, dv, sc, causal, block_mask=bm,
+                                       stream=stream),
         )
     n_ev = len(calls) + 1
 
@@ -354,7 +367,7 @@ def run_ours(args):
         kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
                       "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
                       "avg_ms": avg[n], "algorithmic": fl,
-                      "traffic": recorded_traffic(n, w.name) if bm is None else None}
+                      "traffic": recorded_traffic(n, w.name) if bm is None and not kv_cap else None}
     db = F.delta_bytes(w.B, w.Hq, w.Lq, w.D)
     ach = db / (avg["delta"] * 1e-3) / 1e9
     kernels["delta"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -367,14 +380,17 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not kv_cap:
         e2e = run_e2e(args, w, dev, stream, gbattn, credited, bm)
 
     n_dkv = 1 if w.D <= 128 else 2
     extra = {}
     if bm is not None:
         extra = {"block_mask": args.block_mask, "mask_blocks_kept": int(bm_np.sum()),
-                 "mask_blocks": int(bm_np.size), "visible_pairs_per_head": pairs}
+                 "mask_blocks": int(bm_np.size)}
+    if kv_cap:
+        extra["kv_capacity"] = kv_cap
+    extra["visible_pairs_per_head"] = pairs
     line = {
         "metric": METRIC if bm is None else METRIC_MASKED, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -386,6 +402,9 @@ def run_ours(args):
             **extra,
         }),
         "pct_of_bf16_peak": 100.0 * value / ws / peaks["bf16_tflops"],
+        # the same time with 3.5 x 4*D FLOPs credited per visible (query, key)
+        # pair instead of the half-rectangle convention (differs for Lq != Lk)
+        "tflops_visible_pairs": 3.5 * 4.0 * w.D * w.B * w.Hq * pairs * ws * args.steps / max_s / 1e12,
         "pct_of_bf16_peak_sustained": 100.0 * value / ws / peaks["bf16_tflops_sustained"],
         "peaks": peaks,
         "phase_ms": avg,
@@ -495,6 +514,8 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--block-mask", default="none",
                     help="block-sparse pattern: none, window:W (W key blocks of 128), random:P")
+    ap.add_argument("--kv-capacity", type=int, default=0,
+                    help="k/v as the first Lk rows of an N-row cache per head (0: contiguous)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")

@@ -139,29 +139,68 @@ int dispatch_delta(const AttnArgs& a) {
   }
 }
 
-}  // namespace
-}  // namespace gbattn
+// Row pitch of k and v: 0 (contiguous) or at least Lk, within the TMA
+// stride limit (2^40 bytes between heads).
+attn_status_t check_kv_pitch(int64_t kv_pitch, int Lk, int D) {
+  if (kv_pitch < 0 || (kv_pitch != 0 && kv_pitch < Lk)) return ATTN_ERR_INVALID_ARG;
+  if (kv_pitch > (int64_t{1} << 40) / (2 * D)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
 
-using namespace gbattn;
-
-extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                                  int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
-                                  cudaStream_t stream) {
+// Forward with an optional block mask (null = none) and K/V row pitch.
+attn_status_t fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
+                       int64_t kv_pitch, int B, int Hq, int Hkv, int Lq, int Lk, int D, float scale, int causal,
+                       attn_dtype_t dtype, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
-  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
   if (s != ATTN_OK) return s;
+  s = check_kv_pitch(kv_pitch, Lk, D);
+  if (s != ATTN_OK) return s;
+  if (block_mask && D > 128) return ATTN_ERR_UNSUPPORTED;
   AttnArgs a;
   int dev;
   const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
   if (ds != ATTN_OK) return ds;
-  a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse;
+  a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse, a.block_mask = block_mask, a.kv_pitch = kv_pitch;
   a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();
   return finish(dispatch_fwd(a));
 }
+
+// Backward (dK/dV kernel, then dQ kernel) with the same options.
+attn_status_t bwd_call(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                       const float* delta, const uint8_t* block_mask, int64_t kv_pitch, void* dq, void* dk, void* dv,
+                       int B, int Hq, int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !delta || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  s = check_kv_pitch(kv_pitch, Lk, D);
+  if (s != ATTN_OK) return s;
+  if (block_mask && D > 128) return ATTN_ERR_UNSUPPORTED;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta;
+  a.block_mask = block_mask, a.kv_pitch = kv_pitch;
+  a.dq = dq, a.dk = dk, a.dv = dv;
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dispatch_bwd(a));
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
 
 extern "C" attn_status_t attn_bwd_delta(const void* o, const void* dO, float* delta, int B, int Hq, int Lq, int D,
                                         attn_dtype_t dtype, cudaStream_t stream) {
@@ -179,26 +218,18 @@ extern "C" attn_status_t attn_bwd_delta(const void* o, const void* dO, float* de
   return finish(dispatch_delta(a));
 }
 
+extern "C" attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                  cudaStream_t stream) {
+  return fwd_call(q, k, v, o, lse, nullptr, 0, B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype, stream);
+}
+
 extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                   const float* lse, const float* delta, void* dq, void* dk, void* dv, int B, int Hq,
                                   int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
                                   cudaStream_t stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !delta || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
-      !aligned16(dv))
-    return ATTN_ERR_INVALID_ARG;
-  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
-  if (s != ATTN_OK) return s;
-  AttnArgs a;
-  int dev;
-  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
-  if (ds != ATTN_OK) return ds;
-  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta;
-  a.dq = dq, a.dk = dk, a.dv = dv;
-  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
-  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
-  a.stream = stream, a.limit_ns = wait_limit_ns();
-  return finish(dispatch_bwd(a));
+  return bwd_call(q, k, v, o, dO, lse, delta, nullptr, 0, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype,
+                  stream);
 }
 
 // Block-sparse variants: the same calls with a [ceil(Lq/128), ceil(Lk/128)]
@@ -206,21 +237,8 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
 extern "C" attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
                                          const uint8_t* block_mask, int B, int Hq, int Hkv, int Lq, int Lk, int D,
                                          float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse || !block_mask) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return ATTN_ERR_INVALID_ARG;
-  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
-  if (s != ATTN_OK) return s;
-  if (D > 128) return ATTN_ERR_UNSUPPORTED;
-  AttnArgs a;
-  int dev;
-  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
-  if (ds != ATTN_OK) return ds;
-  a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse, a.block_mask = block_mask;
-  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
-  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
-  a.stream = stream, a.limit_ns = wait_limit_ns();
-  return finish(dispatch_fwd(a));
+  if (!block_mask) return ATTN_ERR_INVALID_ARG;
+  return fwd_call(q, k, v, o, lse, block_mask, 0, B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype, stream);
 }
 
 extern "C" attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const void* o,
@@ -228,23 +246,26 @@ extern "C" attn_status_t attn_bwd_masked(const void* q, const void* k, const voi
                                          const uint8_t* block_mask, void* dq, void* dk, void* dv, int B, int Hq,
                                          int Hkv, int Lq, int Lk, int D, float scale, int causal, attn_dtype_t dtype,
                                          cudaStream_t stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !delta || !block_mask || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
-      !aligned16(dv))
-    return ATTN_ERR_INVALID_ARG;
-  const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
-  if (s != ATTN_OK) return s;
-  if (D > 128) return ATTN_ERR_UNSUPPORTED;
-  AttnArgs a;
-  int dev;
-  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
-  if (ds != ATTN_OK) return ds;
-  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta, a.block_mask = block_mask;
-  a.dq = dq, a.dk = dk, a.dv = dv;
-  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
-  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
-  a.stream = stream, a.limit_ns = wait_limit_ns();
-  return finish(dispatch_bwd(a));
+  if (!block_mask) return ATTN_ERR_INVALID_ARG;
+  return bwd_call(q, k, v, o, dO, lse, delta, block_mask, 0, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, scale, causal,
+                  dtype, stream);
+}
+
+// Every option at once: an optional block mask (null = none) and the row
+// pitch of k and v (0 = Lk, i.e. contiguous; larger when they are the first
+// Lk rows of each head of a longer cache).
+extern "C" attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const uint8_t* block_mask, int64_t kv_pitch, int B, int Hq, int Hkv, int Lq,
+                                     int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
+  return fwd_call(q, k, v, o, lse, block_mask, kv_pitch, B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype, stream);
+}
+
+extern "C" attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                     const float* lse, const float* delta, const uint8_t* block_mask,
+                                     int64_t kv_pitch, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq,
+                                     int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
+  return bwd_call(q, k, v, o, dO, lse, delta, block_mask, kv_pitch, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, scale,
+                  causal, dtype, stream);
 }
 
 // The two halves of attn_bwd, for callers that run them on separate streams.

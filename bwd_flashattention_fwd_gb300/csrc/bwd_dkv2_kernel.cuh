@@ -268,14 +268,15 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const int qmin = kj - p.off;  // causal: queries below this index cannot see key kj
-    const size_t krow = static_cast<size_t>(bhk) * p.Lk + kj;
+    const size_t krow = static_cast<size_t>(bhk) * p.Lk + kj;  // row of dK / dV
+    const size_t kin = static_cast<size_t>(bhk) * p.kv_pitch + kj;  // row of K
     // K row into tensor memory: this warp copies columns [half*D/2,
     // (half+1)*D/2) of its 32 key rows (zeros past Lk), as 16-bit pairs.
     {
       constexpr int HALF = D / 2;   // elements per thread
       constexpr int NV = HALF / 8;  // 16-byte loads per thread
       const uint4* src =
-          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(k) + krow * D + half * HALF);
+          reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(k) + kin * D + half * HALF);
       uint32_t ka[HALF / 2];
 #pragma unroll
       for (int v = 0; v < NV; ++v) {

@@ -25,14 +25,17 @@ namespace GBATTN_CAT(inst_d, GBATTN_HEAD_DIM) {
 
 constexpr int kD = GBATTN_HEAD_DIM;
 
-// Rank-3 view [B*H, L, D] of a contiguous [B, H, L, D] tensor; boxes of
+// Rank-3 view [B*H, L, D] of a [B, H, pitch, D] tensor (contiguous when
+// pitch = L; a slice of the first L rows of each head otherwise); boxes of
 // 64 columns x box_rows rows with the 128-byte swizzle the MMA descriptors
-// expect.  Rows past L (and columns past D) read as zeros.
-bool make_map(const AttnArgs& a, CUtensorMap* m, const void* base, int L, int BH, int box_rows) {
+// expect.  Rows past L (and columns past D) read as zeros, so rows behind a
+// slice are never read.
+bool make_map(const AttnArgs& a, CUtensorMap* m, const void* base, int L, int BH, int box_rows,
+              int64_t pitch = 0) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                                 static_cast<cuuint64_t>(kD) * 2 * static_cast<cuuint64_t>(L)};
+  const cuuint64_t rows = static_cast<cuuint64_t>(pitch > 0 ? pitch : L);
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(kD) * 2 * rows};
   const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
   const CUresult r = a.encode(m, a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -65,8 +68,8 @@ template <bool BF16, bool CAUSAL, bool MASKED>
 int fwd2_impl(const AttnArgs& a) {
   using Gm = Fwd2Geom<(kD <= 128 ? kD : 128)>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   FwdParams p{};
   p.o = a.o_out;
@@ -94,8 +97,8 @@ int fwd_impl(const AttnArgs& a) {
   } else {
   using Gm = FwdGeom<kD>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   FwdParams p{};
   p.o = a.o_out;
@@ -127,6 +130,7 @@ BwdParams bwd_params(const AttnArgs& a) {
   p.limit_ns = a.limit_ns;
   p.bmask = a.block_mask;
   p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
+  p.kv_pitch = a.kv_pitch > 0 ? a.kv_pitch : a.Lk;
   return p;
 }
 
@@ -135,7 +139,7 @@ int dkv_impl(const AttnArgs& a) {
   using Gm = DkvGeom<kD, MODE>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -152,7 +156,7 @@ int dkv2_impl(const AttnArgs& a) {
   using Gm = Dkv2Geom<DD>;
   CUtensorMap tq, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -172,7 +176,7 @@ int dq3_impl(const AttnArgs& a) {
   using Gm = Dq3Geom<DD>;
   CUtensorMap tq, tdo, tk, tv;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -196,7 +200,7 @@ int dq_impl(const AttnArgs& a) {
   using Gm = DqGeom<kD>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK))
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;

@@ -51,6 +51,7 @@ struct BwdParams {
   // block-sparse variant: uint8 [ceil(Lq/128), ceil(Lk/128)], row-major
   const uint8_t* bmask;
   int nkb;  // ceil(Lk / 128): row length of the mask
+  int64_t kv_pitch;  // rows between consecutive heads of k and v (>= Lk)
 };
 
 // Block-mask entry (query block qb, key block kb); nonzero keeps the pair.

@@ -39,6 +39,8 @@ struct AttnArgs {
   EncodeTiledFn encode = nullptr;
   // block-sparse variant: uint8 [ceil(Lq/128), ceil(Lk/128)] on the device, or null
   const uint8_t* block_mask = nullptr;
+  // rows between consecutive (b, hk) heads of k and v; 0 = Lk (contiguous)
+  int64_t kv_pitch = 0;
 };
 
 // Launch results: 0 = launched, 1 = tensor-map encoding rejected the

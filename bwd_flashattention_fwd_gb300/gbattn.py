@@ -24,8 +24,9 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc", "attn_fwd_masked", "attn_bwd_masked",
-            "attn_last_device_status", "attn_status_string")
+EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc",
+            "attn_fwd_masked", "attn_bwd_masked", "attn_fwd_ex", "attn_bwd_ex", "attn_last_device_status",
+            "attn_status_string")
 
 _lib = None
 
@@ -63,6 +64,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_masked.restype = ci
     lib.attn_bwd_masked.argtypes = [vp] * 11 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.attn_bwd_masked.restype = ci
+    i64 = ctypes.c_int64
+    lib.attn_fwd_ex.argtypes = [vp] * 6 + [i64, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_fwd_ex.restype = ci
+    lib.attn_bwd_ex.argtypes = [vp] * 8 + [i64] + [vp] * 3 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd_ex.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -180,6 +186,45 @@ def attn_bwd_masked(q, k, v, o, dO, lse, delta, block_mask, dq, dk, dv, scale: f
                                         _ptr(block_mask), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D,
                                         float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
     return _check(st, "attn_bwd_masked", check)
+
+
+def kv_row_pitch(k, v) -> int:
+    """Row pitch of k and v for attn_fwd_ex / attn_bwd_ex: 0 when both are
+    contiguous, else the capacity P of a [B, Hkv, P, D] buffer they are the
+    first Lk rows of (cache[:, :, :Lk, :]).  Any other layout is rejected."""
+    if k.is_contiguous() and v.is_contiguous():
+        return 0
+    B, Hkv, Lk, D = k.shape
+    st = k.stride()
+    if st[3] != 1 or st[2] != D or st[1] % D or st[0] != Hkv * st[1] or tuple(v.stride()) != tuple(st):
+        raise ValueError(f"k/v strides {tuple(k.stride())}, {tuple(v.stride())} are not a slice of a "
+                         f"[B, Hkv, capacity, D] cache")
+    return st[1] // D
+
+
+def attn_fwd_ex(q, k, v, o, lse, scale: float, causal: bool, block_mask=None, kv_pitch=None, stream=None,
+                check: bool = True) -> int:
+    """attn_fwd with an optional block mask and k / v sliced from a longer
+    cache (kv_pitch None: taken from the tensors' strides)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    pitch = kv_row_pitch(k, v) if kv_pitch is None else int(kv_pitch)
+    st = load_library().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(block_mask), pitch, B, Hq,
+                                    Hkv, Lq, Lk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                                    _stream_handle(stream))
+    return _check(st, "attn_fwd_ex", check)
+
+
+def attn_bwd_ex(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bool, block_mask=None, kv_pitch=None,
+                stream=None, check: bool = True) -> int:
+    """attn_bwd with the options of attn_fwd_ex (dk, dv contiguous)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    pitch = kv_row_pitch(k, v) if kv_pitch is None else int(kv_pitch)
+    st = load_library().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
+                                    _ptr(block_mask), pitch, _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D,
+                                    float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_bwd_ex", check)
 
 
 def attn_last_device_status(stream=None) -> int:

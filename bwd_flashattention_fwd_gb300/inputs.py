@@ -47,7 +47,10 @@ class Workload:
         return replace(self, **kw)
 
 
-# The five workloads, shaped like the ones the pages measure or describe.
+# The workloads, shaped like the ones the pages measure or describe.  The
+# last two are long-cache rectangles (few query rows against a long key
+# range; "Add a fused full-attention path for head_dim 256 on NAX devices",
+# section "Kernel benchmarks", 1024 x 8192 and 2048 x 8192).
 WORKLOADS = {
     w.name: w
     for w in [
@@ -59,6 +62,8 @@ WORKLOADS = {
             "ragged_mha_q4064_k4112_d96",
             B=4, Hq=16, Hkv=16, Lq=4064, Lk=4112, D=96, dtype="fp16", std=0.5, seed=1004,
         ),
+        Workload("longcache_q1024_k8192_d128", B=1, Hq=32, Hkv=8, Lq=1024, Lk=8192, D=128, seed=1006),
+        Workload("longcache_q2048_k8192_d256", B=1, Hq=16, Hkv=2, Lq=2048, Lk=8192, D=256, seed=1007),
     ]
 }
 

@@ -138,6 +138,31 @@ attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const
                               int causal, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * K and V sliced out of a longer key/value cache ("Add a fused full-attention
+ * path for head_dim 256 on NAX devices", section "Ragged causal inputs": a
+ * preallocated cache holds more positions per head than the call uses, so
+ * the call's keys are keys[..., :Lk, :] of a [B, Hkv, capacity, D] buffer).
+ * attn_fwd_ex / attn_bwd_ex are attn_fwd / attn_bwd with two options:
+ *   block_mask: as for attn_fwd_masked, or NULL for no block mask.
+ *   kv_pitch: rows between the starts of consecutive (b, hk) heads of k and v,
+ *     i.e. the cache capacity; 0 means Lk (contiguous k and v).  Element
+ *     (b, hk, j, d) of k is read at k + ((b*Hkv + hk)*kv_pitch + j)*D + d, for
+ *     j < Lk only: rows j >= Lk of the cache (stale entries) are never read,
+ *     whatever they hold.  dk and dv are written contiguous [B,Hkv,Lk,D].
+ *   Errors: kv_pitch < 0 or 0 < kv_pitch < Lk is ATTN_ERR_INVALID_ARG; a pitch
+ *   of 2^40 bytes or more per head is ATTN_ERR_UNSUPPORTED; a block mask with
+ *   D = 256 is ATTN_ERR_UNSUPPORTED.  Everything else as for attn_fwd /
+ *   attn_bwd.  Pass attn_bwd_ex the lse of attn_fwd_ex with the same options.
+ */
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const uint8_t* block_mask, int64_t kv_pitch, int B, int Hq, int Hkv, int Lq,
+                          int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                          const float* lse, const float* delta, const uint8_t* block_mask, int64_t kv_pitch,
+                          void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                          float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * attn_bwd for callers that cannot allocate device memory.  (The pages have no
  * counterpart: this is an entry point of this library only.)
  *

@@ -124,3 +124,41 @@ def test_masked_rejects_on_host(lib):
         assert bwd_masked(lib, ptrs) == gbattn.ATTN_ERR_INVALID_ARG
     assert bwd_masked(lib, D=256) == gbattn.ATTN_ERR_UNSUPPORTED
     assert bwd_masked(lib, Lq=301, Lk=300) == gbattn.ATTN_ERR_INVALID_ARG
+
+
+def fwd_ex(lib, mask=None, pitch=0, D=128, Lq=300, Lk=300):
+    return lib.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, mask, pitch, 1, 4, 2, Lq, Lk, D, ctypes.c_float(0.1), 1, 1,
+                           None)
+
+
+def bwd_ex(lib, ptrs=None, mask=None, pitch=0, D=128, Lq=300, Lk=300):
+    ptrs = ptrs or [FAKE] * 10
+    return lib.attn_bwd_ex(*ptrs[:7], mask, pitch, *ptrs[7:], 1, 4, 2, Lq, Lk, D, ctypes.c_float(0.1), 1, 1, None)
+
+
+def test_ex_rejects_on_host(lib):
+    assert fwd_ex(lib, pitch=-1) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_ex(lib, pitch=299) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_ex(lib, pitch=1 << 40) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_ex(lib, mask=FAKE, D=256) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_ex(lib, D=80) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_ex(lib, Lq=301) == gbattn.ATTN_ERR_INVALID_ARG
+    for i in range(10):
+        ptrs = [FAKE] * 10
+        ptrs[i] = None
+        assert bwd_ex(lib, ptrs) == gbattn.ATTN_ERR_INVALID_ARG
+    assert bwd_ex(lib, pitch=100) == gbattn.ATTN_ERR_INVALID_ARG
+    assert bwd_ex(lib, mask=FAKE, D=256) == gbattn.ATTN_ERR_UNSUPPORTED
+
+
+def test_kv_row_pitch_from_strides():
+    import torch
+
+    cache = torch.empty((2, 3, 40, 64), dtype=torch.bfloat16)
+    k = cache[:, :, :25]
+    assert gbattn.kv_row_pitch(k, cache[:, :, :25]) == 40
+    assert gbattn.kv_row_pitch(cache, cache) == 0
+    with pytest.raises(ValueError):
+        gbattn.kv_row_pitch(cache[:, :, :, :32], cache[:, :, :, :32])
+    with pytest.raises(ValueError):
+        gbattn.kv_row_pitch(k, cache.transpose(1, 2)[:, :25])

@@ -255,7 +255,8 @@ def oracle_head_output(qd, kd, vd, w, b, hq):
 
 
 FULL = [WORKLOADS[n] for n in ("llama_gqa_l2048_d128", "qwen3_8b_gqa_l8192_d128", "gqa_l8192_d256",
-                               "ragged_mha_q4064_k4112_d96")]
+                               "ragged_mha_q4064_k4112_d96", "longcache_q1024_k8192_d128",
+                               "longcache_q2048_k8192_d256")]
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
