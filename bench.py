@@ -7,7 +7,7 @@ is credited TFLOP/s: 3.5 x the forward FLOPs (4*B*Hq*Lq*Lk*D, halved for
 causal) over the summed device time of the step's kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--block-mask none|window:W|random:P] [--kv-capacity N]
+                    [--block-mask none|window:W|random:P] [--kv-capacity N] [--decode]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload on its own GPU (weak scaling); the value is all ranks' work
@@ -19,7 +19,9 @@ With `--block-mask` the step runs the block-sparse entry points
 3.5 x 4*D FLOPs per (query, key) pair the mask and the causal rule leave
 visible.  With `--kv-capacity N` k and v are the first Lk rows of each head
 of an N-row cache whose other rows hold large stale values, and the step runs
-attn_fwd_ex / attn_bwd_ex.
+attn_fwd_ex / attn_bwd_ex.  With `--decode` (short query lengths) the step
+runs attn_fwd_decode, attn_bwd_delta and attn_bwd_decode, and the roofline
+is HBM bytes (the key/value range read and the gradients written).
 """
 
 from __future__ import annotations
@@ -290,7 +292,17 @@ def run_ours(args):
             caches.append(c)
         k, v = caches[0][:, :, :w.Lk], caches[1][:, :, :w.Lk]
 
-    if bm is None and not kv_cap:
+    if args.decode:
+        if bm is not None or kv_cap:
+            raise SystemExit("--decode takes neither --block-mask nor --kv-capacity")
+        ws_dec = gbattn.decode_workspace(q, k)
+        phase_names = ("fwd", "delta", "bwd")
+        calls = (
+            lambda: gbattn.attn_fwd_decode(q, k, v, o, lse, ws_dec, sc, causal, stream),
+            lambda: gbattn.attn_bwd_delta(o, do, dlt, stream),
+            lambda: gbattn.attn_bwd_decode(q, k, v, o, do, lse, dlt, dq, dk, dv, ws_dec, sc, causal, stream),
+        )
+    elif bm is None and not kv_cap:
         phase_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
         calls = (
             lambda: gbattn.attn_fwd(q, k, v, o, lse, sc, causal, stream),
@@ -362,6 +374,12 @@ def run_ours(args):
     kernels = {}
     mm_phases = [n for n in phase_names if n != "delta"]
     for n in mm_phases:
+        if args.decode:  # bound by the key/value range read
+            by = F.decode_bytes(n, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D)
+            ach = by / (avg[n] * 1e-3) / 1e9
+            kernels[n] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": ach / peaks["hbm_gbs"], "avg_ms": avg[n], "algorithmic": by, "traffic": None}
+            continue
         fl = F.kernel_flops_pairs(n, w.B, w.Hq, w.D, pairs)
         ach = fl / (avg[n] * 1e-3) / 1e12
         kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
@@ -380,7 +398,7 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e and not kv_cap:
+    if not args.no_e2e and not kv_cap and not args.decode:
         e2e = run_e2e(args, w, dev, stream, gbattn, credited, bm)
 
     n_dkv = 1 if w.D <= 128 else 2
@@ -390,6 +408,8 @@ def run_ours(args):
                  "mask_blocks": int(bm_np.size)}
     if kv_cap:
         extra["kv_capacity"] = kv_cap
+    if args.decode:
+        extra["path"] = "decode (packed GQA rows, split key range)"
     extra["visible_pairs_per_head"] = pairs
     line = {
         "metric": METRIC if bm is None else METRIC_MASKED, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -411,7 +431,9 @@ def run_ours(args):
         "roofline": roof,
         "kernels": kernels,
         "e2e": e2e,
-        "gpu_launches": args.steps * (1 + 1 + n_dkv + 1),
+        # fwd, delta, dK/dV (two kernels at D = 256), dQ; the decode path adds
+        # the combine and the dQ reduction
+        "gpu_launches": args.steps * (1 + 1 + n_dkv + 1 + (2 if args.decode else 0)),
         "clocks": clk,
         "wall_s_timed_region": t_wall,
         "kernel_source_hash": kernel_source_hash(),
@@ -516,6 +538,7 @@ def main(argv=None) -> int:
                     help="block-sparse pattern: none, window:W (W key blocks of 128), random:P")
     ap.add_argument("--kv-capacity", type=int, default=0,
                     help="k/v as the first Lk rows of an N-row cache per head (0: contiguous)")
+    ap.add_argument("--decode", action="store_true", help="short-query path (attn_fwd_decode / attn_bwd_decode)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")

@@ -130,6 +130,30 @@ int dispatch_bwd_dkv(const AttnArgs& a) {
     default: return launch_bwd_dkv_d256(a);
   }
 }
+int dispatch_fwd_decode(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_fwd_decode_d64(a);
+    case 96: return launch_fwd_decode_d96(a);
+    case 128: return launch_fwd_decode_d128(a);
+    default: return launch_fwd_decode_d256(a);
+  }
+}
+int dispatch_bwd_dkv_decode(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_bwd_dkv_decode_d64(a);
+    case 96: return launch_bwd_dkv_decode_d96(a);
+    case 128: return launch_bwd_dkv_decode_d128(a);
+    default: return launch_bwd_dkv_decode_d256(a);
+  }
+}
+int dispatch_bwd_dq_decode(const AttnArgs& a) {
+  switch (a.D) {
+    case 64: return launch_bwd_dq_decode_d64(a);
+    case 96: return launch_bwd_dq_decode_d96(a);
+    case 128: return launch_bwd_dq_decode_d128(a);
+    default: return launch_bwd_dq_decode_d256(a);
+  }
+}
 int dispatch_delta(const AttnArgs& a) {
   switch (a.D) {
     case 64: return launch_delta_d64(a);
@@ -195,6 +219,16 @@ attn_status_t bwd_call(const void* q, const void* k, const void* v, const void* 
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();
   return finish(dispatch_bwd(a));
+}
+
+// Decode calls: the packed tile (G * Lq rows) must fit 128 rows, and the
+// caller's workspace must hold the split partials.
+attn_status_t check_decode(int B, int Hq, int Hkv, int Lq, int Lk, int D, const void* ws, size_t ws_bytes) {
+  if (static_cast<long long>(Hq / Hkv) * Lq > kDecodeMaxRows) return ATTN_ERR_UNSUPPORTED;
+  if (!ws || !aligned16(ws)) return ATTN_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * Hq * Lq;
+  if (ws_bytes < decode_workspace_bytes(B, Hkv, rows, Lk, D)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
 }
 
 }  // namespace
@@ -266,6 +300,62 @@ extern "C" attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v
                                      int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {
   return bwd_call(q, k, v, o, dO, lse, delta, block_mask, kv_pitch, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, scale,
                   causal, dtype, stream);
+}
+
+// Decode-shaped attention (short query lengths, "feat(attention): complete
+// Flash Attention VJP implementation": the vector kernels for L <= 8).
+extern "C" size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D) {
+  if (check_attention(B, Hq, Hkv, Lq, Lk, D, 1.f, 0, ATTN_DTYPE_BF16) != ATTN_OK) return 0;
+  if (static_cast<long long>(Hq / Hkv) * Lq > kDecodeMaxRows) return 0;
+  return decode_workspace_bytes(B, Hkv, static_cast<long long>(B) * Hq * Lq, Lk, D);
+}
+
+extern "C" attn_status_t attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                                         void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Lq,
+                                         int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                         cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  s = check_decode(B, Hq, Hkv, Lq, Lk, D, workspace, workspace_bytes);
+  if (s != ATTN_OK) return s;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse, a.workspace = static_cast<float*>(workspace);
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  return finish(dispatch_fwd_decode(a));
+}
+
+extern "C" attn_status_t attn_bwd_decode(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                         const float* lse, const float* delta, void* dq, void* dk, void* dv,
+                                         void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Lq,
+                                         int Lk, int D, float scale, int causal, attn_dtype_t dtype,
+                                         cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !delta || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  s = check_decode(B, Hq, Hkv, Lq, Lk, D, workspace, workspace_bytes);
+  if (s != ATTN_OK) return s;
+  AttnArgs a;
+  int dev;
+  const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
+  if (ds != ATTN_OK) return ds;
+  a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta, a.dq = dq, a.dk = dk, a.dv = dv;
+  a.workspace = static_cast<float*>(workspace);
+  a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
+  a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.stream = stream, a.limit_ns = wait_limit_ns();
+  const int r = dispatch_bwd_dkv_decode(a);
+  return finish(r == kLaunchOk ? dispatch_bwd_dq_decode(a) : r);
 }
 
 // The two halves of attn_bwd, for callers that run them on separate streams.

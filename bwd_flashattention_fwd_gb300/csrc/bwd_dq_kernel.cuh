@@ -24,6 +24,12 @@
 // 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each tile;
 // warp 8 TMA producer; warp 9 issues S / dP and owns the TMEM allocation;
 // warp 10 issues dQ += dS K.
+//
+// DECODE (short query lengths): as in the forward kernel, one packed tile
+// holds the G query heads x Lq rows of a KV head (row r is query r % Lq) and
+// CTA (x, y) covers key tiles [y*split_tiles, ...); it writes its fp32 share
+// of dS K per row, and a reduction kernel sums the shares and applies the
+// scale.  P uses the final lse, so the shares simply add.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -57,7 +63,7 @@ struct DqGeom {
   static_assert(DP_COL + 2 * BK <= TMEM_COLS, "tensor memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DECODE = false>
 __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -83,11 +89,13 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
   const int hk = hq / p.G;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
+  const int qt = DECODE ? 0 : p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
   const int q0 = qt * BQ;
   const int q_hi = min(q0 + BQ, p.Lq);
   const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
-  const int n_kv = (kv_end + BK - 1) / BK;
+  // key tiles [j0, j0 + n_kv) of this CTA
+  const int j0 = DECODE ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
+  const int n_kv = DECODE ? min((kv_end + BK - 1) / BK - j0, p.split_tiles) : (kv_end + BK - 1) / BK;
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -139,12 +147,14 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, j * BK, zkv);
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64,
+                      (j0 + j) * BK, zkv);
       if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 18);
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, j * BK, zkv);
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64,
+                      (j0 + j) * BK, zkv);
     }
     for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
       mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
@@ -222,14 +232,15 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
     const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
     const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
-    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
+    const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
     for (int j = 0; j < n_kv; ++j) {
       const int buf = j & 1;
       mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 16);
       __syncwarp();
       tc_fence_after_sync();
-      const int kc0 = j * BK + half * 32;  // first key of this thread's columns
-      const bool need_mask = (CAUSAL && (j * BK + BK - 1 > q0 + p.off)) || (j * BK + BK > p.Lk);
+      const int k0 = (j0 + j) * BK;
+      const int kc0 = k0 + half * 32;  // first key of this thread's columns
+      const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
       const uint32_t scol = tmem + lrow + Gm::S_COL + buf * BK + half * 32;
       uint32_t sr[32], dr[32];
       tmem_ld32(scol, sr);
@@ -257,13 +268,25 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     mbar_wait(smem_u32(&bar_dqdone), 0, g, kDevTimeoutBase + 17);
     __syncwarp();
     tc_fence_after_sync();
-    typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
+    if constexpr (DECODE) {
+      // this split's share of row bh * Lq + qi, unscaled
+      float* dst = p.ws + ((static_cast<size_t>(blockIdx.y) * gridDim.x + bh) * p.Lq + qi) * D;
 #pragma unroll 1
-    for (int c = half; c < D / 32; c += 2) {
-      uint32_t rr[32];
-      tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
-      tmem_ld_wait(rr);
-      if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+      for (int c = half; c < D / 32; c += 2) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (qi < p.Lq) store_row32_f32(dst + c * 32, rr, 1.f);
+      }
+    } else {
+      typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
+#pragma unroll 1
+      for (int c = half; c < D / 32; c += 2) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+      }
     }
   }
 

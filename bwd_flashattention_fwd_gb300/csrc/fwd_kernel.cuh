@@ -17,6 +17,14 @@
 // each, fp32) and two P buffers (BK/2 columns, bf16/fp16 pairs).  S_j = Q K_j^T
 // runs on the tensor cores while the softmax warps turn S_{j-1} into P_{j-1};
 // O += P_j V_j reads P straight from tensor memory.
+//
+// DECODE (short query lengths): the G query heads x Lq rows of one KV head
+// (consecutive in the [B, Hq, Lq, D] layout) form one packed tile; packed row
+// r is query r % Lq.  CTA (x, y) covers key tiles [y*split_tiles, ...) of
+// KV head x and writes each row's partial O (normalised by its own sum) and
+// partial base-2 log-sum-exp in fp32; a combine kernel merges the splits
+// (the online-softmax merge of "When the Bottleneck Moved", section 3, applied
+// across CTAs).  A row may see no key of its split: its partial lse is -inf.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -44,7 +52,7 @@ struct FwdGeom {
   static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DECODE = false>
 __global__ void __launch_bounds__(192, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -64,14 +72,16 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sK0 = sQ + Gm::Q_BYTES;
   const uint32_t sV0 = sK0 + ST * Gm::KV_BYTES;
 
-  const int bh = blockIdx.x;  // b * Hq + hq
+  const int bh = blockIdx.x;  // b * Hq + hq (decode: b * Hkv + hk, with Hq = Hkv, G = 1)
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
   const int hk = hq / p.G;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
+  const int qt = DECODE ? 0 : p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
   const int q0 = qt * BQ;
   const int q_hi = min(q0 + BQ, p.Lq);
   const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
-  const int n_kv = (kv_end + BK - 1) / BK;
+  // key tiles [j0, j0 + n_kv) of this CTA
+  const int j0 = DECODE ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
+  const int n_kv = DECODE ? min((kv_end + BK - 1) / BK - j0, p.split_tiles) : (kv_end + BK - 1) / BK;
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -116,10 +126,12 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[s]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64, j * BK, zkv);
+        tma_load_3d_w(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64, (j0 + j) * BK,
+                      zkv);
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[s]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64, j * BK, zkv);
+        tma_load_3d_w(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64, (j0 + j) * BK,
+                      zkv);
     }
     // Do not leave the CTA while a copy may still be landing.
     for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = p.scale_log2;
     // last visible key of this row (inclusive)
-    const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
+    const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < n_kv; ++j) {
       mbar_wait(smem_u32(&bar_sfull[j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 6);
@@ -192,7 +204,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]) * sl2;
       }
-      const int k0 = j * BK;
+      const int k0 = (j0 + j) * BK;
       const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
       if (need_mask) {
 #pragma unroll
@@ -203,7 +215,9 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int i = 1; i < BK; ++i) mt = fmaxf(mt, x[i]);
       const float m_new = fmaxf(m, mt);
-      const float alpha = ex2_approx(m - m_new);
+      // (decode: a row that has seen no key of its split keeps m = -inf, P = 0)
+      const float mu = (DECODE && m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m - mu);
       float sum = 0.f;
       const uint32_t pcol = tmem + lrow + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
 #pragma unroll
@@ -211,8 +225,8 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(x[c * 32 + 2 * i] - m_new);
-          const float p1 = ex2_approx(x[c * 32 + 2 * i + 1] - m_new);
+          const float p0 = ex2_approx(x[c * 32 + 2 * i] - mu);
+          const float p1 = ex2_approx(x[c * 32 + 2 * i + 1] - mu);
           sum += p0 + p1;
           pk[i] = E::pack(p0, p1);
         }
@@ -245,16 +259,31 @@ __global__ void __launch_bounds__(192, 1)
     mbar_wait(smem_u32(&bar_odone), (n_kv - 1) & 1, g, kDevTimeoutBase + 8);
     __syncwarp();
     tc_fence_after_sync();
-    const float inv_l = 1.f / l;
-    typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
+    if constexpr (DECODE) {
+      // partial row (split y, packed row bh * Lq + qi) of the combine input
+      const bool empty = !(l > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / l;
+      const size_t x = (static_cast<size_t>(blockIdx.y) * gridDim.x + bh) * p.Lq + qi;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t rr[32];
-      tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
-      tmem_ld_wait(rr);
-      if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (qi < p.Lq) store_row32_f32(p.ws + x * D + c * 32, rr, inv_l);
+      }
+      if (qi < p.Lq) p.ws_lse[x] = empty ? -INFINITY : m + log2f(l);
+    } else {
+      const float inv_l = 1.f / l;
+      typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+        if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
+      }
+      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
     }
-    if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
   }
 
   tc_fence_before_sync();

@@ -7,6 +7,7 @@
 #include "bwd_dkv_kernel.cuh"
 #include "bwd_dq3_kernel.cuh"
 #include "bwd_dq_kernel.cuh"
+#include "decode_kernel.cuh"
 #include "delta_kernel.cuh"
 #include "fwd2_kernel.cuh"
 #include "fwd_kernel.cuh"
@@ -68,7 +69,8 @@ template <bool BF16, bool CAUSAL, bool MASKED>
 int fwd2_impl(const AttnArgs& a) {
   using Gm = Fwd2Geom<(kD <= 128 ? kD : 128)>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
       !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   FwdParams p{};
@@ -97,7 +99,8 @@ int fwd_impl(const AttnArgs& a) {
   } else {
   using Gm = FwdGeom<kD>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
       !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   FwdParams p{};
@@ -139,7 +142,8 @@ int dkv_impl(const AttnArgs& a) {
   using Gm = DkvGeom<kD, MODE>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -176,7 +180,8 @@ int dq3_impl(const AttnArgs& a) {
   using Gm = Dq3Geom<DD>;
   CUtensorMap tq, tdo, tk, tv;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -200,7 +205,8 @@ int dq_impl(const AttnArgs& a) {
   using Gm = DqGeom<kD>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) || !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -225,6 +231,103 @@ template <bool BF16, bool CAUSAL>
 int bwd_impl(const AttnArgs& a) {
   const int r = dkv_all<BF16, CAUSAL>(a);
   return r == kLaunchOk ? dq_impl<BF16, CAUSAL>(a) : r;
+}
+
+// Decode-shaped forward (G * Lq <= 128): the single-tile forward kernel on
+// packed tiles, its key range split over CTAs, then the combine kernel.
+template <bool BF16, bool CAUSAL>
+int fwd_decode_impl(const AttnArgs& a) {
+  using Gm = FwdGeom<kD>;
+  const int R = (a.Hq / a.Hkv) * a.Lq;  // packed rows of one KV head
+  const long long groups = static_cast<long long>(a.B) * a.Hkv;
+  const long long nrows = groups * R;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(a, &tq, a.q, R, a.B * a.Hkv, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+    return kLaunchBadMap;
+  const DecodeSplit sp = decode_split(groups, decode_fwd_tiles(a.Lk, kD));
+  FwdParams p{};
+  p.status = a.status;
+  p.B = a.B, p.Hq = a.Hkv, p.Hkv = a.Hkv, p.Lq = R, p.Lk = a.Lk, p.G = 1;
+  p.off = a.Lk - a.Lq;  // from the true query length
+  p.n_qtiles = 1;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.limit_ns = a.limit_ns;
+  p.qmod = a.Lq;
+  p.split_tiles = sp.tiles_per_split;
+  p.ws = a.workspace;
+  p.ws_lse = a.workspace + static_cast<size_t>(sp.n_split) * nrows * kD;
+  const dim3 grid(static_cast<unsigned>(groups), sp.n_split);
+  const int r = launch(attn_fwd_kernel<kD, BF16, CAUSAL, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq,
+                       tk, tv, p);
+  if (r != kLaunchOk) return r;
+  const long long blocks = (nrows + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+  attn_decode_combine_kernel<kD, BF16><<<static_cast<unsigned>(blocks), kCombineThreads, 0, a.stream>>>(
+      p.ws, p.ws_lse, sp.n_split, nrows, a.o_out, a.lse_out);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
+// Decode-shaped dQ: the single-tile dQ kernel on packed tiles, its key range
+// split over CTAs, then the reduction of the fp32 shares.
+template <bool BF16, bool CAUSAL>
+int dq_decode_impl(const AttnArgs& a) {
+  using Gm = DqGeom<kD>;
+  const int R = (a.Hq / a.Hkv) * a.Lq;
+  const long long groups = static_cast<long long>(a.B) * a.Hkv;
+  const long long nrows = groups * R;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(a, &tq, a.q, R, a.B * a.Hkv, Gm::BQ) || !make_map(a, &tdo, a.dO, R, a.B * a.Hkv, Gm::BQ) ||
+      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+    return kLaunchBadMap;
+  const DecodeSplit sp = decode_split(groups, decode_dq_tiles(a.Lk));
+  BwdParams p = bwd_params(a);  // off = Lk - Lq from the true query length
+  p.Hq = a.Hkv, p.Lq = R, p.G = 1;
+  p.n_qtiles = 1;
+  p.n_ktiles = decode_dq_tiles(a.Lk);
+  p.qmod = a.Lq;
+  p.split_tiles = sp.tiles_per_split;
+  p.ws = a.workspace;
+  const dim3 grid(static_cast<unsigned>(groups), sp.n_split);
+  const int r = launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
+                       tq, tk, tv, tdo, p);
+  if (r != kLaunchOk) return r;
+  const long long n4 = nrows * kD / 4;
+  long long blocks = (n4 + kReduceThreads - 1) / kReduceThreads;
+  const long long cap = static_cast<long long>(a.num_sms > 0 ? a.num_sms : 152) * 8;
+  if (blocks > cap) blocks = cap;
+  attn_decode_dq_reduce_kernel<kD, BF16><<<static_cast<unsigned>(blocks), kReduceThreads, 0, a.stream>>>(
+      p.ws, sp.n_split, nrows, a.scale, a.dq);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
+// Decode-shaped dK/dV: D <= 128 runs the dK/dV kernel on packed query tiles
+// (G * Lq rows of one KV head); D = 256 the general pair of kernels.
+template <bool BF16, bool CAUSAL>
+int dkv_decode_impl(const AttnArgs& a) {
+  if constexpr (kD <= 128) {
+    constexpr int DD = kD <= 128 ? kD : 128;  // (this branch is compiled for every D)
+    using Gm = Dkv2Geom<DD>;
+    const int R = (a.Hq / a.Hkv) * a.Lq;
+    CUtensorMap tq, tv, tdo;
+    if (!make_map(a, &tq, a.q, R, a.B * a.Hkv, Gm::BQ) || !make_map(a, &tdo, a.dO, R, a.B * a.Hkv, Gm::BQ) ||
+        !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      return kLaunchBadMap;
+    BwdParams p = bwd_params(a);  // off = Lk - Lq from the true query length
+    p.Hq = a.Hkv, p.Lq = R, p.G = 1;
+    p.qmod = a.Lq;
+    p.n_qtiles = (R + Gm::BQ - 1) / Gm::BQ;
+    p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
+    const dim3 grid(a.B * a.Hkv, p.n_ktiles);
+    auto kern = attn_bwd_dkv2_kernel<DD, BF16, CAUSAL, false, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+      return kLaunchCudaError;
+    kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, a.k, p);
+    return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+  } else {
+    return dkv_all<BF16, CAUSAL>(a);
+  }
 }
 
 template <bool BF16>
@@ -266,6 +369,21 @@ int GBATTN_CAT(launch_bwd_dkv_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
 
 int GBATTN_CAT(launch_delta_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
   return a.bf16 ? delta_impl<true>(a) : delta_impl<false>(a);
+}
+
+int GBATTN_CAT(launch_fwd_decode_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? fwd_decode_impl<true, true>(a) : fwd_decode_impl<true, false>(a);
+  return a.causal ? fwd_decode_impl<false, true>(a) : fwd_decode_impl<false, false>(a);
+}
+
+int GBATTN_CAT(launch_bwd_dkv_decode_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? dkv_decode_impl<true, true>(a) : dkv_decode_impl<true, false>(a);
+  return a.causal ? dkv_decode_impl<false, true>(a) : dkv_decode_impl<false, false>(a);
+}
+
+int GBATTN_CAT(launch_bwd_dq_decode_d, GBATTN_HEAD_DIM)(const AttnArgs& a) {
+  if (a.bf16) return a.causal ? dq_decode_impl<true, true>(a) : dq_decode_impl<true, false>(a);
+  return a.causal ? dq_decode_impl<false, true>(a) : dq_decode_impl<false, false>(a);
 }
 
 }  // namespace gbattn

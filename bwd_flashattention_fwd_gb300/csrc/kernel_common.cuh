@@ -34,6 +34,13 @@ struct FwdParams {
   // block-sparse variant: uint8 [ceil(Lq/128), ceil(Lk/128)], row-major
   const uint8_t* bmask;
   int nkb;  // ceil(Lk / 128): row length of the mask
+  // decode variant: Lq above is the packed row count G * Lq of one KV head,
+  // qmod the true Lq (packed row r is query r % qmod); each CTA covers
+  // split_tiles key tiles and writes fp32 partial O rows to ws and their
+  // base-2 log-sum-exp to ws_lse
+  int qmod, split_tiles;
+  float* ws;
+  float* ws_lse;
 };
 
 struct BwdParams {
@@ -52,7 +59,19 @@ struct BwdParams {
   const uint8_t* bmask;
   int nkb;  // ceil(Lk / 128): row length of the mask
   int64_t kv_pitch;  // rows between consecutive heads of k and v (>= Lk)
+  // decode variant of the dQ kernel (as in FwdParams): fp32 partial dQ rows
+  int qmod, split_tiles;
+  float* ws;
 };
+
+// fp32 row of 32 values (128 bytes, 16-byte aligned) to global memory, scaled.
+__device__ __forceinline__ void store_row32_f32(float* dst, const uint32_t (&r)[32], float mul) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    d[q] = make_float4(__uint_as_float(r[4 * q]) * mul, __uint_as_float(r[4 * q + 1]) * mul,
+                       __uint_as_float(r[4 * q + 2]) * mul, __uint_as_float(r[4 * q + 3]) * mul);
+}
 
 // Block-mask entry (query block qb, key block kb); nonzero keeps the pair.
 __device__ __forceinline__ bool mask_keep(const uint8_t* m, int nkb, int qb, int kb) {
@@ -119,6 +138,7 @@ struct Elem<true> {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
     return __bfloat1622float2(v);
   }
+  __device__ __forceinline__ static T from_float(float x) { return __float2bfloat16_rn(x); }
 };
 template <>
 struct Elem<false> {
@@ -131,6 +151,7 @@ struct Elem<false> {
     __half2 v = *reinterpret_cast<__half2*>(&u);
     return __half22float2(v);
   }
+  __device__ __forceinline__ static T from_float(float x) { return __float2half_rn(x); }
 };
 
 // Number of 64-element (128-byte) column chunks a row of D 16-bit elements

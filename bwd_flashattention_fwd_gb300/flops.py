@@ -80,3 +80,18 @@ def kernel_flops_pairs(kernel: str, B: int, Hq: int, D: int, pairs: int) -> floa
 def delta_bytes(B: int, Hq: int, Lq: int, D: int, elem_bytes: int = 2) -> int:
     rows = B * Hq * Lq
     return 2 * rows * D * elem_bytes + 4 * rows
+
+
+def decode_bytes(kernel: str, B: int, Hq: int, Hkv: int, Lq: int, Lk: int, D: int, elem_bytes: int = 2) -> int:
+    """Compulsory HBM bytes of the decode-shaped calls, which are bound by
+    reading the key/value range: fwd reads q, k, v and writes o and lse; bwd
+    reads q, k, v, dO, lse, delta and writes dq, dk, dv (the split partials
+    stay in L2 and are not counted)."""
+    q = B * Hq * Lq * D * elem_bytes
+    kv = B * Hkv * Lk * D * elem_bytes
+    rows = B * Hq * Lq * 4
+    if kernel == "fwd":
+        return q + 2 * kv + q + rows
+    if kernel == "bwd":
+        return 2 * q + 2 * kv + 2 * rows + q + 2 * kv
+    raise ValueError(kernel)

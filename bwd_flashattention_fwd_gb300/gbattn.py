@@ -25,8 +25,8 @@ ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc",
-            "attn_fwd_masked", "attn_bwd_masked", "attn_fwd_ex", "attn_bwd_ex", "attn_last_device_status",
-            "attn_status_string")
+            "attn_fwd_masked", "attn_bwd_masked", "attn_fwd_ex", "attn_bwd_ex", "attn_decode_workspace_bytes",
+            "attn_fwd_decode", "attn_bwd_decode", "attn_last_device_status", "attn_status_string")
 
 _lib = None
 
@@ -69,6 +69,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_ex.restype = ci
     lib.attn_bwd_ex.argtypes = [vp] * 8 + [i64] + [vp] * 3 + [ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.attn_bwd_ex.restype = ci
+    sz = ctypes.c_size_t
+    lib.attn_decode_workspace_bytes.argtypes = [ci] * 6
+    lib.attn_decode_workspace_bytes.restype = sz
+    lib.attn_fwd_decode.argtypes = [vp] * 6 + [sz, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_fwd_decode.restype = ci
+    lib.attn_bwd_decode.argtypes = [vp] * 11 + [sz, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.attn_bwd_decode.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -225,6 +232,42 @@ def attn_bwd_ex(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bo
                                     _ptr(block_mask), pitch, _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, D,
                                     float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
     return _check(st, "attn_bwd_ex", check)
+
+
+def attn_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, D: int) -> int:
+    """Bytes of device workspace attn_fwd_decode / attn_bwd_decode need (0: shape not served)."""
+    return int(load_library().attn_decode_workspace_bytes(B, Hq, Hkv, Lq, Lk, D))
+
+
+def decode_workspace(q, k) -> torch.Tensor:
+    """A workspace tensor (uint8, on q's device) for the decode calls on q, k."""
+    B, Hq, Lq, D = q.shape
+    n = attn_decode_workspace_bytes(B, Hq, k.shape[1], Lq, k.shape[2], D)
+    if n == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "attn_decode_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def attn_fwd_decode(q, k, v, o, lse, workspace, scale: float, causal: bool, stream=None, check: bool = True) -> int:
+    """attn_fwd for short query lengths (G * Lq <= 128), key range split over CTAs."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), B, Hq, Hkv, Lq, Lk, D,
+                                        float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_fwd_decode", check)
+
+
+def attn_bwd_decode(q, k, v, o, dO, lse, delta, dq, dk, dv, workspace, scale: float, causal: bool, stream=None,
+                    check: bool = True) -> int:
+    """attn_bwd for short query lengths (G * Lq <= 128)."""
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    st = load_library().attn_bwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), B, Hq, Hkv, Lq, Lk, D,
+                                        float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    return _check(st, "attn_bwd_decode", check)
 
 
 def attn_last_device_status(stream=None) -> int:

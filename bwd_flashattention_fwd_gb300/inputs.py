@@ -64,6 +64,8 @@ WORKLOADS = {
         ),
         Workload("longcache_q1024_k8192_d128", B=1, Hq=32, Hkv=8, Lq=1024, Lk=8192, D=128, seed=1006),
         Workload("longcache_q2048_k8192_d256", B=1, Hq=16, Hkv=2, Lq=2048, Lk=8192, D=256, seed=1007),
+        # decode-shaped: 8 new query rows per sequence against an 8192-key context
+        Workload("decode_b4_q8_k8192_d128", B=4, Hq=32, Hkv=8, Lq=8, Lk=8192, D=128, seed=1008),
     ]
 }
 

@@ -33,6 +33,7 @@
 #define GBATTN_H_
 
 #include <cuda_runtime_api.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -161,6 +162,35 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
                           const float* lse, const float* delta, const uint8_t* block_mask, int64_t kv_pitch,
                           void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int D,
                           float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Decode-shaped attention: short query lengths against long key ranges
+ * ("feat(attention): complete Flash Attention VJP implementation": vector
+ * kernels for sequences of at most 8; here any G * Lq <= 128, G = Hq / Hkv).
+ * The same results as attn_fwd / attn_bwd (same arguments, layouts and
+ * errors), computed for few query rows: the G query heads x Lq rows of each
+ * KV head are processed as one tile of G*Lq rows, and each KV head's key
+ * range is split over several CTAs whose partial results are merged.
+ *   workspace: DEVICE pointer, 16-byte aligned, at least
+ *     attn_decode_workspace_bytes(B, Hq, Hkv, Lq, Lk, D) bytes, owned by the
+ *     caller; contents on entry are ignored and on exit are undefined.  One
+ *     workspace may serve both calls but not two calls in flight at once.
+ *   attn_decode_workspace_bytes returns 0 for a shape these calls reject
+ *     (invalid, or G*Lq > 128).
+ *   Errors: G*Lq > 128 is ATTN_ERR_UNSUPPORTED; a null, misaligned or too
+ *   small workspace is ATTN_ERR_INVALID_ARG; the rest as for attn_fwd /
+ *   attn_bwd.  attn_bwd_decode writes dk and dv with the attn_bwd_dkv kernel
+ *   and dq with the split kernel; lse and delta as for attn_bwd (delta from
+ *   attn_bwd_delta).
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D);
+attn_status_t attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                              size_t workspace_bytes, int B, int Hq, int Hkv, int Lq, int Lk, int D, float scale,
+                              int causal, attn_dtype_t dtype, cudaStream_t stream);
+attn_status_t attn_bwd_decode(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, const float* delta, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, int B, int Hq, int Hkv, int Lq, int Lk, int D, float scale,
+                              int causal, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
  * attn_bwd for callers that cannot allocate device memory.  (The pages have no

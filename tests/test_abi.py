@@ -162,3 +162,25 @@ def test_kv_row_pitch_from_strides():
         gbattn.kv_row_pitch(cache[:, :, :, :32], cache[:, :, :, :32])
     with pytest.raises(ValueError):
         gbattn.kv_row_pitch(k, cache.transpose(1, 2)[:, :25])
+
+
+def test_decode_workspace_and_rejects_on_host(lib):
+    lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.attn_decode_workspace_bytes(4, 32, 8, 8, 8192, 128)
+    assert need > 0 and need % 16 == 0
+    assert lib.attn_decode_workspace_bytes(1, 32, 1, 8, 8192, 128) == 0  # G * Lq = 256 rows
+    assert lib.attn_decode_workspace_bytes(1, 32, 8, 8, 8192, 80) == 0
+
+    def fwd_dec(ws=FAKE, nbytes=need, Hq=32, Hkv=8, Lq=8, D=128):
+        return lib.attn_fwd_decode(FAKE, FAKE, FAKE, FAKE, FAKE, ws, ctypes.c_size_t(nbytes), 4, Hq, Hkv, Lq, 8192,
+                                   D, ctypes.c_float(0.1), 1, 1, None)
+
+    assert fwd_dec(ws=None) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_dec(ws=FAKE + 8) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_dec(nbytes=need - 1) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_dec(Hq=32, Hkv=1) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_dec(D=48) == gbattn.ATTN_ERR_UNSUPPORTED
+    ptrs = [FAKE] * 10
+    ptrs[3] = None
+    assert lib.attn_bwd_decode(*ptrs, FAKE, ctypes.c_size_t(need), 4, 32, 8, 8, 8192, 128, ctypes.c_float(0.1), 1,
+                               1, None) == gbattn.ATTN_ERR_INVALID_ARG
