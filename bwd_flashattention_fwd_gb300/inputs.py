@@ -122,3 +122,55 @@ def block_mask(spec: str, Lq: int, Lk: int, seed: int = 0, blk: int = 128):
         rng = np.random.default_rng(seed)
         return (rng.random((nqb, nkb)) < float(arg)).astype(np.uint8)
     raise ValueError(f"unknown block-mask pattern {spec!r}")
+
+
+# ---------------------------------------------------------------------------
+# Linear cross-entropy inputs ("When the Bottleneck Moved", section 1: the
+# output layer of a Qwen3-8B fine-tune, hidden 4096, vocabulary 151936)
+# ---------------------------------------------------------------------------
+
+
+@dataclass(frozen=True)
+class LceWorkload:
+    name: str
+    N: int  # tokens
+    Dm: int  # hidden size
+    V: int  # vocabulary
+    dtype: str = "bf16"
+    h_std: float = 1.0  # hidden states after the final RMS norm
+    w_std: float = 0.02  # output-projection weights
+    ignore_frac: float = 0.0  # share of rows whose target is -1 (ignored)
+    seed: int = 2000
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPES[self.dtype]
+
+    def with_(self, **kw) -> "LceWorkload":
+        return replace(self, **kw)
+
+
+LCE_WORKLOADS = {
+    w.name: w
+    for w in [
+        LceWorkload("lce_tiny_n200_d128_v1000", N=200, Dm=128, V=1000, seed=2000),
+        LceWorkload("lce_qwen3_8b_n8192", N=8192, Dm=4096, V=151936, seed=2001),
+    ]
+}
+
+
+def make_lce_inputs(w: LceWorkload, device: str | torch.device = "cpu"):
+    """hidden [N, Dm], weight [V, Dm] (16-bit), targets [N] int32 (-1 =
+    ignored) and the upstream gradient dloss [N] float32 (1/N: the gradient
+    of the mean loss), drawn in that order from a CPU generator."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    h = (torch.randn((w.N, w.Dm), generator=gen, dtype=torch.float32) * w.h_std).to(w.torch_dtype)
+    wt = (torch.randn((w.V, w.Dm), generator=gen, dtype=torch.float32) * w.w_std).to(w.torch_dtype)
+    t = torch.randint(0, w.V, (w.N,), generator=gen, dtype=torch.int64)
+    if w.ignore_frac > 0:
+        drop = torch.rand((w.N,), generator=gen) < w.ignore_frac
+        t = torch.where(drop, torch.full_like(t, -1), t)
+    t = t.to(torch.int32)
+    dloss = torch.full((w.N,), 1.0 / w.N, dtype=torch.float32)
+    return tuple(x.to(device).contiguous() for x in (h, wt, t, dloss))

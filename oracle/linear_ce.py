@@ -1,0 +1,72 @@
+"""fp64 CPU oracle for the linear cross-entropy loss and its gradients.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links
+this module: only the tests, the smoke check and the bench's CPU-baseline leg
+use it.  It shares no code with the CUDA kernels.
+
+What it computes, written as the plain definition with the (N, V) logits
+matrix materialised (page 3, "When the Bottleneck Moved", section 1 "The
+first hypothesis: remove logits, train longer": logits = hidden @ W.T and
+loss_i = logsumexp(logits_i) - logits_i,target_i; the fused kernel streams
+over vocabulary tiles with an online log-sum-exp instead, which reaches the
+same value up to rounding):
+
+* Forward, for every row i with target t_i:
+    z_iv   = sum_d H_id W_vd                      (logits, v < V)
+    lse_i  = m_i + ln sum_v exp(z_iv - m_i),  m_i = max_v z_iv
+    loss_i = lse_i - z_i,t_i
+* Backward, with an upstream gradient dloss_i per row (the derivative of the
+  definition above; the pages give no formula for it):
+    p_iv  = exp(z_iv - lse_i)                     (softmax of the row)
+    g_iv  = dloss_i * (p_iv - [v == t_i])
+    dH    = g W,   dW = g^T H.
+* A negative target marks a row that takes no part (a padding token; the
+  pages are silent): its loss is 0 and its gradient rows are 0.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def logits(h: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """z = H W^T, [N, V]."""
+    return h @ w.T
+
+
+def forward(h: np.ndarray, w: np.ndarray, t: np.ndarray):
+    """(loss [N], lse [N]) in float64; lse is the natural-log log-sum-exp."""
+    z = logits(h, w)
+    m = z.max(axis=1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    rows = np.arange(z.shape[0])
+    valid = t >= 0
+    zt = np.where(valid, z[rows, np.where(valid, t, 0)], 0.0)
+    loss = np.where(valid, lse - zt, 0.0)
+    return loss, lse
+
+
+def grad_logits(h: np.ndarray, w: np.ndarray, t: np.ndarray, lse: np.ndarray, dloss: np.ndarray) -> np.ndarray:
+    """g = dloss * (softmax(z) - onehot(t)), [N, V]; zero rows where t < 0."""
+    z = logits(h, w)
+    g = np.exp(z - lse[:, None])
+    valid = t >= 0
+    rows = np.arange(z.shape[0])[valid]
+    g[rows, t[valid]] -= 1.0
+    return g * np.where(valid, dloss, 0.0)[:, None]
+
+
+def backward(h: np.ndarray, w: np.ndarray, t: np.ndarray, lse: np.ndarray, dloss: np.ndarray):
+    """(dH [N, Dm], dW [V, Dm]) in float64."""
+    g = grad_logits(h, w, t, lse, dloss)
+    return g @ w, g.T @ h
+
+
+def flops_forward(N: int, V: int, Dm: int) -> float:
+    """One matrix product H W^T: 2 N V Dm."""
+    return 2.0 * N * V * Dm
+
+
+def flops_backward(N: int, V: int, Dm: int) -> float:
+    """Recomputed logits, g W and g^T H: three products of 2 N V Dm."""
+    return 3.0 * flops_forward(N, V, Dm)
