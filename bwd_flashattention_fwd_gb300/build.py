@@ -1,8 +1,9 @@
 """Build libgbattn.so in-tree with nvcc for sm_103a.
 
 The kernel instantiations compile as one translation unit per head dimension
-(inst.cu with -DGBATTN_HEAD_DIM=<D>), in parallel, plus the C-ABI unit; the
-objects link into bwd_flashattention_fwd_gb300/libgbattn.so.
+(inst.cu with -DGBATTN_HEAD_DIM=<D>), in parallel, plus the C-ABI unit and
+the linear cross-entropy unit (lce.cu); the objects link, with cuBLAS, into
+bwd_flashattention_fwd_gb300/libgbattn.so.
 """
 
 from __future__ import annotations
@@ -57,8 +58,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         obj = os.path.join(BUILD, f"inst_d{d}.o")
         jobs.append([nvcc, *ARCH, *FLAGS, *extra_flags, f"-DGBATTN_HEAD_DIM={d}", "-c",
                      os.path.join(CSRC, "inst.cu"), "-o", obj])
-    jobs.append([nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, "api.cu"), "-o",
-                 os.path.join(BUILD, "api.o")])
+    for unit in ("api", "lce"):
+        jobs.append([nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, unit + ".cu"), "-o",
+                     os.path.join(BUILD, unit + ".o")])
     with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         outs = list(ex.map(_run, jobs))
     if verbose:
@@ -66,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stdout.write(o)
     objs = [j[-1] for j in jobs]
     tmp = LIB + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"])
     os.replace(tmp, LIB)
     return LIB
 

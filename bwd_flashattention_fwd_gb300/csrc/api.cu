@@ -234,6 +234,15 @@ attn_status_t check_decode(int B, int Hq, int Hkv, int Lq, int Lk, int D, const 
 }  // namespace
 }  // namespace gbattn
 
+namespace gbattn {
+// For the other translation units of the library (the linear cross-entropy
+// calls share the device state and the status word).
+attn_status_t shared_device_state(int* dev, EncodeTiledFn* enc, int** status, int* num_sms) {
+  return device_state(dev, enc, status, num_sms);
+}
+uint64_t shared_wait_limit_ns() { return wait_limit_ns(); }
+}  // namespace gbattn
+
 using namespace gbattn;
 
 extern "C" attn_status_t attn_bwd_delta(const void* o, const void* dO, float* delta, int B, int Hq, int Lq, int D,

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/gbattn.h"
+
 namespace gbattn {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -78,6 +80,11 @@ inline size_t decode_workspace_bytes(int B, int Hkv, long long rows, int Lk, int
   const size_t qb = static_cast<size_t>(q.n_split) * rows * D * 4;
   return fb > qb ? fb : qb;
 }
+
+// Device state shared by every call of the library (api.cu): tensor-map
+// encoder, device status word, SM count; and the bounded-wait limit.
+attn_status_t shared_device_state(int* dev, EncodeTiledFn* enc, int** status, int* num_sms);
+uint64_t shared_wait_limit_ns();
 
 // Launch results: 0 = launched, 1 = tensor-map encoding rejected the
 // arguments, 2 = CUDA launch error (cudaGetLastError() holds it).

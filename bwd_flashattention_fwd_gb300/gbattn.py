@@ -26,7 +26,8 @@ ATTN_DTYPE_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc",
             "attn_fwd_masked", "attn_bwd_masked", "attn_fwd_ex", "attn_bwd_ex", "attn_decode_workspace_bytes",
-            "attn_fwd_decode", "attn_bwd_decode", "attn_last_device_status", "attn_status_string")
+            "attn_fwd_decode", "attn_bwd_decode", "attn_last_device_status", "attn_status_string",
+            "lce_workspace_bytes", "lce_fwd", "lce_bwd")
 
 _lib = None
 
@@ -76,6 +77,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_decode.restype = ci
     lib.attn_bwd_decode.argtypes = [vp] * 11 + [sz, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.attn_bwd_decode.restype = ci
+    lib.lce_workspace_bytes.argtypes = [ci, ci, ci]
+    lib.lce_workspace_bytes.restype = sz
+    lib.lce_fwd.argtypes = [vp] * 6 + [sz, ci, ci, ci, ci, vp]
+    lib.lce_fwd.restype = ci
+    lib.lce_bwd.argtypes = [vp] * 8 + [sz, ci, ci, ci, ci, vp]
+    lib.lce_bwd.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -268,6 +275,37 @@ def attn_bwd_decode(q, k, v, o, dO, lse, delta, dq, dk, dv, workspace, scale: fl
                                         workspace.numel() * workspace.element_size(), B, Hq, Hkv, Lq, Lk, D,
                                         float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
     return _check(st, "attn_bwd_decode", check)
+
+
+def lce_workspace_bytes(N: int, Dm: int, V: int) -> int:
+    """Bytes of device workspace lce_fwd / lce_bwd need (0: shape rejected)."""
+    return int(load_library().lce_workspace_bytes(N, Dm, V))
+
+
+def lce_workspace(hidden, weight) -> torch.Tensor:
+    N, Dm = hidden.shape
+    n = lce_workspace_bytes(N, Dm, weight.shape[0])
+    if n == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "lce_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=hidden.device)
+
+
+def lce_fwd(hidden, weight, targets, loss, lse, workspace, stream=None, check: bool = True) -> int:
+    """Per-row linear cross-entropy loss and natural-log lse (writes loss, lse)."""
+    N, Dm = hidden.shape
+    st = load_library().lce_fwd(_ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss), _ptr(lse), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), N, Dm, weight.shape[0],
+                                _dtype_code(hidden), _stream_handle(stream))
+    return _check(st, "lce_fwd", check)
+
+
+def lce_bwd(hidden, weight, targets, lse, dloss, dhidden, dweight, workspace, stream=None, check: bool = True) -> int:
+    """dhidden and dweight of sum_i dloss[i] * loss[i] (writes both)."""
+    N, Dm = hidden.shape
+    st = load_library().lce_bwd(_ptr(hidden), _ptr(weight), _ptr(targets), _ptr(lse), _ptr(dloss), _ptr(dhidden),
+                                _ptr(dweight), _ptr(workspace), workspace.numel() * workspace.element_size(), N, Dm,
+                                weight.shape[0], _dtype_code(hidden), _stream_handle(stream))
+    return _check(st, "lce_bwd", check)
 
 
 def attn_last_device_status(stream=None) -> int:

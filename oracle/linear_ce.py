@@ -70,3 +70,51 @@ def flops_forward(N: int, V: int, Dm: int) -> float:
 def flops_backward(N: int, V: int, Dm: int) -> float:
     """Recomputed logits, g W and g^T H: three products of 2 N V Dm."""
     return 3.0 * flops_forward(N, V, Dm)
+
+
+# ---------------------------------------------------------------------------
+# Helpers for large problems: the same definitions evaluated on chosen rows or
+# vocabulary entries, with the weight matrix decoded one vocabulary chunk at a
+# time (w_chunk(v0, v1) returns rows v0..v1-1 of W as float64).
+# ---------------------------------------------------------------------------
+
+
+def logits_rows(h_rows: np.ndarray, w_chunk, V: int, chunk: int = 16384) -> np.ndarray:
+    """z for the given rows of H, [n, V]."""
+    return np.concatenate([h_rows @ w_chunk(v0, min(V, v0 + chunk)).T for v0 in range(0, V, chunk)], axis=1)
+
+
+def forward_rows(h_rows: np.ndarray, t_rows: np.ndarray, w_chunk, V: int):
+    """(loss, lse) of the given rows."""
+    z = logits_rows(h_rows, w_chunk, V)
+    m = z.max(axis=1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    valid = t_rows >= 0
+    zt = np.where(valid, z[np.arange(len(t_rows)), np.where(valid, t_rows, 0)], 0.0)
+    return np.where(valid, lse - zt, 0.0), lse
+
+
+def dhidden_rows(h_rows, t_rows, dloss_rows, w_chunk, V: int, chunk: int = 16384):
+    """dH for the given rows: (dloss * (softmax - onehot)) W."""
+    z = logits_rows(h_rows, w_chunk, V, chunk)
+    _, lse = forward_rows(h_rows, t_rows, w_chunk, V)
+    g = np.exp(z - lse[:, None])
+    valid = t_rows >= 0
+    g[np.arange(len(t_rows))[valid], t_rows[valid]] -= 1.0
+    g *= np.where(valid, dloss_rows, 0.0)[:, None]
+    out = np.zeros((h_rows.shape[0], h_rows.shape[1]))
+    for v0 in range(0, V, chunk):
+        out += g[:, v0:v0 + chunk] @ w_chunk(v0, min(V, v0 + chunk))
+    return out
+
+
+def dweight_entries(h: np.ndarray, t: np.ndarray, dloss: np.ndarray, w_chunk, V: int, entries):
+    """dW for the given vocabulary entries (needs every row's lse)."""
+    entries = np.asarray(entries)
+    _, lse = forward_rows(h, t, w_chunk, V)
+    z = h @ np.concatenate([w_chunk(v, v + 1) for v in entries]).T  # [N, len(entries)]
+    g = np.exp(z - lse[:, None])
+    valid = t >= 0
+    g -= (t[:, None] == entries[None, :]) & valid[:, None]
+    g *= np.where(valid, dloss, 0.0)[:, None]
+    return g.T @ h

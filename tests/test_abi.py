@@ -11,7 +11,8 @@ import pytest
 
 from bwd_flashattention_fwd_gb300 import build, gbattn
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gbattn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = [os.path.join(INCLUDE, h) for h in ("gbattn.h", "gblce.h")]
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
 
 
@@ -22,9 +23,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:attn|lce)_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_function(lib):
@@ -184,3 +187,29 @@ def test_decode_workspace_and_rejects_on_host(lib):
     ptrs[3] = None
     assert lib.attn_bwd_decode(*ptrs, FAKE, ctypes.c_size_t(need), 4, 32, 8, 8, 8192, 128, ctypes.c_float(0.1), 1,
                                1, None) == gbattn.ATTN_ERR_INVALID_ARG
+
+
+def test_lce_rejects_on_host(lib):
+    lib.lce_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.lce_workspace_bytes(300, 128, 1000)
+    assert need > 0 and lib.lce_workspace_bytes(300, 100, 1000) == 0 and lib.lce_workspace_bytes(0, 128, 10) == 0
+
+    def fwd_l(ptrs=None, nbytes=need, N=300, Dm=128, V=1000, dtype=1):
+        ptrs = ptrs or [FAKE] * 6
+        return lib.lce_fwd(*ptrs, ctypes.c_size_t(nbytes), N, Dm, V, dtype, None)
+
+    for i in range(6):
+        ptrs = [FAKE] * 6
+        ptrs[i] = None
+        assert fwd_l(ptrs) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_l([FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE]) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_l(Dm=100) == gbattn.ATTN_ERR_UNSUPPORTED
+    assert fwd_l(N=0) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_l(dtype=7) == gbattn.ATTN_ERR_INVALID_ARG
+    assert fwd_l(nbytes=0) == gbattn.ATTN_ERR_INVALID_ARG
+    for i in range(8):
+        ptrs = [FAKE] * 8
+        ptrs[i] = None
+        assert lib.lce_bwd(*ptrs, ctypes.c_size_t(need), 300, 128, 1000, 1, None) == gbattn.ATTN_ERR_INVALID_ARG
+    assert lib.lce_bwd(*([FAKE] * 8), ctypes.c_size_t(need - 16), 300, 128, 1000, 1, None) == \
+        gbattn.ATTN_ERR_INVALID_ARG

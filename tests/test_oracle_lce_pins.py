@@ -165,3 +165,18 @@ def test_planted_mistake_is_caught(name, fwd, bwd):
         except AssertionError:
             caught = True
     assert caught, name
+
+
+def test_chunked_helpers_match_whole_problem():
+    h, w, t, dloss = rand_case(N=9, Dm=4, V=37, seed=5)
+    chunk = lambda v0, v1: w[v0:v1]  # noqa: E731
+    loss, lse = L.forward(h, w, t)
+    dh, dw = L.backward(h, w, t, lse, dloss)
+    rows = np.array([0, 1, 5, 8])
+    l2, lse2 = L.forward_rows(h[rows], t[rows], chunk, 37)
+    np.testing.assert_allclose(l2, loss[rows], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse[rows], rtol=1e-13)
+    np.testing.assert_allclose(L.dhidden_rows(h[rows], t[rows], dloss[rows], chunk, 37, chunk=10), dh[rows],
+                               rtol=1e-12, atol=1e-13)
+    ent = [0, 3, 36]
+    np.testing.assert_allclose(L.dweight_entries(h, t, dloss, chunk, 37, ent), dw[ent], rtol=1e-12, atol=1e-13)
