@@ -8,6 +8,7 @@ causal) over the summed device time of the step's kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--block-mask none|window:W|random:P] [--kv-capacity N] [--decode]
+                    [--lce [--lce-workload NAME]]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload on its own GPU (weak scaling); the value is all ranks' work
@@ -21,7 +22,9 @@ visible.  With `--kv-capacity N` k and v are the first Lk rows of each head
 of an N-row cache whose other rows hold large stale values, and the step runs
 attn_fwd_ex / attn_bwd_ex.  With `--decode` (short query lengths) the step
 runs attn_fwd_decode, attn_bwd_delta and attn_bwd_decode, and the roofline
-is HBM bytes (the key/value range read and the gradients written).
+is HBM bytes (the key/value range read and the gradients written).  With
+`--lce` the step is the fused linear cross-entropy (lce_fwd + lce_bwd) of a
+Qwen3-8B output layer, credited 2 N V Dm FLOPs forward and 3 x that backward.
 """
 
 from __future__ import annotations
@@ -44,7 +47,15 @@ import torch  # noqa: E402
 
 from bwd_flashattention_fwd_gb300 import flops as F  # noqa: E402
 from bwd_flashattention_fwd_gb300 import replicas  # noqa: E402
-from bwd_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, block_mask, make_inputs  # noqa: E402
+from bwd_flashattention_fwd_gb300.inputs import (  # noqa: E402
+    LCE_WORKLOADS,
+    WORKLOADS,
+    LceWorkload,
+    Workload,
+    block_mask,
+    make_inputs,
+    make_lce_inputs,
+)
 
 METRIC = "fwd+bwd attention TFLOP/s, causal GQA L=8192 D=128 bf16; % of BF16 TC peak"
 METRIC_MASKED = "block-sparse fwd+bwd attention TFLOP/s (3.5 x 4*D FLOPs per visible pair), GQA D=128 bf16"
@@ -527,6 +538,149 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
             "pipelining": "two device buffer sets; input copies, compute and output copies on separate streams"}
 
 
+# ---------------------------------------------------------------------------
+# Fused linear cross-entropy
+# ---------------------------------------------------------------------------
+
+METRIC_LCE = "fused linear cross-entropy fwd+bwd TFLOP/s, Qwen3-8B output layer (N=8192, hidden 4096, vocab 151936) bf16"
+
+
+def lce_cpu_baseline(w: LceWorkload, rows: int = 4) -> dict:
+    """The fp64 oracle's loss and dH for a few rows (all of V and Dm)."""
+    import oracle.linear_ce as L
+    from bwd_flashattention_fwd_gb300.inputs import to_f64
+
+    h, wt, t, dloss = make_lce_inputs(w, "cpu")
+    sel = list(range(rows))
+    hd, tn, dn = to_f64(h[sel]), t[sel].numpy().astype("int64"), dloss[sel].numpy().astype("float64")
+    chunk = lambda v0, v1: to_f64(wt[v0:v1])  # noqa: E731  (decoded per chunk: 0.5 GB at a time)
+    t0 = time.perf_counter()
+    L.forward_rows(hd, tn, chunk, w.V)
+    L.dhidden_rows(hd, tn, dn, chunk, w.V)
+    dt = time.perf_counter() - t0
+    # forward_rows twice (once inside dhidden_rows) plus g W: four products of 2 V Dm per row
+    credited = rows * 4 * 2.0 * w.V * w.Dm
+    return {"value": credited / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle loss and dH for {rows} rows at full vocabulary and hidden size "
+                      f"({credited:.3g} FLOP, {dt:.2f} s)"}
+
+
+def run_lce(args):
+    from bwd_flashattention_fwd_gb300 import build, gbattn
+
+    rank, local_rank, ws_n = replicas.world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    replicas.init("nccl")
+    build.build()
+    gbattn.load_library()
+    w = LCE_WORKLOADS[args.lce_workload]
+    h, wt, t, dloss = make_lce_inputs(w, dev)
+    loss = torch.empty(w.N, dtype=torch.float32, device=dev)
+    lse = torch.empty_like(loss)
+    dh, dw = torch.empty_like(h), torch.empty_like(wt)
+    wsb = gbattn.lce_workspace(h, wt)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        gbattn.lce_fwd(h, wt, t, loss, lse, wsb, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        gbattn.lce_bwd(h, wt, t, lse, dloss, dh, dw, wsb, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize(dev)
+    if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(physical_gpu_index(local_rank))
+    replicas.barrier(dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    replicas.barrier(dev)
+    clk = clocks.stop()
+    if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
+        raise RuntimeError("device-side wait timed out during the timed steps")
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    local_s = sum(e[0].elapsed_time(e[2]) for e in events) / 1e3
+    f_fwd = 2.0 * w.N * w.V * w.Dm
+    f_bwd = 3.0 * f_fwd
+    value_flops, _, max_s = replicas.aggregate_throughput((f_fwd + f_bwd) * args.steps, local_s, dev)
+    peaks = load_peaks()
+    pk = peaks["bf16_tflops_sustained"]
+    kernels = {}
+    for n, fl, ms in (("lce_fwd", f_fwd, fwd_ms), ("lce_bwd", f_bwd, bwd_ms)):
+        ach = fl / (ms * 1e-3) / 1e12
+        kernels[n] = {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk,
+                      "avg_ms": ms, "algorithmic": fl, "traffic": None}
+    roof = {k2: kernels["lce_fwd"][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = "lce_fwd (fused logits tiles + online LSE; the backward's GEMMs are cuBLAS)"
+    roof["peak_kind"] = f"bf16 dense, sustained ({peaks['source']})"
+
+    e2e = None
+    if not args.no_e2e:
+        # per step: hidden, targets and dloss in from pinned host memory; loss and
+        # dH back; the weight and its gradient stay on the device (parameters)
+        hh, th, dh_host = h.cpu().pin_memory(), t.cpu().pin_memory(), dloss.cpu().pin_memory()
+        loss_h = torch.empty_like(loss, device="cpu").pin_memory()
+        dhid_h = torch.empty_like(dh, device="cpu").pin_memory()
+        n = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n):
+            h.copy_(hh, non_blocking=True)
+            t.copy_(th, non_blocking=True)
+            dloss.copy_(dh_host, non_blocking=True)
+            step()
+            loss_h.copy_(loss, non_blocking=True)
+            dhid_h.copy_(dh, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        es = e0.elapsed_time(e1) / 1e3
+        ev, _, _ = replicas.aggregate_throughput((f_fwd + f_bwd) * n, es, dev)
+        e2e = {"value": ev / 1e12, "unit": UNIT, "steps": n, "ms_per_step": es * 1e3 / n,
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hh, th, dh_host)),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in (loss_h, dhid_h))}
+    n_chunks = -(-w.V // 16384)
+    line = {
+        "metric": METRIC_LCE, "value": value_flops / 1e12, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "hidden": w.Dm, "vocab": w.V, "h_std": w.h_std, "w_std": w.w_std,
+                   "seed": w.seed, "l2": "256 MiB written between steps; the weight (1.2 GB) exceeds L2",
+                   "parallelism": "replicas" if ws_n > 1 else "single GPU",
+                   "flops": "forward 2 N V Dm; backward 3 x that (recomputed logits, g W, g^T H)"},
+        "pct_of_bf16_peak": 100.0 * value_flops / 1e12 / ws_n / peaks["bf16_tflops"],
+        "peaks": peaks, "phase_ms": {"lce_fwd": fwd_ms, "lce_bwd": bwd_ms}, "roofline": roof, "kernels": kernels,
+        "e2e": e2e,
+        # ours: logits kernel + combine (forward); per chunk one logits kernel, plus the final cast (backward)
+        "gpu_launches": args.steps * (2 + n_chunks + 1),
+        "library_launches_per_step": {"cublas_gemm": 2 * n_chunks},
+        "clocks": clk, "kernel_source_hash": kernel_source_hash(),
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = lce_cpu_baseline(w)
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    replicas.shutdown()
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,6 +693,8 @@ def main(argv=None) -> int:
     ap.add_argument("--kv-capacity", type=int, default=0,
                     help="k/v as the first Lk rows of an N-row cache per head (0: contiguous)")
     ap.add_argument("--decode", action="store_true", help="short-query path (attn_fwd_decode / attn_bwd_decode)")
+    ap.add_argument("--lce", action="store_true", help="fused linear cross-entropy step instead of attention")
+    ap.add_argument("--lce-workload", default="lce_qwen3_8b_n8192", choices=sorted(LCE_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")
@@ -548,6 +704,8 @@ def main(argv=None) -> int:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.lce:
+        return run_lce(args)
     return run_ours(args)
 
 
