@@ -64,6 +64,8 @@ WORKLOADS = {
         ),
         Workload("longcache_q1024_k8192_d128", B=1, Hq=32, Hkv=8, Lq=1024, Lk=8192, D=128, seed=1006),
         Workload("longcache_q2048_k8192_d256", B=1, Hq=16, Hkv=2, Lq=2048, Lk=8192, D=256, seed=1007),
+        # profiling case: the 8192 workload's heads at half the length (160 MB, above L2)
+        Workload("qwen3_8b_gqa_l4096_d128", B=1, Hq=32, Hkv=8, Lq=4096, Lk=4096, D=128, seed=1009),
         # decode-shaped: 8 new query rows per sequence against an 8192-key context
         Workload("decode_b4_q8_k8192_d128", B=4, Hq=32, Hkv=8, Lq=8, Lk=8192, D=128, seed=1008),
     ]
@@ -155,6 +157,8 @@ LCE_WORKLOADS = {
     for w in [
         LceWorkload("lce_tiny_n200_d128_v1000", N=200, Dm=128, V=1000, seed=2000),
         LceWorkload("lce_qwen3_8b_n8192", N=8192, Dm=4096, V=151936, seed=2001),
+        # profiling case: same hidden size, a fifth of the vocabulary (256 MB of weights, above L2)
+        LceWorkload("lce_n2048_d4096_v32768", N=2048, Dm=4096, V=32768, seed=2002),
     ]
 }
 
