@@ -412,7 +412,7 @@ def run_ours(args):
     if not args.no_e2e and not kv_cap and not args.decode:
         e2e = run_e2e(args, w, dev, stream, gbattn, credited, bm)
 
-    n_dkv = 1 if w.D <= 128 else 2
+    n_dkv = 1  # one dK/dV launch (at D = 256 it holds both halves)
     extra = {}
     if bm is not None:
         extra = {"block_mask": args.block_mask, "mask_blocks_kept": int(bm_np.sum()),
@@ -442,7 +442,7 @@ def run_ours(args):
         "roofline": roof,
         "kernels": kernels,
         "e2e": e2e,
-        # fwd, delta, dK/dV (two kernels at D = 256), dQ; the decode path adds
+        # fwd, delta, dK/dV, dQ; the decode path adds
         # the combine and the dQ reduction
         "gpu_launches": args.steps * (1 + 1 + n_dkv + 1 + (2 if args.decode else 0)),
         "clocks": clk,

@@ -20,7 +20,8 @@
 // MODE selects which outputs one CTA accumulates.  kDkvBoth keeps dK and dV
 // in tensor memory together (D <= 128).  At D = 256 the two accumulators
 // alone fill the 512 TMEM columns, so dV (kDkvDvOnly: S^T, P^T, dV) and dK
-// (kDkvDkOnly: S^T, dP^T, dS^T, dK) are produced by separate CTAs.
+// (kDkvDkOnly: S^T, dP^T, dS^T, dK) are produced by separate CTAs of one
+// launch (attn_bwd_dkv_kernel below).
 //
 // Warp roles (320 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (key rows) and query columns 32*(w/4)..+31 of each tile;
@@ -76,11 +77,10 @@ struct DkvGeom {
   static_assert((NEED_DS ? DPT_COL + 2 * BQ : ST_COL + 2 * BQ) <= TMEM_COLS, "tensor memory budget");
 };
 
+// One CTA's work: key tile kt of KV head bhk = b * Hkv + hk, in mode MODE.
 template <int D, bool BF16, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
-    attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                        const BwdParams p) {
+__device__ __forceinline__ void dkv_tile(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                         const CUtensorMap& tmdO, const BwdParams& p, const int bhk, const int kt) {
   using Gm = DkvGeom<D, MODE>;
   using E = Elem<BF16>;
   constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
@@ -100,9 +100,7 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
   const uint32_t sQ0 = sbase + Gm::RES_BYTES;
   const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
 
-  const int bhk = blockIdx.x;  // b * Hkv + hk
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
-  const int kt = blockIdx.y;
   const int k0 = kt * BK;
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
   const int nq = p.n_qtiles - qt_start;
@@ -329,6 +327,32 @@ __global__ void __launch_bounds__(DkvGeom<D, MODE>::NUM_THREADS, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
   }
+}
+
+// D = 256: both halves in one launch, x = 2 * (b * Hkv + hk) + (0: dV, 1: dK),
+// y = key tile.  CTAs are dispatched in x-then-y order, so the heavy key tiles
+// (small kt: the most visible query tiles under causal masking) of both halves
+// start first and the light ones of either half fill the tail.
+template <int D>
+struct DkvPairGeom {
+  using Dv = DkvGeom<D, kDkvDvOnly>;
+  using Dk = DkvGeom<D, kDkvDkOnly>;
+  static_assert(Dv::NUM_THREADS == Dk::NUM_THREADS, "one block size for both halves");
+  static constexpr int NUM_THREADS = Dv::NUM_THREADS;
+  static constexpr int SMEM_BYTES = Dv::SMEM_BYTES > Dk::SMEM_BYTES ? Dv::SMEM_BYTES : Dk::SMEM_BYTES;
+  static constexpr int BQ = Dv::BQ, BK = Dv::BK;
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(DkvPairGeom<D>::NUM_THREADS, 1)
+    attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                        const BwdParams p) {
+  const int bhk = static_cast<int>(blockIdx.x >> 1), kt = static_cast<int>(blockIdx.y);
+  if (blockIdx.x & 1)
+    dkv_tile<D, BF16, CAUSAL, kDkvDkOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
+  else
+    dkv_tile<D, BF16, CAUSAL, kDkvDvOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
 }
 
 }  // namespace gbattn

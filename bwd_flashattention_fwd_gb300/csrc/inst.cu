@@ -137,9 +137,10 @@ BwdParams bwd_params(const AttnArgs& a) {
   return p;
 }
 
-template <bool BF16, bool CAUSAL, int MODE>
+// D = 256: the dV and dK halves in one launch (bwd_dkv_kernel.cuh).
+template <bool BF16, bool CAUSAL>
 int dkv_impl(const AttnArgs& a) {
-  using Gm = DkvGeom<kD, MODE>;
+  using Gm = DkvPairGeom<kD>;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
       !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
@@ -148,9 +149,9 @@ int dkv_impl(const AttnArgs& a) {
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
-  const dim3 grid(a.B * a.Hkv, p.n_ktiles);
-  return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL, MODE>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
-                tq, tk, tv, tdo, p);
+  const dim3 grid(2 * a.B * a.Hkv, p.n_ktiles);
+  return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk, tv,
+                tdo, p);
 }
 
 // D <= 128: K held in tensor memory as the A operand of S^T (bwd_dkv2_kernel.cuh).
@@ -222,8 +223,7 @@ int dkv_all(const AttnArgs& a) {
   if constexpr (kD <= 128) {
     return a.block_mask ? dkv2_impl<BF16, CAUSAL, true>(a) : dkv2_impl<BF16, CAUSAL, false>(a);
   } else {
-    const int r = dkv_impl<BF16, CAUSAL, kDkvDvOnly>(a);
-    return r == kLaunchOk ? dkv_impl<BF16, CAUSAL, kDkvDkOnly>(a) : r;
+    return dkv_impl<BF16, CAUSAL>(a);
   }
 }
 
