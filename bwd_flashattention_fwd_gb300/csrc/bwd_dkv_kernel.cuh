@@ -329,6 +329,291 @@ __device__ __forceinline__ void dkv_tile(const CUtensorMap& tmQ, const CUtensorM
   }
 }
 
+// D = 256, dK half.  With K and V both in shared memory (128 KB) only one
+// 64 KB Q/dO stage fits, so loads and MMAs would take turns.  Here K sits in
+// tensor memory as the A operand of S^T = K Q^T (copied in by the row
+// threads), V stays in shared memory for dP^T = V dO^T, and two Q/dO stages
+// fit.  Tensor memory: dK (256 columns), K (128: 256 16-bit values per row),
+// S^T and dP^T (64 each, single buffers).  The row threads copy S^T to
+// registers and release it at once, so S^T of the next query tile is
+// computed while they work; they write dS^T (16-bit pairs) over the dP^T
+// columns they have read, and the one MMA warp issues dK += dS^T Q and then
+// dP^T of the next tile into the same columns (tcgen05 MMAs of one thread
+// run in issue order).
+struct Dk256Geom {
+  static constexpr int D = 256, BK = 128, BQ = 64, NCH = 4;
+  static constexpr int V_BYTES = NCH * BK * 128;  // 64 KB
+  static constexpr int Q_BYTES = NCH * BQ * 128;  // 32 KB
+  static constexpr int STAGES_FIT = (kMaxDynSmem - kSmemReserve - 1024 - V_BYTES) / (2 * Q_BYTES);
+  static constexpr int STAGES = STAGES_FIT > 3 ? 3 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = 1024 + V_BYTES + STAGES * 2 * Q_BYTES;
+  static constexpr int DK_COL = 0, K_COL = 256, ST_COL = 384, DPT_COL = 448;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_COMPUTE_WARPS = 8;
+  static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
+  static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
+  static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
+  static_assert(STAGES >= 2, "two Q/dO stages");
+  static_assert(DPT_COL + BQ <= TMEM_COLS, "tensor memory budget");
+};
+
+template <bool BF16, bool CAUSAL>
+__device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                           const BwdParams& p, const int bhk, const int kt) {
+  using Gm = Dk256Geom;
+  using E = Elem<BF16>;
+  constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_v, bar_kready, bar_stfull[ST], bar_stempty[ST], bar_sfull, bar_sfree, bar_dpfull,
+      bar_pready, bar_accdone;
+  __shared__ __align__(16) float nlse_s[ST][BQ];  // -lse per query column
+  __shared__ __align__(16) float dlt_s[ST][BQ];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sV = sbase;
+  const uint32_t sQ0 = sbase + Gm::V_BYTES;
+  const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
+
+  const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
+  const int k0 = kt * BK;
+  const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
+  const int nq = p.n_qtiles - qt_start;
+  const int n_iter = p.G * nq;  // (query head, query tile) iterations
+  const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_v), 1);
+    mbar_init(smem_u32(&bar_kready), NCT);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(smem_u32(&bar_stfull[s]), 33);  // TMA expect_tx arrive + 32 producer lanes
+      mbar_init(smem_u32(&bar_stempty[s]), 1);  // the MMA warp's last read of the stage (dK)
+    }
+    mbar_init(smem_u32(&bar_sfull), 1);
+    mbar_init(smem_u32(&bar_sfree), NCT);
+    mbar_init(smem_u32(&bar_dpfull), 1);
+    mbar_init(smem_u32(&bar_pready), NCT);
+    mbar_init(smem_u32(&bar_accdone), 1);
+    fence_mbar_init();
+  }
+  if (warp == Gm::MMA_WARP) {
+    tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == Gm::PRODUCER_WARP) {
+    // ---------------- producer (whole warp) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+      tma_prefetch_desc(&tmV);
+    }
+    __syncwarp();
+    mbar_arrive_expect_tx_w(smem_u32(&bar_v), Gm::V_BYTES);
+    for (int c = 0; c < NCH; ++c) tma_load_3d_w(sV + c * BK * 128, &tmV, smem_u32(&bar_v), c * 64, k0, bhk);
+    RingPos<ST> st;
+    int gi = 0, qtile = qt_start;  // query head in the group and query tile of iteration it
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot;
+      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 111);
+      __syncwarp();
+      const int q0 = qtile * BQ;
+      const int zq = b * p.Hq + hk * p.G + gi;
+      mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
+      for (int c = 0; c < NCH; ++c) {
+        tma_load_3d_w(sQ0 + s * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
+        tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
+      }
+#pragma unroll
+      for (int t = 0; t < BQ / 32; ++t) {
+        const int c = lane + 32 * t;
+        const int qi = q0 + c;
+        const size_t row = static_cast<size_t>(zq) * p.Lq + qi;
+        nlse_s[s][c] = qi < p.Lq ? -p.lse[row] : -INFINITY;
+        dlt_s[s][c] = qi < p.Lq ? p.delta[row] : 0.f;
+      }
+      mbar_arrive(smem_u32(&bar_stfull[s]));
+      if (++qtile == p.n_qtiles) qtile = qt_start, ++gi;
+    }
+    mbar_wait_drain(smem_u32(&bar_v), 0, p.limit_ns);
+    for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
+      mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
+  } else if (warp == Gm::MMA_WARP) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
+    constexpr uint32_t IDESC_ACC = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dVk = make_sdesc_sw128(sV, 16, 1024);          // V tile, K-major
+    const uint64_t dQk = make_sdesc_sw128(sQ0, 16, 1024);         // Q stage 0, K-major
+    const uint64_t dOk = make_sdesc_sw128(sdO0, 16, 1024);        // dO stage 0, K-major
+    const uint64_t dQm = make_sdesc_sw128(sQ0, BQ * 128, 1024);   // Q stage 0, MN-major
+    // S^T(it) = K Q^T into its buffer (K from tensor memory)
+    auto issue_s = [&](int s) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = s * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        mma_ts_w(tmem + Gm::ST_COL, tmem + Gm::K_COL + kk * 8, sdesc_add(dQk, qo), IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_sfull));
+    };
+    // dP^T(it) = V dO^T into its buffer
+    auto issue_dp = [&](int s) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t vo = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        const uint32_t qo = s * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        mma_ss_w(tmem + Gm::DPT_COL, sdesc_add(dVk, vo), sdesc_add(dOk, qo), IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_dpfull));
+    };
+    mbar_wait(smem_u32(&bar_kready), 0, g, kDevTimeoutBase + 112);
+    mbar_wait(smem_u32(&bar_v), 0, g, kDevTimeoutBase + 113);
+    RingPos<ST> st, st_n;  // stage of iteration it and of it + 1
+    st_n.next();
+    if (n_iter > 0) {
+      mbar_wait(smem_u32(&bar_stfull[0]), 0, g, kDevTimeoutBase + 114);
+      __syncwarp();
+      tc_fence_after_sync();
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int it = 0; it < n_iter; ++it, st.next(), st_n.next()) {
+      const int s = st.slot;
+      const bool more = it + 1 < n_iter;
+      if (more) {
+        // the row threads hold S^T(it) in registers: S^T(it+1) may overwrite it
+        mbar_wait(smem_u32(&bar_sfree), it & 1, g, kDevTimeoutBase + 115);
+        mbar_wait(smem_u32(&bar_stfull[st_n.slot]), st_n.phase, g, kDevTimeoutBase + 116);
+        __syncwarp();
+        tc_fence_after_sync();
+        issue_s(st_n.slot);
+      }
+      // dS^T(it) is in the dP^T columns
+      mbar_wait(smem_u32(&bar_pready), it & 1, g, kDevTimeoutBase + 117);
+      __syncwarp();
+      tc_fence_after_sync();
+      // A operand: 16 queries per K step; queries 32h..32h+31 of warpgroup h
+      // sit as pairs in columns 32h..32h+15 of the buffer.
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk) {
+        const uint32_t acol = Gm::DPT_COL + (kk >> 1) * 32 + (kk & 1) * 8;
+        mma_ts_w(tmem + Gm::DK_COL, tmem + acol, sdesc_add(dQm, s * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      // S^T(it), dP^T(it) and dK(it) were this thread's reads of the stage
+      mma_commit_w(smem_u32(&bar_stempty[s]));
+      // dP^T(it+1) overwrites dS^T(it) behind the dK MMAs that read it
+      if (more) issue_dp(st_n.slot);
+    }
+    mma_commit_w(smem_u32(&bar_accdone));
+    mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+    __syncwarp();
+  } else {
+    // ---------------- key-row threads ----------------
+    const int quad = warp & 3;   // TMEM lane quadrant (key rows)
+    const int half = warp >> 2;  // query columns 32*half .. +31; K / dK columns half*128 .. +127
+    const int r = quad * 32 + lane;
+    const int kj = k0 + r;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const int qmin = kj - p.off;  // causal: queries below this index cannot see key kj
+    {
+      // K row into tensor memory: this thread copies elements [half*128, half*128+128)
+      // of key row kj (zeros past Lk) as 64 columns of 16-bit pairs.
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(p.k) +
+                                                        (static_cast<size_t>(bhk) * p.kv_pitch + kj) * D + half * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t t16[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (kj < p.Lk) x = src[c * 4 + v];
+          t16[4 * v + 0] = x.x, t16[4 * v + 1] = x.y, t16[4 * v + 2] = x.z, t16[4 * v + 3] = x.w;
+        }
+        tmem_st16(tmem + lrow + Gm::K_COL + half * 64 + c * 16, t16);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_kready));
+    }
+    RingPos<ST> st;
+    int qtile = qt_start;
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot;
+      const int q0 = qtile * BQ;
+      if (++qtile == p.n_qtiles) qtile = qt_start;
+      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 118);
+      mbar_wait(smem_u32(&bar_sfull), it & 1, g, kDevTimeoutBase + 119);
+      __syncwarp();
+      tc_fence_after_sync();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + lrow + Gm::ST_COL + half * 32, sr);
+      tmem_ld_wait(sr);
+      // S^T(it) is in registers: the next S^T may overwrite the buffer
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_sfree));
+      mbar_wait(smem_u32(&bar_dpfull), it & 1, g, kDevTimeoutBase + 120);
+      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t dcol = tmem + lrow + Gm::DPT_COL + half * 32;
+      tmem_ld32(dcol, dr);
+      tmem_ld_wait(dr);
+      const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
+      const uint64_t* nlse_row = reinterpret_cast<const uint64_t*>(&nlse_s[s][half * 32]);
+      const uint64_t* dlt_row = reinterpret_cast<const uint64_t*>(&dlt_s[s][half * 32]);
+      const int qc0 = q0 + half * 32;
+      uint32_t dk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c0 = 2 * i;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), sl2x2, nlse_row[i]), x0, x1);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (need_mask) {
+          if (qc0 + c0 < qmin) p0 = 0.f;
+          if (qc0 + c0 + 1 < qmin) p1 = 0.f;
+        }
+        const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[c0]), __uint_as_float(dr[c0 + 1])), dlt_row[i]);
+        float ds0, ds1;
+        f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
+        dk[i] = E::pack(ds0, ds1);
+      }
+      tmem_st16(dcol, dk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_pready));
+    }
+    mbar_wait(smem_u32(&bar_accdone), 0, g, kDevTimeoutBase + 121);
+    __syncwarp();
+    tc_fence_after_sync();
+    // epilogue: warpgroup `half` writes dK columns [half*128, half*128+128)
+    typename E::T* dst = reinterpret_cast<typename E::T*>(p.dk) + (static_cast<size_t>(bhk) * p.Lk + kj) * D;
+#pragma unroll 1
+    for (int c = half * 4; c < half * 4 + 4; ++c) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
+      tmem_ld_wait(rr);
+      if (kj < p.Lk) store_row32<BF16>(dst + c * 32, rr, p.scale);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Gm::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+}
+
 // D = 256: both halves in one launch, x = 2 * (b * Hkv + hk) + (0: dV, 1: dK),
 // y = key tile.  CTAs are dispatched in x-then-y order, so the heavy key tiles
 // (small kt: the most visible query tiles under causal masking) of both halves
@@ -337,9 +622,10 @@ template <int D>
 struct DkvPairGeom {
   using Dv = DkvGeom<D, kDkvDvOnly>;
   using Dk = DkvGeom<D, kDkvDkOnly>;
-  static_assert(Dv::NUM_THREADS == Dk::NUM_THREADS, "one block size for both halves");
+  static_assert(Dv::NUM_THREADS == Dk256Geom::NUM_THREADS, "one block size for both halves");
   static constexpr int NUM_THREADS = Dv::NUM_THREADS;
-  static constexpr int SMEM_BYTES = Dv::SMEM_BYTES > Dk::SMEM_BYTES ? Dv::SMEM_BYTES : Dk::SMEM_BYTES;
+  static constexpr int SMEM_BYTES =
+      Dv::SMEM_BYTES > Dk256Geom::SMEM_BYTES ? Dv::SMEM_BYTES : Dk256Geom::SMEM_BYTES;
   static constexpr int BQ = Dv::BQ, BK = Dv::BK;
 };
 
@@ -349,9 +635,12 @@ __global__ void __launch_bounds__(DkvPairGeom<D>::NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                         const BwdParams p) {
   const int bhk = static_cast<int>(blockIdx.x >> 1), kt = static_cast<int>(blockIdx.y);
-  if (blockIdx.x & 1)
-    dkv_tile<D, BF16, CAUSAL, kDkvDkOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
-  else
+  if (blockIdx.x & 1) {
+    if constexpr (D == 256)
+      dk256_tile<BF16, CAUSAL>(tmQ, tmV, tmdO, p, bhk, kt);
+    else
+      dkv_tile<D, BF16, CAUSAL, kDkvDkOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
+  } else
     dkv_tile<D, BF16, CAUSAL, kDkvDvOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
 }
 

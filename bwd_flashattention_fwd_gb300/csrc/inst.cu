@@ -134,6 +134,7 @@ BwdParams bwd_params(const AttnArgs& a) {
   p.bmask = a.block_mask;
   p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
   p.kv_pitch = a.kv_pitch > 0 ? a.kv_pitch : a.Lk;
+  p.k = a.k;
   return p;
 }
 
