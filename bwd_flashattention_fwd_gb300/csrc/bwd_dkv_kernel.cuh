@@ -614,6 +614,234 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
   }
 }
 
+// D = 256, dV half: K in tensor memory as for the dK half, so shared memory
+// holds only Q/dO stages (three of 64 KB, enough to hide the loads' latency).
+// Tensor memory: dV (256 columns), K (128), S^T (two buffers of 64).  The row
+// threads turn S^T into P^T (16-bit pairs, written over the columns they
+// read) and the MMA warp issues dV += P^T dO, then S^T of the tile after
+// next into the same buffer.
+struct Dv256Geom {
+  static constexpr int D = 256, BK = 128, BQ = 64, NCH = 4;
+  static constexpr int Q_BYTES = NCH * BQ * 128;  // 32 KB
+  static constexpr int STAGES_FIT = (kMaxDynSmem - kSmemReserve - 1024) / (2 * Q_BYTES);
+  static constexpr int STAGES = STAGES_FIT > 3 ? 3 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * Q_BYTES;
+  static constexpr int DV_COL = 0, K_COL = 256, ST_COL = 384;  // S^T: 2 x 64
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_COMPUTE_WARPS = 8;
+  static constexpr int NCT = 32 * NUM_COMPUTE_WARPS;
+  static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
+  static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
+  static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
+  static_assert(STAGES >= 3, "three Q/dO stages");
+  static_assert(ST_COL + 2 * BQ <= TMEM_COLS, "tensor memory budget");
+};
+
+template <bool BF16, bool CAUSAL>
+__device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtensorMap& tmdO, const BwdParams& p,
+                                           const int bhk, const int kt) {
+  using Gm = Dv256Geom;
+  using E = Elem<BF16>;
+  constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_kready, bar_stfull[ST], bar_stempty[ST], bar_sfull[2], bar_pready[2], bar_accdone;
+  __shared__ __align__(16) float nlse_s[ST][BQ];  // -lse per query column
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ0 = sbase;
+  const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
+
+  const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
+  const int k0 = kt * BK;
+  const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
+  const int nq = p.n_qtiles - qt_start;
+  const int n_iter = p.G * nq;
+  const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_kready), NCT);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(smem_u32(&bar_stfull[s]), 33);  // TMA expect_tx arrive + 32 producer lanes
+      mbar_init(smem_u32(&bar_stempty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_sfull[i]), 1);
+      mbar_init(smem_u32(&bar_pready[i]), NCT);
+    }
+    mbar_init(smem_u32(&bar_accdone), 1);
+    fence_mbar_init();
+  }
+  if (warp == Gm::MMA_WARP) {
+    tmem_alloc(smem_u32(&tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == Gm::PRODUCER_WARP) {
+    // ---------------- producer (whole warp) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+    }
+    __syncwarp();
+    RingPos<ST> st;
+    int gi = 0, qtile = qt_start;
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot;
+      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 131);
+      __syncwarp();
+      const int q0 = qtile * BQ;
+      const int zq = b * p.Hq + hk * p.G + gi;
+      mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
+      for (int c = 0; c < NCH; ++c) {
+        tma_load_3d_w(sQ0 + s * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
+        tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
+      }
+#pragma unroll
+      for (int t = 0; t < BQ / 32; ++t) {
+        const int c = lane + 32 * t;
+        const int qi = q0 + c;
+        nlse_s[s][c] = qi < p.Lq ? -p.lse[static_cast<size_t>(zq) * p.Lq + qi] : -INFINITY;
+      }
+      mbar_arrive(smem_u32(&bar_stfull[s]));
+      if (++qtile == p.n_qtiles) qtile = qt_start, ++gi;
+    }
+    for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
+      mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
+  } else if (warp == Gm::MMA_WARP) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
+    constexpr uint32_t IDESC_ACC = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dQk = make_sdesc_sw128(sQ0, 16, 1024);         // Q stage 0, K-major
+    const uint64_t dOm = make_sdesc_sw128(sdO0, BQ * 128, 1024);  // dO stage 0, MN-major
+    RingPos<ST> st, st_s;  // stages of the next dV and of the next S^T
+    auto issue_s = [&](int it) {
+      const int s = st_s.slot;
+      mbar_wait(smem_u32(&bar_stfull[s]), st_s.phase, g, kDevTimeoutBase + 132);
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = s * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        mma_ts_w(tmem + Gm::ST_COL + (it & 1) * BQ, tmem + Gm::K_COL + kk * 8, sdesc_add(dQk, qo), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_sfull[it & 1]));
+      st_s.next();
+    };
+    mbar_wait(smem_u32(&bar_kready), 0, g, kDevTimeoutBase + 133);
+    for (int it = 0; it < 2 && it < n_iter; ++it) issue_s(it);
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot, buf = it & 1;
+      mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 134);
+      __syncwarp();
+      tc_fence_after_sync();
+      // A operand: queries 32h..32h+31 of warpgroup h as pairs in columns
+      // 32h..32h+15 of the buffer
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk) {
+        const uint32_t acol = Gm::ST_COL + buf * BQ + (kk >> 1) * 32 + (kk & 1) * 8;
+        mma_ts_w(tmem + Gm::DV_COL, tmem + acol, sdesc_add(dOm, s * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_w(smem_u32(&bar_stempty[s]));
+      // S^T(it+2) overwrites P^T(it) behind the dV MMAs that read it
+      if (it + 2 < n_iter) issue_s(it + 2);
+    }
+    mma_commit_w(smem_u32(&bar_accdone));
+    mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+    __syncwarp();
+  } else {
+    // ---------------- key-row threads ----------------
+    const int quad = warp & 3;
+    const int half = warp >> 2;  // query columns 32*half .. +31; K / dV columns half*128 .. +127
+    const int r = quad * 32 + lane;
+    const int kj = k0 + r;
+    const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const int qmin = kj - p.off;
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(p.k) +
+                                                        (static_cast<size_t>(bhk) * p.kv_pitch + kj) * D + half * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t t16[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (kj < p.Lk) x = src[c * 4 + v];
+          t16[4 * v + 0] = x.x, t16[4 * v + 1] = x.y, t16[4 * v + 2] = x.z, t16[4 * v + 3] = x.w;
+        }
+        tmem_st16(tmem + lrow + Gm::K_COL + half * 64 + c * 16, t16);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_kready));
+    }
+    RingPos<ST> st;
+    int qtile = qt_start;
+    for (int it = 0; it < n_iter; ++it, st.next()) {
+      const int s = st.slot, buf = it & 1;
+      const int q0 = qtile * BQ;
+      if (++qtile == p.n_qtiles) qtile = qt_start;
+      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 135);
+      mbar_wait(smem_u32(&bar_sfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 136);
+      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t scol = tmem + lrow + Gm::ST_COL + buf * BQ + half * 32;
+      uint32_t sr[32];
+      tmem_ld32(scol, sr);
+      tmem_ld_wait(sr);
+      const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
+      const uint64_t* nlse_row = reinterpret_cast<const uint64_t*>(&nlse_s[s][half * 32]);
+      const int qc0 = q0 + half * 32;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c0 = 2 * i;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), sl2x2, nlse_row[i]), x0, x1);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (need_mask) {
+          if (qc0 + c0 < qmin) p0 = 0.f;
+          if (qc0 + c0 + 1 < qmin) p1 = 0.f;
+        }
+        pk[i] = E::pack(p0, p1);
+      }
+      tmem_st16(scol, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_pready[buf]));
+    }
+    mbar_wait(smem_u32(&bar_accdone), 0, g, kDevTimeoutBase + 137);
+    __syncwarp();
+    tc_fence_after_sync();
+    typename E::T* dst = reinterpret_cast<typename E::T*>(p.dv) + (static_cast<size_t>(bhk) * p.Lk + kj) * D;
+#pragma unroll 1
+    for (int c = half * 4; c < half * 4 + 4; ++c) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
+      tmem_ld_wait(rr);
+      if (kj < p.Lk) store_row32<BF16>(dst + c * 32, rr, 1.f);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == Gm::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+}
+
 // D = 256: both halves in one launch, x = 2 * (b * Hkv + hk) + (0: dV, 1: dK),
 // y = key tile.  CTAs are dispatched in x-then-y order, so the heavy key tiles
 // (small kt: the most visible query tiles under causal masking) of both halves
@@ -622,10 +850,11 @@ template <int D>
 struct DkvPairGeom {
   using Dv = DkvGeom<D, kDkvDvOnly>;
   using Dk = DkvGeom<D, kDkvDkOnly>;
-  static_assert(Dv::NUM_THREADS == Dk256Geom::NUM_THREADS, "one block size for both halves");
+  static_assert(Dv::NUM_THREADS == Dk256Geom::NUM_THREADS && Dv256Geom::NUM_THREADS == Dk256Geom::NUM_THREADS,
+                "one block size for both halves");
   static constexpr int NUM_THREADS = Dv::NUM_THREADS;
-  static constexpr int SMEM_BYTES =
-      Dv::SMEM_BYTES > Dk256Geom::SMEM_BYTES ? Dv::SMEM_BYTES : Dk256Geom::SMEM_BYTES;
+  static constexpr int SMEM_A = Dv::SMEM_BYTES > Dk256Geom::SMEM_BYTES ? Dv::SMEM_BYTES : Dk256Geom::SMEM_BYTES;
+  static constexpr int SMEM_BYTES = SMEM_A > Dv256Geom::SMEM_BYTES ? SMEM_A : Dv256Geom::SMEM_BYTES;
   static constexpr int BQ = Dv::BQ, BK = Dv::BK;
 };
 
@@ -640,8 +869,12 @@ __global__ void __launch_bounds__(DkvPairGeom<D>::NUM_THREADS, 1)
       dk256_tile<BF16, CAUSAL>(tmQ, tmV, tmdO, p, bhk, kt);
     else
       dkv_tile<D, BF16, CAUSAL, kDkvDkOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
-  } else
-    dkv_tile<D, BF16, CAUSAL, kDkvDvOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
+  } else {
+    if constexpr (D == 256)
+      dv256_tile<BF16, CAUSAL>(tmQ, tmdO, p, bhk, kt);
+    else
+      dkv_tile<D, BF16, CAUSAL, kDkvDvOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
+  }
 }
 
 }  // namespace gbattn
