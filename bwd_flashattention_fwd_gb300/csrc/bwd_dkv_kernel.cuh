@@ -334,12 +334,13 @@ __device__ __forceinline__ void dkv_tile(const CUtensorMap& tmQ, const CUtensorM
 // tensor memory as the A operand of S^T = K Q^T (copied in by the row
 // threads), V stays in shared memory for dP^T = V dO^T, and two Q/dO stages
 // fit.  Tensor memory: dK (256 columns), K (128: 256 16-bit values per row),
-// S^T and dP^T (64 each, single buffers).  The row threads copy S^T to
-// registers and release it at once, so S^T of the next query tile is
-// computed while they work; they write dS^T (16-bit pairs) over the dP^T
-// columns they have read, and the one MMA warp issues dK += dS^T Q and then
-// dP^T of the next tile into the same columns (tcgen05 MMAs of one thread
-// run in issue order).
+// S^T and dP^T (64 each, single buffers).  The row threads copy S^T and dP^T
+// to registers and release dP^T at once, so dP^T of the next query tile (the
+// slower product: both of its operands come from shared memory) is computed
+// while they work; they write dS^T (16-bit pairs) over the S^T columns they
+// have read, and the one MMA warp issues dK += dS^T Q and then S^T of the
+// next tile into the same columns (tcgen05 MMAs of one thread run in issue
+// order).
 struct Dk256Geom {
   static constexpr int D = 256, BK = 128, BQ = 64, NCH = 4;
   static constexpr int V_BYTES = NCH * BK * 128;  // 64 KB
@@ -366,7 +367,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
   constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_v, bar_kready, bar_stfull[ST], bar_stempty[ST], bar_sfull, bar_sfree, bar_dpfull,
+  __shared__ uint64_t bar_v, bar_kready, bar_stfull[ST], bar_stempty[ST], bar_sfull, bar_dpfree, bar_dpfull,
       bar_pready, bar_accdone;
   __shared__ __align__(16) float nlse_s[ST][BQ];  // -lse per query column
   __shared__ __align__(16) float dlt_s[ST][BQ];
@@ -395,7 +396,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       mbar_init(smem_u32(&bar_stempty[s]), 1);  // the MMA warp's last read of the stage (dK)
     }
     mbar_init(smem_u32(&bar_sfull), 1);
-    mbar_init(smem_u32(&bar_sfree), NCT);
+    mbar_init(smem_u32(&bar_dpfree), NCT);
     mbar_init(smem_u32(&bar_dpfull), 1);
     mbar_init(smem_u32(&bar_pready), NCT);
     mbar_init(smem_u32(&bar_accdone), 1);
@@ -489,14 +490,14 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       const int s = st.slot;
       const bool more = it + 1 < n_iter;
       if (more) {
-        // the row threads hold S^T(it) in registers: S^T(it+1) may overwrite it
-        mbar_wait(smem_u32(&bar_sfree), it & 1, g, kDevTimeoutBase + 115);
+        // the row threads hold dP^T(it) in registers: dP^T(it+1) may overwrite it
+        mbar_wait(smem_u32(&bar_dpfree), it & 1, g, kDevTimeoutBase + 115);
         mbar_wait(smem_u32(&bar_stfull[st_n.slot]), st_n.phase, g, kDevTimeoutBase + 116);
         __syncwarp();
         tc_fence_after_sync();
-        issue_s(st_n.slot);
+        issue_dp(st_n.slot);
       }
-      // dS^T(it) is in the dP^T columns
+      // dS^T(it) is in the S^T columns
       mbar_wait(smem_u32(&bar_pready), it & 1, g, kDevTimeoutBase + 117);
       __syncwarp();
       tc_fence_after_sync();
@@ -504,14 +505,14 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       // sit as pairs in columns 32h..32h+15 of the buffer.
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk) {
-        const uint32_t acol = Gm::DPT_COL + (kk >> 1) * 32 + (kk & 1) * 8;
+        const uint32_t acol = Gm::ST_COL + (kk >> 1) * 32 + (kk & 1) * 8;
         mma_ts_w(tmem + Gm::DK_COL, tmem + acol, sdesc_add(dQm, s * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
                  (it > 0 || kk > 0) ? 1u : 0u);
       }
       // S^T(it), dP^T(it) and dK(it) were this thread's reads of the stage
       mma_commit_w(smem_u32(&bar_stempty[s]));
-      // dP^T(it+1) overwrites dS^T(it) behind the dK MMAs that read it
-      if (more) issue_dp(st_n.slot);
+      // S^T(it+1) overwrites dS^T(it) behind the dK MMAs that read it
+      if (more) issue_s(st_n.slot);
     }
     mma_commit_w(smem_u32(&bar_accdone));
     mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
@@ -556,17 +557,17 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       __syncwarp();
       tc_fence_after_sync();
       uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lrow + Gm::ST_COL + half * 32, sr);
+      const uint32_t scol = tmem + lrow + Gm::ST_COL + half * 32;
+      tmem_ld32(scol, sr);
       tmem_ld_wait(sr);
-      // S^T(it) is in registers: the next S^T may overwrite the buffer
-      tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bar_sfree));
       mbar_wait(smem_u32(&bar_dpfull), it & 1, g, kDevTimeoutBase + 120);
       __syncwarp();
       tc_fence_after_sync();
-      const uint32_t dcol = tmem + lrow + Gm::DPT_COL + half * 32;
-      tmem_ld32(dcol, dr);
+      tmem_ld32(tmem + lrow + Gm::DPT_COL + half * 32, dr);
       tmem_ld_wait(dr);
+      // dP^T(it) is in registers: the next dP^T may overwrite the buffer
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_dpfree));
       const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
       const uint64_t* nlse_row = reinterpret_cast<const uint64_t*>(&nlse_s[s][half * 32]);
       const uint64_t* dlt_row = reinterpret_cast<const uint64_t*>(&dlt_s[s][half * 32]);
@@ -587,7 +588,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
         f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
         dk[i] = E::pack(ds0, ds1);
       }
-      tmem_st16(dcol, dk);
+      tmem_st16(scol, dk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready));
