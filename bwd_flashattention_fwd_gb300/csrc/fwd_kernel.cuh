@@ -11,7 +11,7 @@
 // Warp roles (192 threads):
 //   warps 0-3  softmax: thread t of warp w owns query row 32w+t, which is TMEM
 //              lane 32w+t of every accumulator;
-//   warp 4     TMA producer: Q once, then K/V tiles into a STAGES-deep ring;
+//   warp 4     TMA producer: Q once, then K and V tiles into their rings;
 //   warp 5     MMA issuer (one thread) and TMEM owner.
 // Tensor memory (512 columns): O (D columns, fp32), two S buffers (BK columns
 // each, fp32) and two P buffers (BK/2 columns, bf16/fp16 pairs).  S_j = Q K_j^T
@@ -38,9 +38,13 @@ struct FwdGeom {
   static constexpr int NCH = n_chunks(D);
   static constexpr int Q_BYTES = NCH * BQ * 128;
   static constexpr int KV_BYTES = NCH * BK * 128;
-  static constexpr int STAGES_FIT = (kMaxDynSmem - kSmemReserve - 1024 - Q_BYTES) / (2 * KV_BYTES);
-  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * 2 * KV_BYTES;
+  // K and V tiles have rings of their own: a K tile is free once S = Q K^T
+  // has read it, a V tile only after P V, so the K ring runs further ahead.
+  // (The kernel's static shared memory, barriers only, stays under 1 KB.)
+  static constexpr int SLOTS = (kMaxDynSmem - 1024 - 1024 - Q_BYTES) / KV_BYTES;
+  static constexpr int KSTAGES = SLOTS - 2 > 4 ? 4 : SLOTS - 2;
+  static constexpr int VSTAGES = SLOTS - KSTAGES > 4 ? 4 : SLOTS - KSTAGES;
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES;
   static constexpr int O_COL = 0;
   static constexpr int S_COL0 = (D <= 128) ? 128 : 256;
   static constexpr int S_COL1 = S_COL0 + BK;
@@ -48,7 +52,7 @@ struct FwdGeom {
   static constexpr int P_COL1 = P_COL0 + BK / 2;
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_THREADS = 192;
-  static_assert(STAGES >= 2, "need a double-buffered K/V ring");
+  static_assert(KSTAGES >= 2 && VSTAGES >= 2, "need double-buffered K and V rings");
   static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
 };
 
@@ -58,10 +62,10 @@ __global__ void __launch_bounds__(192, 1)
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Gm = FwdGeom<D>;
   using E = Elem<BF16>;
-  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
+  constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, KST = Gm::KSTAGES, VST = Gm::VSTAGES;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kfull[ST], bar_vfull[ST], bar_kvempty[ST], bar_sfull[2],
+  __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
       bar_pready[2], bar_odone, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;
   const uint32_t sK0 = sQ + Gm::Q_BYTES;
-  const uint32_t sV0 = sK0 + ST * Gm::KV_BYTES;
+  const uint32_t sV0 = sK0 + KST * Gm::KV_BYTES;
 
   const int bh = blockIdx.x;  // b * Hq + hq (decode: b * Hkv + hk, with Hq = Hkv, G = 1)
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
@@ -87,10 +91,13 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(smem_u32(&bar_kfull[s]), 1);
+      mbar_init(smem_u32(&bar_kempty[s]), 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(smem_u32(&bar_vfull[s]), 1);
-      mbar_init(smem_u32(&bar_kvempty[s]), 1);
+      mbar_init(smem_u32(&bar_vempty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_sfull[i]), 1);
@@ -120,22 +127,28 @@ __global__ void __launch_bounds__(192, 1)
     const int zkv = b * p.Hkv + hk;
     mbar_arrive_expect_tx_w(smem_u32(&bar_q), Gm::Q_BYTES);
     for (int c = 0; c < NCH; ++c) tma_load_3d_w(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % ST, u = j / ST;
-      if (u > 0) mbar_wait(smem_u32(&bar_kvempty[s]), (u - 1) & 1, g, kDevTimeoutBase + 1);
+    RingPos<KST> kp;
+    RingPos<VST> vp;
+    for (int j = 0; j < n_kv; ++j, kp.next(), vp.next()) {
+      const int ks = kp.slot, vs = vp.slot;
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), kp.phase ^ 1u, g, kDevTimeoutBase + 1);
       __syncwarp();
-      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[s]), Gm::KV_BYTES);
+      mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sK0 + s * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[s]), c * 64, (j0 + j) * BK,
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, (j0 + j) * BK,
                       zkv);
-      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[s]), Gm::KV_BYTES);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), vp.phase ^ 1u, g, kDevTimeoutBase + 9);
+      __syncwarp();
+      mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sV0 + s * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[s]), c * 64, (j0 + j) * BK,
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, (j0 + j) * BK,
                       zkv);
     }
     // Do not leave the CTA while a copy may still be landing.
-    for (int j = (n_kv > ST ? n_kv - ST : 0); j < n_kv; ++j)
-      mbar_wait_drain(smem_u32(&bar_vfull[j % ST]), (j / ST) & 1, p.limit_ns);
+    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == 5) {
     // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
@@ -149,8 +162,8 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after_sync();
     for (int j = 0; j <= n_kv; ++j) {
       if (j < n_kv) {
-        const int s = j % ST;
-        mbar_wait(smem_u32(&bar_kfull[s]), (j / ST) & 1, g, kDevTimeoutBase + 3);
+        const int s = j % KST;
+        mbar_wait(smem_u32(&bar_kfull[s]), (j / KST) & 1, g, kDevTimeoutBase + 3);
         __syncwarp();
         tc_fence_after_sync();
         const uint32_t d = tmem + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
@@ -161,11 +174,12 @@ __global__ void __launch_bounds__(192, 1)
           mma_ss_w(d, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
         }
         mma_commit_w(smem_u32(&bar_sfull[j & 1]));
+        mma_commit_w(smem_u32(&bar_kempty[s]));  // S_j was K_j's only reader
       }
       if (j >= 1) {
-        const int jp = j - 1, sp = jp % ST;
+        const int jp = j - 1, sp = jp % VST;
         mbar_wait(smem_u32(&bar_pready[jp & 1]), (jp >> 1) & 1, g, kDevTimeoutBase + 4);
-        mbar_wait(smem_u32(&bar_vfull[sp]), (jp / ST) & 1, g, kDevTimeoutBase + 5);
+        mbar_wait(smem_u32(&bar_vfull[sp]), (jp / VST) & 1, g, kDevTimeoutBase + 5);
         __syncwarp();
         tc_fence_after_sync();
         const uint32_t pcol = tmem + ((jp & 1) ? Gm::P_COL1 : Gm::P_COL0);
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_ts_w(tmem + Gm::O_COL, pcol + kk * 8, sdesc_add(dVm, sp * Gm::KV_BYTES + kk * 2048), IDESC_PV,
                    (jp > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(smem_u32(&bar_kvempty[sp]));
+        mma_commit_w(smem_u32(&bar_vempty[sp]));
         mma_commit_w(smem_u32(&bar_odone));
       }
     }
