@@ -58,7 +58,7 @@ from bwd_flashattention_fwd_gb300.inputs import (  # noqa: E402
 )
 
 METRIC = "fwd+bwd attention TFLOP/s, causal GQA L=8192 D=128 bf16; % of BF16 TC peak"
-METRIC_MASKED = "block-sparse fwd+bwd attention TFLOP/s (3.5 x 4*D FLOPs per visible pair), GQA D=128 bf16"
+METRIC_MASKED = "block-sparse fwd+bwd attention TFLOP/s (3.5 x 4*D FLOPs per visible pair)"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "qwen3_8b_gqa_l8192_d128"
 L2_FLUSH_BYTES = 256 << 20

@@ -182,7 +182,6 @@ attn_status_t fwd_call(const void* q, const void* k, const void* v, void* o, flo
   if (s != ATTN_OK) return s;
   s = check_kv_pitch(kv_pitch, Lk, D);
   if (s != ATTN_OK) return s;
-  if (block_mask && D > 128) return ATTN_ERR_UNSUPPORTED;
   AttnArgs a;
   int dev;
   const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
@@ -207,7 +206,6 @@ attn_status_t bwd_call(const void* q, const void* k, const void* v, const void* 
   if (s != ATTN_OK) return s;
   s = check_kv_pitch(kv_pitch, Lk, D);
   if (s != ATTN_OK) return s;
-  if (block_mask && D > 128) return ATTN_ERR_UNSUPPORTED;
   AttnArgs a;
   int dev;
   const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
@@ -276,7 +274,7 @@ extern "C" attn_status_t attn_bwd(const void* q, const void* k, const void* v, c
 }
 
 // Block-sparse variants: the same calls with a [ceil(Lq/128), ceil(Lk/128)]
-// uint8 block mask on the device; head dimensions up to 128.
+// uint8 block mask on the device.
 extern "C" attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
                                          const uint8_t* block_mask, int B, int Hq, int Hkv, int Lq, int Lk, int D,
                                          float scale, int causal, attn_dtype_t dtype, cudaStream_t stream) {

@@ -359,7 +359,7 @@ struct Dk256Geom {
   static_assert(DPT_COL + BQ <= TMEM_COLS, "tensor memory budget");
 };
 
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool MASKED>
 __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                            const BwdParams& p, const int bhk, const int kt) {
   using Gm = Dk256Geom;
@@ -383,8 +383,10 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int k0 = kt * BK;
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
-  const int nq = p.n_qtiles - qt_start;
-  const int n_iter = p.G * nq;  // (query head, query tile) iterations
+  // query tile qt is computed (block mask: the CTA's 128 keys are one mask
+  // column, a 64-row query tile half a mask row)
+  auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
+  const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);  // (query head, query tile) iterations
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -422,7 +424,8 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     mbar_arrive_expect_tx_w(smem_u32(&bar_v), Gm::V_BYTES);
     for (int c = 0; c < NCH; ++c) tma_load_3d_w(sV + c * BK * 128, &tmV, smem_u32(&bar_v), c * 64, k0, bhk);
     RingPos<ST> st;
-    int gi = 0, qtile = qt_start;  // query head in the group and query tile of iteration it
+    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
+    int gi = 0, qtile = qw.first(qt_start);  // query head in the group and query tile of iteration it
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 111);
@@ -443,7 +446,8 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
         dlt_s[s][c] = qi < p.Lq ? p.delta[row] : 0.f;
       }
       mbar_arrive(smem_u32(&bar_stfull[s]));
-      if (++qtile == p.n_qtiles) qtile = qt_start, ++gi;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
     }
     mbar_wait_drain(smem_u32(&bar_v), 0, p.limit_ns);
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
@@ -547,11 +551,13 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       mbar_arrive(smem_u32(&bar_kready));
     }
     RingPos<ST> st;
-    int qtile = qt_start;
+    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
+    int qtile = qw.first(qt_start);
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       const int q0 = qtile * BQ;
-      if (++qtile == p.n_qtiles) qtile = qt_start;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start);
       mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 118);
       mbar_wait(smem_u32(&bar_sfull), it & 1, g, kDevTimeoutBase + 119);
       __syncwarp();
@@ -601,8 +607,13 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll 1
     for (int c = half * 4; c < half * 4 + 4; ++c) {
       uint32_t rr[32];
-      tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
-      tmem_ld_wait(rr);
+      if (n_iter > 0) {  // the same for the whole CTA: tcgen05.ld is warp-collective
+        tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept query tile: dK = 0
+      }
       if (kj < p.Lk) store_row32<BF16>(dst + c * 32, rr, p.scale);
     }
   }
@@ -638,7 +649,7 @@ struct Dv256Geom {
   static_assert(ST_COL + 2 * BQ <= TMEM_COLS, "tensor memory budget");
 };
 
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool MASKED>
 __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtensorMap& tmdO, const BwdParams& p,
                                            const int bhk, const int kt) {
   using Gm = Dv256Geom;
@@ -659,8 +670,10 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int k0 = kt * BK;
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
-  const int nq = p.n_qtiles - qt_start;
-  const int n_iter = p.G * nq;
+  // query tile qt is computed (block mask: the CTA's 128 keys are one mask
+  // column, a 64-row query tile half a mask row)
+  auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
+  const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);  // (query head, query tile) iterations
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -694,7 +707,8 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     }
     __syncwarp();
     RingPos<ST> st;
-    int gi = 0, qtile = qt_start;
+    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
+    int gi = 0, qtile = qw.first(qt_start);
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 131);
@@ -713,7 +727,8 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
         nlse_s[s][c] = qi < p.Lq ? -p.lse[static_cast<size_t>(zq) * p.Lq + qi] : -INFINITY;
       }
       mbar_arrive(smem_u32(&bar_stfull[s]));
-      if (++qtile == p.n_qtiles) qtile = qt_start, ++gi;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
     }
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
       mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
@@ -788,11 +803,13 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       mbar_arrive(smem_u32(&bar_kready));
     }
     RingPos<ST> st;
-    int qtile = qt_start;
+    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
+    int qtile = qw.first(qt_start);
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot, buf = it & 1;
       const int q0 = qtile * BQ;
-      if (++qtile == p.n_qtiles) qtile = qt_start;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start);
       mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 135);
       mbar_wait(smem_u32(&bar_sfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 136);
       __syncwarp();
@@ -829,8 +846,13 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll 1
     for (int c = half * 4; c < half * 4 + 4; ++c) {
       uint32_t rr[32];
-      tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
-      tmem_ld_wait(rr);
+      if (n_iter > 0) {
+        tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
+        tmem_ld_wait(rr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept query tile: dV = 0
+      }
       if (kj < p.Lk) store_row32<BF16>(dst + c * 32, rr, 1.f);
     }
   }
@@ -859,7 +881,9 @@ struct DkvPairGeom {
   static constexpr int BQ = Dv::BQ, BK = Dv::BK;
 };
 
-template <int D, bool BF16, bool CAUSAL>
+// MASKED (D = 256 only): block-sparse variant; a key tile's CTA walks the
+// query tiles its mask column keeps and writes zeros if it keeps none.
+template <int D, bool BF16, bool CAUSAL, bool MASKED = false>
 __global__ void __launch_bounds__(DkvPairGeom<D>::NUM_THREADS, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -867,12 +891,12 @@ __global__ void __launch_bounds__(DkvPairGeom<D>::NUM_THREADS, 1)
   const int bhk = static_cast<int>(blockIdx.x >> 1), kt = static_cast<int>(blockIdx.y);
   if (blockIdx.x & 1) {
     if constexpr (D == 256)
-      dk256_tile<BF16, CAUSAL>(tmQ, tmV, tmdO, p, bhk, kt);
+      dk256_tile<BF16, CAUSAL, MASKED>(tmQ, tmV, tmdO, p, bhk, kt);
     else
       dkv_tile<D, BF16, CAUSAL, kDkvDkOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
   } else {
     if constexpr (D == 256)
-      dv256_tile<BF16, CAUSAL>(tmQ, tmdO, p, bhk, kt);
+      dv256_tile<BF16, CAUSAL, MASKED>(tmQ, tmdO, p, bhk, kt);
     else
       dkv_tile<D, BF16, CAUSAL, kDkvDvOnly>(tmQ, tmK, tmV, tmdO, p, bhk, kt);
   }

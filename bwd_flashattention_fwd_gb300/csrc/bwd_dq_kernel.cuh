@@ -30,6 +30,11 @@
 // CTA (x, y) covers key tiles [y*split_tiles, ...); it writes its fp32 share
 // of dS K per row, and a reduction kernel sums the shares and applies the
 // scale.  P uses the final lse, so the shares simply add.
+//
+// MASKED: block-sparse variant ("feat(attention): complete Flash Attention
+// VJP implementation", section "Sparse Block Masks": the dQ kernel skips the
+// key blocks whose mask entry is zero); a query tile with no kept key block
+// writes dQ = 0.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -63,7 +68,7 @@ struct DqGeom {
   static_assert(DP_COL + 2 * BK <= TMEM_COLS, "tensor memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool DECODE = false>
+template <int D, bool BF16, bool CAUSAL, bool DECODE = false, bool MASKED = false>
 __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -96,6 +101,11 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
   // key tiles [j0, j0 + n_kv) of this CTA
   const int j0 = DECODE ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
   const int n_kv = DECODE ? min((kv_end + BK - 1) / BK - j0, p.split_tiles) : (kv_end + BK - 1) / BK;
+  static_assert(!(MASKED && DECODE), "no block mask on the decode path");
+  static_assert(BQ == kMaskBlock && kMaskBlock % BK == 0, "query tile = mask block");
+  // key tile jt is computed (block mask), and the number of computed tiles (warp-collective)
+  auto keep = [&](int jt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt, jt * BK / kMaskBlock); };
+  const int nk = count_kept<MASKED>(keep, 0, n_kv);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -141,24 +151,26 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       tma_load_3d_w(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
       tma_load_3d_w(sdO + c * BQ * 128, &tmdO, smem_u32(&bar_q), c * 64, q0, bh);
     }
-    for (int j = 0; j < n_kv; ++j) {
+    auto kw = kept_walk<MASKED>(keep, n_kv);
+    int jt = kw.first(0);  // key tile of the j-th computed tile
+    for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
       const int ks = j % KST, vs = j % VST;
       if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 11);
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64,
-                      (j0 + j) * BK, zkv);
+                      (j0 + jt) * BK, zkv);
       if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 18);
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64,
-                      (j0 + j) * BK, zkv);
+                      (j0 + jt) * BK, zkv);
     }
-    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+    for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
       mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
-    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+    for (int j = (nk > VST ? nk - VST : 0); j < nk; ++j)
       mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == Gm::MMA_WARP) {
@@ -170,7 +182,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);  // V stage 0, K-major
     mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 12);
     __syncwarp();
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0; j < nk; ++j) {
       const int ks = j % KST, vs = j % VST, buf = j & 1;
       // the dQ MMA of key tile j-2 has read this buffer's dS
       if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 19);
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     // ---------------- dQ += dS K issuer ----------------
     constexpr uint32_t IDESC_DQ = make_idesc_f16(128, D, BF16, false, true);
     const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0; j < nk; ++j) {
       const int ks = j % KST, buf = j & 1;
       mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 10);
       mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 15);
@@ -233,12 +245,14 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
     const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
     const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
-    for (int j = 0; j < n_kv; ++j) {
+    auto kw = kept_walk<MASKED>(keep, n_kv);
+    int jt = kw.first(0);  // key tile of the j-th computed tile
+    for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
       const int buf = j & 1;
       mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 16);
       __syncwarp();
       tc_fence_after_sync();
-      const int k0 = (j0 + j) * BK;
+      const int k0 = (j0 + jt) * BK;
       const int kc0 = k0 + half * 32;  // first key of this thread's columns
       const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
       const uint32_t scol = tmem + lrow + Gm::S_COL + buf * BK + half * 32;
@@ -283,8 +297,13 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
 #pragma unroll 1
       for (int c = half; c < D / 32; c += 2) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
-        tmem_ld_wait(rr);
+        if (!MASKED || nk > 0) {  // the same for the whole CTA: tcgen05.ld is warp-collective
+          tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+          tmem_ld_wait(rr);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept key tile: dQ = 0
+        }
         if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
       }
     }

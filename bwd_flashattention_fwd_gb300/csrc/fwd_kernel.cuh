@@ -25,6 +25,12 @@
 // partial base-2 log-sum-exp in fp32; a combine kernel merges the splits
 // (the online-softmax merge of "When the Bottleneck Moved", section 3, applied
 // across CTAs).  A row may see no key of its split: its partial lse is -inf.
+//
+// MASKED: block-sparse variant ("feat(attention): complete Flash Attention
+// VJP implementation", section "Sparse Block Masks"): the query tile is one
+// 128-row mask block; key tiles whose mask block is zero are neither loaded
+// nor computed (found 32 at a time by a warp ballot), and a row that sees no
+// key gets O = 0 and lse = +inf.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -56,7 +62,7 @@ struct FwdGeom {
   static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool DECODE = false>
+template <int D, bool BF16, bool CAUSAL, bool DECODE = false, bool MASKED = false>
 __global__ void __launch_bounds__(192, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -86,6 +92,11 @@ __global__ void __launch_bounds__(192, 1)
   // key tiles [j0, j0 + n_kv) of this CTA
   const int j0 = DECODE ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
   const int n_kv = DECODE ? min((kv_end + BK - 1) / BK - j0, p.split_tiles) : (kv_end + BK - 1) / BK;
+  static_assert(!(MASKED && DECODE), "no block mask on the decode path");
+  static_assert(BQ == kMaskBlock && kMaskBlock % BK == 0, "query tile = mask block");
+  // key tile jt is computed (block mask), and the number of computed tiles (warp-collective)
+  auto keep = [&](int jt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt, jt * BK / kMaskBlock); };
+  const int nk = count_kept<MASKED>(keep, 0, n_kv);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
@@ -129,25 +140,27 @@ __global__ void __launch_bounds__(192, 1)
     for (int c = 0; c < NCH; ++c) tma_load_3d_w(sQ + c * BQ * 128, &tmQ, smem_u32(&bar_q), c * 64, q0, bh);
     RingPos<KST> kp;
     RingPos<VST> vp;
-    for (int j = 0; j < n_kv; ++j, kp.next(), vp.next()) {
+    auto kw = kept_walk<MASKED>(keep, n_kv);
+    int jt = kw.first(0);  // key tile of the j-th computed tile
+    for (int j = 0; j < nk; ++j, jt = kw.next(jt), kp.next(), vp.next()) {
       const int ks = kp.slot, vs = vp.slot;
       if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), kp.phase ^ 1u, g, kDevTimeoutBase + 1);
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, (j0 + j) * BK,
+        tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, (j0 + jt) * BK,
                       zkv);
       if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), vp.phase ^ 1u, g, kDevTimeoutBase + 9);
       __syncwarp();
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
-        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, (j0 + j) * BK,
+        tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, (j0 + jt) * BK,
                       zkv);
     }
     // Do not leave the CTA while a copy may still be landing.
-    for (int j = (n_kv > KST ? n_kv - KST : 0); j < n_kv; ++j)
+    for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
       mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
-    for (int j = (n_kv > VST ? n_kv - VST : 0); j < n_kv; ++j)
+    for (int j = (nk > VST ? nk - VST : 0); j < nk; ++j)
       mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
     __syncwarp();
   } else if (warp == 5) {
@@ -160,8 +173,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 2);
     __syncwarp();
     tc_fence_after_sync();
-    for (int j = 0; j <= n_kv; ++j) {
-      if (j < n_kv) {
+    for (int j = 0; j <= nk; ++j) {  // j: computed tiles so far
+      if (j < nk) {
         const int s = j % KST;
         mbar_wait(smem_u32(&bar_kfull[s]), (j / KST) & 1, g, kDevTimeoutBase + 3);
         __syncwarp();
@@ -204,7 +217,9 @@ __global__ void __launch_bounds__(192, 1)
     // last visible key of this row (inclusive)
     const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < n_kv; ++j) {
+    auto kw = kept_walk<MASKED>(keep, n_kv);
+    int jt = kw.first(0);  // key tile of the j-th computed tile
+    for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
       mbar_wait(smem_u32(&bar_sfull[j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 6);
       __syncwarp();
       tc_fence_after_sync();
@@ -218,7 +233,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]) * sl2;
       }
-      const int k0 = (j0 + j) * BK;
+      const int k0 = (j0 + jt) * BK;
       const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
       if (need_mask) {
 #pragma unroll
@@ -230,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int i = 1; i < BK; ++i) mt = fmaxf(mt, x[i]);
       const float m_new = fmaxf(m, mt);
       // (decode: a row that has seen no key of its split keeps m = -inf, P = 0)
-      const float mu = (DECODE && m_new == -INFINITY) ? 0.f : m_new;
+      const float mu = ((DECODE || MASKED) && m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - mu);
       float sum = 0.f;
       const uint32_t pcol = tmem + lrow + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(192, 1)
       m = m_new;
     }
     // ---------------- epilogue ----------------
-    mbar_wait(smem_u32(&bar_odone), (n_kv - 1) & 1, g, kDevTimeoutBase + 8);
+    if (nk > 0) mbar_wait(smem_u32(&bar_odone), (nk - 1) & 1, g, kDevTimeoutBase + 8);
     __syncwarp();
     tc_fence_after_sync();
     if constexpr (DECODE) {
@@ -287,16 +302,23 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (qi < p.Lq) p.ws_lse[x] = empty ? -INFINITY : m + log2f(l);
     } else {
-      const float inv_l = 1.f / l;
+      const bool empty = MASKED && !(l > 0.f);  // the row saw no key: O = 0, lse = +inf
+      const float inv_l = empty ? 0.f : 1.f / l;
       typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
-        tmem_ld_wait(rr);
+        if (!MASKED || nk > 0) {  // the same for the whole CTA: tcgen05.ld is warp-collective
+          tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
+          tmem_ld_wait(rr);
+        }
+        if (empty) {  // (also every row when no key tile is kept)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
         if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
       }
-      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = m + log2f(l);
+      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
     }
   }
 

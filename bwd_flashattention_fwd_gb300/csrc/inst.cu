@@ -112,7 +112,12 @@ int fwd_impl(const AttnArgs& a) {
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.limit_ns = a.limit_ns;
+  p.bmask = a.block_mask;
+  p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
   const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  if (a.block_mask)
+    return launch(attn_fwd_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
+                  tq, tk, tv, p);
   return launch(attn_fwd_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
                 tv, p);
   }
@@ -151,6 +156,9 @@ int dkv_impl(const AttnArgs& a) {
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
   const dim3 grid(2 * a.B * a.Hkv, p.n_ktiles);
+  if (a.block_mask && kD == 256)
+    return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL, kD == 256>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
+                  tq, tk, tv, tdo, p);
   return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk, tv,
                 tdo, p);
 }
@@ -214,6 +222,9 @@ int dq_impl(const AttnArgs& a) {
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
   const dim3 grid(a.B * a.Hq, p.n_qtiles);
+  if (a.block_mask)
+    return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
+                  a.stream, tq, tk, tv, tdo, p);
   return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
                 tv, tdo, p);
   }

@@ -126,9 +126,8 @@ attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const vo
  *   O = 0 and lse = +inf (the pages do not define this case); its dQ is 0 and
  *   it adds nothing to dK and dV.  Feed attn_bwd_masked the lse of
  *   attn_fwd_masked with the same mask; delta comes from attn_bwd_delta.
- *   D in {64, 96, 128}; D = 256 returns ATTN_ERR_UNSUPPORTED.  Other arguments
- *   and errors as for attn_fwd / attn_bwd; a null block_mask is
- *   ATTN_ERR_INVALID_ARG.
+ *   Every D of attn_fwd.  Other arguments and errors as for attn_fwd /
+ *   attn_bwd; a null block_mask is ATTN_ERR_INVALID_ARG.
  */
 attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
                               const uint8_t* block_mask, int B, int Hq, int Hkv, int Lq, int Lk, int D,
@@ -151,9 +150,8 @@ attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const
  *     j < Lk only: rows j >= Lk of the cache (stale entries) are never read,
  *     whatever they hold.  dk and dv are written contiguous [B,Hkv,Lk,D].
  *   Errors: kv_pitch < 0 or 0 < kv_pitch < Lk is ATTN_ERR_INVALID_ARG; a pitch
- *   of 2^40 bytes or more per head is ATTN_ERR_UNSUPPORTED; a block mask with
- *   D = 256 is ATTN_ERR_UNSUPPORTED.  Everything else as for attn_fwd /
- *   attn_bwd.  Pass attn_bwd_ex the lse of attn_fwd_ex with the same options.
+ *   of 2^40 bytes or more per head is ATTN_ERR_UNSUPPORTED.  Everything else
+ *   as for attn_fwd / attn_bwd.  Pass attn_bwd_ex the lse of attn_fwd_ex with the same options.
  */
 attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                           const uint8_t* block_mask, int64_t kv_pitch, int B, int Hq, int Hkv, int Lq,

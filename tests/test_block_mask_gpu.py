@@ -104,6 +104,10 @@ for D in (64, 96, 128):
     CASES.append((Workload(f"mask_d{D}_fp16_dense_l700", B=1, Hq=2, Hkv=2, Lq=700, Lk=700, D=D, dtype="fp16",
                            causal=False, seed=5100 + D), "random"))
 CASES += [
+    (Workload("mask_d256_bf16_causal_gqa_l700", B=1, Hq=4, Hkv=2, Lq=700, Lk=700, D=256, seed=5256), "random"),
+    (Workload("mask_d256_fp16_dense_q300_k520", B=1, Hq=2, Hkv=1, Lq=300, Lk=520, D=256, dtype="fp16",
+              causal=False, seed=5257), "random"),
+    (Workload("mask_d256_window_l1024_g8", B=1, Hq=8, Hkv=1, Lq=1024, Lk=1024, D=256, seed=5258), "window"),
     (Workload("mask_rect_causal_q300_k900_d128", B=2, Hq=4, Hkv=1, Lq=300, Lk=900, D=128, seed=5201), "window"),
     # With this seed every non-empty row sees only the 4-key tail block, so
     # each dS term is ~30x larger than with a full block and the 16-bit
@@ -133,8 +137,9 @@ def test_masked_chain_matches_oracle(w, kind):
     check_masked(w, bm)
 
 
-def test_all_ones_mask_matches_unmasked():
-    w = Workload("mask_ones_l600_d128", B=1, Hq=4, Hkv=2, Lq=600, Lk=600, D=128, seed=5300)
+@pytest.mark.parametrize("D", [128, 256])
+def test_all_ones_mask_matches_unmasked(D):
+    w = Workload(f"mask_ones_l600_d{D}", B=1, Hq=4, Hkv=2, Lq=600, Lk=600, D=D, seed=5300)
     q, k, v, do = make_inputs(w, "cuda")
     bm = torch.ones((-(-w.Lq // BLK), -(-w.Lk // BLK)), dtype=torch.uint8, device="cuda")
     om, lm, dqm, dkm, dvm = masked_chain(w, q, k, v, do, bm)
@@ -156,13 +161,8 @@ def test_all_zero_mask_gives_zeros():
         assert torch.count_nonzero(t) == 0, n
 
 
-def test_masked_rejects_d256_and_null_mask():
-    w = Workload("mask_d256", B=1, Hq=1, Hkv=1, Lq=128, Lk=128, D=256, seed=5302)
-    q, k, v, do = make_inputs(w, "cuda")
-    o, lse = torch.empty_like(q), torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
-    bm = torch.ones((1, 1), dtype=torch.uint8, device="cuda")
-    assert gbattn.attn_fwd_masked(q, k, v, o, lse, bm, w.scale, True, check=False) == gbattn.ATTN_ERR_UNSUPPORTED
+def test_masked_rejects_null_mask():
     w2 = Workload("mask_null", B=1, Hq=1, Hkv=1, Lq=128, Lk=128, D=64, seed=5303)
     q, k, v, do = make_inputs(w2, "cuda")
-    o = torch.empty_like(q)
+    o, lse = torch.empty_like(q), torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
     assert gbattn.attn_fwd_masked(q, k, v, o, lse, None, w2.scale, True, check=False) == gbattn.ATTN_ERR_INVALID_ARG
