@@ -143,24 +143,25 @@ BwdParams bwd_params(const AttnArgs& a) {
   return p;
 }
 
-// D = 256: the dV and dK halves in one launch (bwd_dkv_kernel.cuh).
-template <bool BF16, bool CAUSAL>
-int dkv_impl(const AttnArgs& a) {
-  using Gm = DkvPairGeom<kD>;
-  CUtensorMap tq, tk, tv, tdo;
+// D = 256: the dV and dK halves in one launch (bwd_dkv_kernel.cuh).  A
+// template of its own so that only the D = 256 unit instantiates the kernel.
+template <int DD, bool BF16, bool CAUSAL>
+int dkv256_impl(const AttnArgs& a) {
+  static_assert(DD == 256, "the pair kernel is the D = 256 dK/dV path");
+  using Gm = DkvPairGeom;
+  CUtensorMap tq, tv, tdo;
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
       !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
   const dim3 grid(2 * a.B * a.Hkv, p.n_ktiles);
-  if (a.block_mask && kD == 256)
-    return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL, kD == 256>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
-                  tq, tk, tv, tdo, p);
-  return launch(attn_bwd_dkv_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk, tv,
-                tdo, p);
+  auto kern = a.block_mask ? attn_bwd_dkv_kernel<BF16, CAUSAL, true> : attn_bwd_dkv_kernel<BF16, CAUSAL, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+    return kLaunchCudaError;
+  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
 // D <= 128: K held in tensor memory as the A operand of S^T (bwd_dkv2_kernel.cuh).
@@ -235,7 +236,7 @@ int dkv_all(const AttnArgs& a) {
   if constexpr (kD <= 128) {
     return a.block_mask ? dkv2_impl<BF16, CAUSAL, true>(a) : dkv2_impl<BF16, CAUSAL, false>(a);
   } else {
-    return dkv_impl<BF16, CAUSAL>(a);
+    return dkv256_impl<kD, BF16, CAUSAL>(a);
   }
 }
 
