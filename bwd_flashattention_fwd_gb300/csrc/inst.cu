@@ -97,29 +97,29 @@ int fwd_impl(const AttnArgs& a) {
   if constexpr (kD <= 128) {
     return a.block_mask ? fwd2_impl<BF16, CAUSAL, true>(a) : fwd2_impl<BF16, CAUSAL, false>(a);
   } else {
-  using Gm = FwdGeom<kD>;
-  CUtensorMap tq, tk, tv;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
-    return kLaunchBadMap;
-  FwdParams p{};
-  p.o = a.o_out;
-  p.lse = a.lse_out;
-  p.status = a.status;
-  p.B = a.B, p.Hq = a.Hq, p.Hkv = a.Hkv, p.Lq = a.Lq, p.Lk = a.Lk, p.G = a.Hq / a.Hkv;
-  p.off = a.Lk - a.Lq;
-  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
-  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
-  p.limit_ns = a.limit_ns;
-  p.bmask = a.block_mask;
-  p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
-  const dim3 grid(a.B * a.Hq, p.n_qtiles);
-  if (a.block_mask)
-    return launch(attn_fwd_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
-                  tq, tk, tv, p);
-  return launch(attn_fwd_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
-                tv, p);
+    using Gm = FwdGeom<kD>;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) ||
+        !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+        !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      return kLaunchBadMap;
+    FwdParams p{};
+    p.o = a.o_out;
+    p.lse = a.lse_out;
+    p.status = a.status;
+    p.B = a.B, p.Hq = a.Hq, p.Hkv = a.Hkv, p.Lq = a.Lq, p.Lk = a.Lk, p.G = a.Hq / a.Hkv;
+    p.off = a.Lk - a.Lq;
+    p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+    p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+    p.limit_ns = a.limit_ns;
+    p.bmask = a.block_mask;
+    p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
+    const dim3 grid(a.B * a.Hq, p.n_qtiles);
+    if (a.block_mask)
+      return launch(attn_fwd_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
+                    tq, tk, tv, p);
+    return launch(attn_fwd_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
+                  tv, p);
   }
 }
 
@@ -213,21 +213,21 @@ int dq_impl(const AttnArgs& a) {
   if constexpr (kD <= 128) {
     return a.block_mask ? dq3_impl<BF16, CAUSAL, true>(a) : dq3_impl<BF16, CAUSAL, false>(a);
   } else {
-  using Gm = DqGeom<kD>;
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
-    return kLaunchBadMap;
-  BwdParams p = bwd_params(a);
-  p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
-  p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
-  const dim3 grid(a.B * a.Hq, p.n_qtiles);
-  if (a.block_mask)
-    return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
-                  a.stream, tq, tk, tv, tdo, p);
-  return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
-                tv, tdo, p);
+    using Gm = DqGeom<kD>;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
+        !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+        !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      return kLaunchBadMap;
+    BwdParams p = bwd_params(a);
+    p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
+    p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
+    const dim3 grid(a.B * a.Hq, p.n_qtiles);
+    if (a.block_mask)
+      return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
+                    a.stream, tq, tk, tv, tdo, p);
+    return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
+                  tv, tdo, p);
   }
 }
 
