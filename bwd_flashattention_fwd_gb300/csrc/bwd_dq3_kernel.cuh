@@ -324,6 +324,52 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     constexpr int HALF = D / 2;  // elements of a Q / dO row this thread copies
     uint32_t sphase = 0;  // parity of the S buffer's next fill
     RingPos<NDP> db;      // dP buffer of the next key tile
+    // Q and dO rows of the item of round rn from the prefetch buffer (TMA
+    // layout: 64-column chunks of 128-byte rows, 16-byte units swizzled by
+    // row % 8; zeros past Lq and past D) into tensor memory: this warp copies
+    // elements [half*D/2, (half+1)*D/2) of its 32 rows as 16-bit pairs.  No
+    // MMA of the previous item reads them any more (its final commit has
+    // completed).
+    auto copy_q = [&](int rn) {
+      mbar_wait(smem_u32(&bar_qbfull), rn & 1, g, kDevTimeoutBase + 73);
+      uint32_t qa[HALF / 2], oa[HALF / 2];
+#pragma unroll
+      for (int v = 0; v < HALF / 8; ++v) {
+        const int e = half * HALF + 8 * v;  // first element of this 16-byte unit
+        const uint32_t off = (e / 64) * (BQ * 128) + rr_ * 128 + ((((e % 64) / 8) ^ (rr_ & 7)) * 16);
+        const uint4 x = ld_shared_v4(sQb + off), y = ld_shared_v4(sDOb + off);
+        qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
+        oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
+      }
+      // the producer may refill the buffer once every row thread has read it
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bar_qbfree));
+      // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
+#pragma unroll
+      for (int c = 0; c + 16 <= HALF / 2; c += 16) {
+        uint32_t t16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t16[i] = qa[c + i];
+        tmem_st16(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t16);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t16[i] = oa[c + i];
+        tmem_st16(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t16);
+      }
+      if constexpr ((HALF / 2) % 16 == 8) {
+        constexpr int c = HALF / 2 - 8;
+        uint32_t t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = qa[c + i];
+        tmem_st8(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = oa[c + i];
+        tmem_st8(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t8);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_qready));
+    };
+    if (dq3_round_item(0, n_items) >= 0) copy_q(0);
     for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
       const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
       const int q0 = it.qt * BQ;
@@ -331,51 +377,6 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       const int n_kv = n_kv_of(it.qt);
       const int nk = n_kept(it.qt);
       const size_t row = static_cast<size_t>(it.bh) * p.Lq + qi;
-      // Q and dO rows from the prefetch buffer (TMA layout: 64-column chunks
-      // of 128-byte rows, 16-byte units swizzled by row % 8; zeros past Lq
-      // and past D) into tensor memory: this warp copies elements
-      // [half*D/2, (half+1)*D/2) of its 32 rows as 16-bit pairs.  The
-      // previous item's MMAs are complete: its dQ was read out after the
-      // item's final commit.
-      mbar_wait(smem_u32(&bar_qbfull), r & 1, g, kDevTimeoutBase + 73);
-      {
-        uint32_t qa[HALF / 2], oa[HALF / 2];
-#pragma unroll
-        for (int v = 0; v < HALF / 8; ++v) {
-          const int e = half * HALF + 8 * v;  // first element of this 16-byte unit
-          const uint32_t off = (e / 64) * (BQ * 128) + rr_ * 128 + ((((e % 64) / 8) ^ (rr_ & 7)) * 16);
-          const uint4 x = ld_shared_v4(sQb + off), y = ld_shared_v4(sDOb + off);
-          qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
-          oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
-        }
-        // the producer may refill the buffer once every row thread has read it
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&bar_qbfree));
-        // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
-#pragma unroll
-        for (int c = 0; c + 16 <= HALF / 2; c += 16) {
-          uint32_t t16[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) t16[i] = qa[c + i];
-          tmem_st16(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t16);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) t16[i] = oa[c + i];
-          tmem_st16(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t16);
-        }
-        if constexpr ((HALF / 2) % 16 == 8) {
-          constexpr int c = HALF / 2 - 8;
-          uint32_t t8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) t8[i] = qa[c + i];
-          tmem_st8(tmem + lrow + Gm::Q_COL + half * (HALF / 2) + c, t8);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) t8[i] = oa[c + i];
-          tmem_st8(tmem + lrow + Gm::DO_COL + half * (HALF / 2) + c, t8);
-        }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(smem_u32(&bar_qready));
-      }
       const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
       const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
       const uint64_t nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
@@ -441,6 +442,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       mbar_wait(smem_u32(&bar_dqdone), r & 1, g, kDevTimeoutBase + 70);
       __syncwarp();
       tc_fence_after_sync();
+      // the next item's Q and dO first, so that its first S and dP products
+      // run while this item's dQ is read out and stored
+      if (dq3_round_item(r + 1, n_items) >= 0) copy_q(r + 1);
       typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
 #pragma unroll 1
       for (int c = half; c < D / 32; c += 2) {
