@@ -39,11 +39,6 @@
 // are neither loaded nor computed, and every warp walks the same list of kept
 // tiles.  A key tile with no kept query tile writes dK = dV = 0.
 //
-// DECODE (short query lengths): the G query heads x Lq rows of the KV head
-// form the query tiles (packed row r is query r % Lq), so one or two tiles
-// replace G loops over a mostly empty tile; every packed tile may hold rows
-// that see the CTA's keys, and the causal test uses each column's true query
-// index.
 #pragma once
 
 #include <type_traits>
@@ -90,7 +85,7 @@ struct Dkv2Geom {
   static_assert(POLY_Q1 >= 0 && POLY_Q1 <= 16 && POLY_Q2 >= 0 && POLY_Q2 <= 16, "polynomial share");
 };
 
-template <int D, bool BF16, bool CAUSAL, bool MASKED, bool DECODE = false>
+template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     attn_bwd_dkv2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO, const void* __restrict__ k, const BwdParams p) {
@@ -116,7 +111,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int kt = blockIdx.y;
   const int k0 = kt * BK;
-  const int qt_start = (CAUSAL && !DECODE) ? max(0, k0 - p.off) / BQ : 0;
+  const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
   static_assert(BK == kMaskBlock && 2 * BQ == kMaskBlock, "key tile = mask block, query tile = half a block");
   // query tile qt is computed (block mask)
   auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
@@ -322,8 +317,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 90);
       __syncwarp();
       tc_fence_after_sync();
-      // (decode: every packed tile holds query index 0)
-      const bool need_mask = CAUSAL && ((DECODE ? 0 : q0) < k0 + BK - 1 - p.off);
+      const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
       const uint32_t dcol = tmem + lrow + Gm::DPT_COL + buf * BQ + half * 32;
       uint32_t sr[32], dr[32];
       tmem_ld32(tmem + lrow + Gm::ST_COL + half * 32, sr);
@@ -336,13 +330,6 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       const uint64_t* nlse_row = reinterpret_cast<const uint64_t*>(&nlse_s[s][half * 32]);
       const uint64_t* dlt_row = reinterpret_cast<const uint64_t*>(&dlt_s[s][half * 32]);
       const int qc0 = q0 + half * 32;
-      // decode: bit c set when column qc0 + c (query (qc0 + c) % Lq) sees key kj
-      uint32_t vis = 0xffffffffu;
-      if (DECODE && need_mask) {
-        vis = 0u;
-        for (int c = 0, qq = qc0 % p.qmod; c < 32; ++c, qq = (qq + 1 == p.qmod) ? 0 : qq + 1)
-          vis |= (qq >= qmin ? 1u : 0u) << c;
-      }
       uint32_t pk[16], dk[16];
       // NPOLY of the 16 pairs, spread evenly, use the polynomial
       auto pds_tile = [&](auto npoly_tag) {
@@ -360,13 +347,8 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
             p1 = ex2_approx(x1);
           }
           if (need_mask) {
-            if (DECODE) {
-              if (!((vis >> c0) & 1u)) p0 = 0.f;
-              if (!((vis >> (c0 + 1)) & 1u)) p1 = 0.f;
-            } else {
-              if (qc0 + c0 < qmin) p0 = 0.f;
-              if (qc0 + c0 + 1 < qmin) p1 = 0.f;
-            }
+            if (qc0 + c0 < qmin) p0 = 0.f;
+            if (qc0 + c0 + 1 < qmin) p1 = 0.f;
           }
           pk[i] = E::pack(p0, p1);
           const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[c0]), __uint_as_float(dr[c0 + 1])), dlt_row[i]);

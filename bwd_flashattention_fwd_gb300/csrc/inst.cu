@@ -315,28 +315,31 @@ int dq_decode_impl(const AttnArgs& a) {
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
-// Decode-shaped dK/dV: D <= 128 runs the dK/dV kernel on packed query tiles
-// (G * Lq rows of one KV head); D = 256 the general pair of kernels.
+// Decode-shaped dK/dV: D <= 128 streams each KV head's key tiles against its
+// one packed query tile (decode_kernel.cuh); D = 256 runs the general pair.
 template <bool BF16, bool CAUSAL>
 int dkv_decode_impl(const AttnArgs& a) {
   if constexpr (kD <= 128) {
     constexpr int DD = kD <= 128 ? kD : 128;  // (this branch is compiled for every D)
-    using Gm = Dkv2Geom<DD>;
+    using Gm = DecodeDkvGeom<DD>;
     const int R = (a.Hq / a.Hkv) * a.Lq;
-    CUtensorMap tq, tv, tdo;
-    if (!make_map(a, &tq, a.q, R, a.B * a.Hkv, Gm::BQ) || !make_map(a, &tdo, a.dO, R, a.B * a.Hkv, Gm::BQ) ||
+    const long long groups = static_cast<long long>(a.B) * a.Hkv;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(a, &tq, a.q, R, a.B * a.Hkv, Gm::RQ) || !make_map(a, &tdo, a.dO, R, a.B * a.Hkv, Gm::RQ) ||
+        !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
         !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
       return kLaunchBadMap;
     BwdParams p = bwd_params(a);  // off = Lk - Lq from the true query length
     p.Hq = a.Hkv, p.Lq = R, p.G = 1;
     p.qmod = a.Lq;
-    p.n_qtiles = (R + Gm::BQ - 1) / Gm::BQ;
     p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
-    const dim3 grid(a.B * a.Hkv, p.n_ktiles);
-    auto kern = attn_bwd_dkv2_kernel<DD, BF16, CAUSAL, false, true>;
+    const DecodeSplit sp = decode_split(groups, p.n_ktiles);
+    p.split_tiles = sp.tiles_per_split;
+    const dim3 grid(static_cast<unsigned>(groups), sp.n_split);
+    auto kern = attn_decode_dkv_kernel<DD, BF16, CAUSAL>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
       return kLaunchCudaError;
-    kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, a.k, p);
+    kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, p);
     return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
   } else {
     return dkv_all<BF16, CAUSAL>(a);
