@@ -140,6 +140,7 @@ BwdParams bwd_params(const AttnArgs& a) {
   p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
   p.kv_pitch = a.kv_pitch > 0 ? a.kv_pitch : a.Lk;
   p.k = a.k;
+  p.v = a.v;
   return p;
 }
 
@@ -149,18 +150,17 @@ template <int DD, bool BF16, bool CAUSAL>
 int dkv256_impl(const AttnArgs& a) {
   static_assert(DD == 256, "the pair kernel is the D = 256 dK/dV path");
   using Gm = DkvPairGeom;
-  CUtensorMap tq, tv, tdo;
-  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+  CUtensorMap tq, tdo;
+  if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
   p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
-  const dim3 grid(2 * a.B * a.Hkv, p.n_ktiles);
+  const dim3 grid(2 * a.B * a.Hkv, p.n_ktiles);  // x: the two CTAs of a cluster
   auto kern = a.block_mask ? attn_bwd_dkv_kernel<BF16, CAUSAL, true> : attn_bwd_dkv_kernel<BF16, CAUSAL, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
     return kLaunchCudaError;
-  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, p);
+  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tdo, p);
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 

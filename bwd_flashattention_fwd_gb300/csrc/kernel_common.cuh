@@ -60,6 +60,7 @@ struct BwdParams {
   int nkb;  // ceil(Lk / 128): row length of the mask
   int64_t kv_pitch;  // rows between consecutive heads of k and v (>= Lk)
   const void* k;     // K itself, for kernels that copy K rows into tensor memory
+  const void* v;     // V itself, likewise
   // decode variant of the dQ kernel (as in FwdParams): fp32 partial dQ rows
   int qmod, split_tiles;
   float* ws;
