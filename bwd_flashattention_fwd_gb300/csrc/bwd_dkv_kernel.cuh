@@ -48,8 +48,10 @@ struct PtXch {
 // mbarriers of the hand-off, in the shared memory of both CTAs (the kernel
 // declares them, so they sit at the same offset in either CTA).  pfull, in
 // the dK CTA: one local arrival that expects the slot's bytes, which the dV
-// CTA's asynchronous stores complete.  pfree, in the dV CTA: one arrival per
-// warp of the dK CTA's row threads once they hold the slot's values.
+// CTA's asynchronous stores complete (the bytes are visible to a thread that
+// sees the phase complete, as for a TMA load).  pfree, in the dV CTA: one
+// arrival per warp of the dK CTA's row threads once they have used the
+// slot's values.
 struct PtXchBars {
   uint64_t pfull[PtXch::SLOTS], pfree[PtXch::SLOTS];
 };
@@ -145,6 +147,18 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     RingPos<ST> st;
     auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
     int gi = 0, qtile = qw.first(qt_start);  // query head in the group and query tile of iteration it
+    // the per-query values of an iteration are loaded one iteration ahead, so
+    // their latency overlaps the wait for a free stage
+    float pre[BQ / 32];
+    auto load_pre = [&]() {
+      const int zq = b * p.Hq + hk * p.G + gi;
+#pragma unroll
+      for (int t = 0; t < BQ / 32; ++t) {
+        const int qi = qtile * BQ + lane + 32 * t;
+        pre[t] = qi < p.Lq ? p.delta[static_cast<size_t>(zq) * p.Lq + qi] : 0.f;
+      }
+    };
+    if (n_iter > 0) load_pre();
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 111);
@@ -157,14 +171,11 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
         tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
       }
 #pragma unroll
-      for (int t = 0; t < BQ / 32; ++t) {
-        const int c = lane + 32 * t;
-        const int qi = q0 + c;
-        dlt_s[s][c] = qi < p.Lq ? p.delta[static_cast<size_t>(zq) * p.Lq + qi] : 0.f;
-      }
+      for (int t = 0; t < BQ / 32; ++t) dlt_s[s][lane + 32 * t] = pre[t];
       mbar_arrive(smem_u32(&bar_stfull[s]));
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
+      if (it + 1 < n_iter) load_pre();
     }
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
       mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
@@ -252,7 +263,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       uint32_t dr[32];
       tmem_ld32(dcol, dr);
       // P^T(it) from the dV CTA: 32 queries (four chunks) of this thread's key row
-      mbar_wait_cluster(smem_u32(&xb.pfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 117);
+      mbar_wait(smem_u32(&xb.pfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 117);
       // the slot's next use (query tile it + 2) expects its bytes: the dV CTA
       // cannot write them before every warp here has released this use
       if (threadIdx.x == 0 && it + 2 < n_iter && !abort_flag) mbar_arrive_expect_tx(smem_u32(&xb.pfull[buf]), PtXch::SLOT_BYTES);
@@ -394,6 +405,18 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     RingPos<ST> st;
     auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
     int gi = 0, qtile = qw.first(qt_start);
+    // the per-query values of an iteration are loaded one iteration ahead, so
+    // their latency overlaps the wait for a free stage
+    float pre[BQ / 32];
+    auto load_pre = [&]() {
+      const int zq = b * p.Hq + hk * p.G + gi;
+#pragma unroll
+      for (int t = 0; t < BQ / 32; ++t) {
+        const int qi = qtile * BQ + lane + 32 * t;
+        pre[t] = qi < p.Lq ? -p.lse[static_cast<size_t>(zq) * p.Lq + qi] : -INFINITY;
+      }
+    };
+    if (n_iter > 0) load_pre();
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 131);
@@ -406,14 +429,11 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
         tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
       }
 #pragma unroll
-      for (int t = 0; t < BQ / 32; ++t) {
-        const int c = lane + 32 * t;
-        const int qi = q0 + c;
-        nlse_s[s][c] = qi < p.Lq ? -p.lse[static_cast<size_t>(zq) * p.Lq + qi] : -INFINITY;
-      }
+      for (int t = 0; t < BQ / 32; ++t) nlse_s[s][lane + 32 * t] = pre[t];
       mbar_arrive(smem_u32(&bar_stfull[s]));
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
+      if (it + 1 < n_iter) load_pre();
     }
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
       mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
@@ -522,8 +542,8 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       }
       tmem_st16(scol, pk);
       // P^T(it) to the dK CTA: four 16-byte chunks of this thread's key row,
-      // once that CTA has read the slot's previous contents
-      if (it >= 2) mbar_wait_cluster(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, kDevTimeoutBase + 138);
+      // once that CTA has used the slot's previous contents
+      if (it >= 2) mbar_wait(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, kDevTimeoutBase + 138);
       const uint32_t full1 = cluster_map(smem_u32(&xb.pfull[buf]), 1);
 #pragma unroll
       for (int v = 0; v < 4; ++v)

@@ -119,10 +119,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t local_addr, uint32_t ra
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
 // Asynchronous 16-byte store into another CTA's shared memory; its bytes
 // count against the transaction count of `cluster_bar` (an mbarrier of that
 // CTA) when they land.
@@ -132,44 +128,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
                : "memory");
 }
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier memory accesses at cluster scope.
+// Arrive on an mbarrier of another CTA of the cluster with the default
+// (CTA-scope) semantics: for a "buffer free" signal sent after the values read
+// from the buffer have been used, so nothing is left to order.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-// Bounded wait on a local mbarrier whose arrivals come from the partner CTA
-// (acquire at cluster scope, so its writes to this CTA's shared memory are
-// visible); same abort rules as mbar_wait.
-static __device__ __noinline__ void mbar_wait_cluster_slow(uint32_t bar, uint32_t parity, const WaitGuard& g,
-                                                    int code) {
-  const uint64_t t0 = global_timer_ns();
-  uint32_t it = 0;
-  while (true) {
-    if (*g.abort_flag) return;
-    if (mbar_try_wait_cluster(bar, parity)) return;
-    if ((++it & 63u) == 0u) {
-      if (global_timer_ns() - t0 > g.limit_ns) {
-        if (g.status) atomicCAS(g.status, 0, code);
-        *g.abort_flag = 1;
-        return;
-      }
-    }
-  }
-}
-__device__ __forceinline__ void mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitGuard& g, int code) {
-  if (mbar_try_wait_cluster(bar, parity)) return;
-  mbar_wait_cluster_slow(bar, parity, g, code);
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // ---------------------------------------------------------------------------
