@@ -56,21 +56,30 @@ struct PtXchBars {
   uint64_t pfull[PtXch::SLOTS], pfree[PtXch::SLOTS];
 };
 
+// Q and dO tiles of 64 queries x 256 columns (four 64-column chunks, 32 KB)
+// sit in two rings of their own, each slot freed by the MMA that last reads
+// it: the slot a tile is loaded into is then free one or two query tiles
+// before that tile is needed, which covers the TMA's latency.  The per-query
+// lse / delta values are loaded by the row threads themselves (one value per
+// lane, a query tile ahead) and spread with shuffles.
+__device__ __forceinline__ void load_tile256(uint32_t dst, const CUtensorMap* map, uint32_t bar, int q0, int zq) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tma_load_3d_w(dst + c * 64 * 128, map, bar, c * 64, q0, zq);
+}
+
 // D = 256, dK half (cluster rank 1).  V sits in tensor memory as the A
-// operand of dP^T = V dO^T (copied in by the row threads), so only the
-// dO^T tile is read from shared memory; P^T comes from the partner CTA.
-// Tensor memory: dK (256 columns), V (128: 256 16-bit values per row), dP^T
-// (two buffers of 64).  The row threads write dS^T (16-bit pairs) over the
-// dP^T columns they have read, and the MMA warp issues dK += dS^T Q, then
-// dP^T of the tile after next into the same buffer (tcgen05 MMAs of one
-// thread run in issue order).
+// operand of dP^T = V dO^T (copied in by the row threads), so only the dO
+// tile is read from shared memory; P^T comes from the partner CTA.  Tensor
+// memory: dK (256 columns), V (128: 256 16-bit values per row), dP^T (two
+// buffers of 64).  The row threads write dS^T (16-bit pairs) over the dP^T
+// columns they have read, and the MMA warp issues dK += dS^T Q, then dP^T of
+// the tile after next into the same buffer (tcgen05 MMAs of one thread run
+// in issue order).
 struct Dk256Geom {
   static constexpr int D = 256, BK = 128, BQ = 64, NCH = 4;
-  static constexpr int Q_BYTES = NCH * BQ * 128;  // 32 KB
-  static constexpr int STATIC_EST = 2048;         // static shared memory of the pair kernel, upper estimate
-  static constexpr int STAGES_FIT = (kMaxDynSmem - STATIC_EST - 1024 - PtXch::BYTES) / (2 * Q_BYTES);
-  static constexpr int STAGES = STAGES_FIT > 3 ? 3 : STAGES_FIT;
-  static constexpr int XCH_OFF = STAGES * 2 * Q_BYTES;  // from the 1024-aligned base
+  static constexpr int Q_BYTES = NCH * BQ * 128;  // one Q or dO tile, 32 KB
+  static constexpr int NQ = 3, NO = 3;            // Q and dO ring slots
+  static constexpr int XCH_OFF = (NQ + NO) * Q_BYTES;  // from the 1024-aligned base
   static constexpr int SMEM_BYTES = 1024 + XCH_OFF + PtXch::BYTES;
   static constexpr int DK_COL = 0, V_COL = 256, DPT_COL = 384;  // dP^T: 2 x 64
   static constexpr int TMEM_COLS = 512;
@@ -79,7 +88,8 @@ struct Dk256Geom {
   static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
   static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
-  static_assert(STAGES >= 3, "three Q/dO stages: dP^T runs two query tiles ahead");
+  static_assert(SMEM_BYTES + 1024 <= kMaxDynSmem, "shared memory budget (1 KB left for static variables)");
+  static_assert(NO >= 3, "dP^T runs two query tiles ahead of dK");
   static_assert(DPT_COL + 2 * BQ <= TMEM_COLS, "tensor memory budget");
 };
 
@@ -88,18 +98,18 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
                                            const int bhk, const int kt, PtXchBars& xb) {
   using Gm = Dk256Geom;
   using E = Elem<BF16>;
-  constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
+  constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NQ = Gm::NQ, NO = Gm::NO, NCT = Gm::NCT;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_vready, bar_stfull[ST], bar_stempty[ST], bar_dpfull[2], bar_dsready[2], bar_accdone;
-  __shared__ __align__(16) float dlt_s[ST][BQ];
+  __shared__ uint64_t bar_vready, bar_qfull[NQ], bar_qempty[NQ], bar_ofull[NO], bar_oempty[NO], bar_dpfull[2],
+      bar_dsready[2], bar_accdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ0 = sbase;
-  const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
+  const uint32_t sdO0 = sQ0 + NQ * Gm::Q_BYTES;
   const uint32_t sX = sbase + Gm::XCH_OFF;
 
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
@@ -114,9 +124,13 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_vready), NCT);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(smem_u32(&bar_stfull[s]), 33);  // TMA expect_tx arrive + 32 producer lanes
-      mbar_init(smem_u32(&bar_stempty[s]), 1);  // the MMA warp's last read of the stage (dK)
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(smem_u32(&bar_qfull[s]), 1);   // TMA expect_tx arrive
+      mbar_init(smem_u32(&bar_qempty[s]), 1);  // dK's commit
+    }
+    for (int s = 0; s < NO; ++s) {
+      mbar_init(smem_u32(&bar_ofull[s]), 1);
+      mbar_init(smem_u32(&bar_oempty[s]), 1);  // dP^T's commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_dpfull[i]), 1);
@@ -136,6 +150,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
   cluster_sync_all();  // both CTAs' mbarriers are initialised before any remote arrival
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
 
   if (warp == Gm::PRODUCER_WARP) {
     // ---------------- producer (whole warp) ----------------
@@ -144,69 +159,73 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       tma_prefetch_desc(&tmdO);
     }
     __syncwarp();
-    RingPos<ST> st;
-    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
-    int gi = 0, qtile = qw.first(qt_start);  // query head in the group and query tile of iteration it
-    // the per-query values of an iteration are loaded one iteration ahead, so
-    // their latency overlaps the wait for a free stage
-    float pre[BQ / 32];
-    auto load_pre = [&]() {
-      const int zq = b * p.Hq + hk * p.G + gi;
-#pragma unroll
-      for (int t = 0; t < BQ / 32; ++t) {
-        const int qi = qtile * BQ + lane + 32 * t;
-        pre[t] = qi < p.Lq ? p.delta[static_cast<size_t>(zq) * p.Lq + qi] : 0.f;
-      }
-    };
-    if (n_iter > 0) load_pre();
-    for (int it = 0; it < n_iter; ++it, st.next()) {
-      const int s = st.slot;
-      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 111);
+    RingPos<NQ> rq;
+    RingPos<NO> ro;
+    // the Q and dO loads walk the (head, query tile) list separately: a
+    // walker carries state under a mask
+    auto wq = qw, wo = qw;
+    int gq = 0, tq = wq.first(qt_start);  // query head in the group and query tile of the next Q load
+    int go = 0, to = wo.first(qt_start);  // and of the next dO load
+    auto load_q = [&](int i) {
+      if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, kDevTimeoutBase + 111);
       __syncwarp();
-      const int q0 = qtile * BQ;
-      const int zq = b * p.Hq + hk * p.G + gi;
-      mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d_w(sQ0 + s * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
-        tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
-      }
-#pragma unroll
-      for (int t = 0; t < BQ / 32; ++t) dlt_s[s][lane + 32 * t] = pre[t];
-      mbar_arrive(smem_u32(&bar_stfull[s]));
-      qtile = qw.next(qtile);
-      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
-      if (it + 1 < n_iter) load_pre();
+      const uint32_t bar = smem_u32(&bar_qfull[rq.slot]);
+      mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
+      load_tile256(sQ0 + rq.slot * Gm::Q_BYTES, &tmQ, bar, tq * BQ, b * p.Hq + hk * p.G + gq);
+      rq.next();
+      tq = wq.next(tq);
+      if (tq >= p.n_qtiles) tq = wq.first(qt_start), ++gq;
+    };
+    auto load_o = [&](int i) {
+      if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, kDevTimeoutBase + 119);
+      __syncwarp();
+      const uint32_t bar = smem_u32(&bar_ofull[ro.slot]);
+      mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
+      load_tile256(sdO0 + ro.slot * Gm::Q_BYTES, &tmdO, bar, to * BQ, b * p.Hq + hk * p.G + go);
+      ro.next();
+      to = wo.next(to);
+      if (to >= p.n_qtiles) to = wo.first(qt_start), ++go;
+    };
+    // in the order the MMA warp needs them: dO runs two query tiles ahead of Q
+    for (int i = 0; i < 2 && i < n_iter; ++i) load_o(i);
+    for (int it = 0; it < n_iter; ++it) {
+      load_q(it);
+      if (it + 2 < n_iter) load_o(it + 2);
     }
-    for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
-      mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
+    for (int i = (n_iter > NQ ? n_iter - NQ : 0); i < n_iter; ++i)
+      mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1, p.limit_ns);
+    for (int i = (n_iter > NO ? n_iter - NO : 0); i < n_iter; ++i)
+      mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1, p.limit_ns);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t IDESC_DP = make_idesc_f16(128, BQ, BF16, false, false);
     constexpr uint32_t IDESC_ACC = make_idesc_f16(128, D, BF16, false, true);
-    const uint64_t dOk = make_sdesc_sw128(sdO0, 16, 1024);       // dO stage 0, K-major
-    const uint64_t dQm = make_sdesc_sw128(sQ0, BQ * 128, 1024);  // Q stage 0, MN-major
-    RingPos<ST> st, st_d;  // stages of the next dK and of the next dP^T
+    const uint64_t dOk = make_sdesc_sw128(sdO0, 16, 1024);       // dO slot 0, K-major
+    const uint64_t dQm = make_sdesc_sw128(sQ0, BQ * 128, 1024);  // Q slot 0, MN-major
+    RingPos<NQ> rq;
+    RingPos<NO> ro;
     // dP^T(it) = V dO^T into buffer it & 1 (V from tensor memory)
     auto issue_dp = [&](int it) {
-      const int s = st_d.slot;
-      mbar_wait(smem_u32(&bar_stfull[s]), st_d.phase, g, kDevTimeoutBase + 113);
+      mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, kDevTimeoutBase + 113);
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qo = s * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t qo = ro.slot * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
         mma_ts_w(tmem + Gm::DPT_COL + (it & 1) * BQ, tmem + Gm::V_COL + kk * 8, sdesc_add(dOk, qo), IDESC_DP,
                  kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_dpfull[it & 1]));
-      st_d.next();
+      mma_commit_w(smem_u32(&bar_oempty[ro.slot]));
+      ro.next();
     };
     mbar_wait(smem_u32(&bar_vready), 0, g, kDevTimeoutBase + 112);
     for (int it = 0; it < 2 && it < n_iter; ++it) issue_dp(it);
-    for (int it = 0; it < n_iter; ++it, st.next()) {
-      const int s = st.slot, buf = it & 1;
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
       // dS^T(it) is in dP^T buffer buf
       mbar_wait(smem_u32(&bar_dsready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 114);
+      mbar_wait(smem_u32(&bar_qfull[rq.slot]), rq.phase, g, kDevTimeoutBase + 115);
       __syncwarp();
       tc_fence_after_sync();
       // A operand: queries 32h..32h+31 of warpgroup h as pairs in columns
@@ -214,11 +233,11 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk) {
         const uint32_t acol = Gm::DPT_COL + buf * BQ + (kk >> 1) * 32 + (kk & 1) * 8;
-        mma_ts_w(tmem + Gm::DK_COL, tmem + acol, sdesc_add(dQm, s * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
+        mma_ts_w(tmem + Gm::DK_COL, tmem + acol, sdesc_add(dQm, rq.slot * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
                  (it > 0 || kk > 0) ? 1u : 0u);
       }
-      // dP^T(it) and dK(it) were this thread's reads of the stage
-      mma_commit_w(smem_u32(&bar_stempty[s]));
+      mma_commit_w(smem_u32(&bar_qempty[rq.slot]));
+      rq.next();
       // dP^T(it+2) overwrites dS^T(it) behind the dK MMAs that read it
       if (it + 2 < n_iter) issue_dp(it + 2);
     }
@@ -252,10 +271,19 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_vready));
     }
-    RingPos<ST> st;
-    for (int it = 0; it < n_iter; ++it, st.next()) {
-      const int s = st.slot, buf = it & 1;
-      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 115);
+    // delta of query half*32 + lane of a query tile (0 past Lq)
+    auto delta_of = [&](int qt, int gq) {
+      const int qi = qt * BQ + half * 32 + lane;
+      return qi < p.Lq ? p.delta[static_cast<size_t>(b * p.Hq + hk * p.G + gq) * p.Lq + qi] : 0.f;
+    };
+    int gi = 0, qtile = qw.first(qt_start);
+    float dl = n_iter > 0 ? delta_of(qtile, gi) : 0.f;
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
+      const float dl_cur = dl;
+      qtile = qw.next(qtile);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
+      if (it + 1 < n_iter) dl = delta_of(qtile, gi);  // next query tile's, in flight during this one
       mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 116);
       __syncwarp();
       tc_fence_after_sync();
@@ -266,12 +294,12 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       mbar_wait(smem_u32(&xb.pfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 117);
       // the slot's next use (query tile it + 2) expects its bytes: the dV CTA
       // cannot write them before every warp here has released this use
-      if (threadIdx.x == 0 && it + 2 < n_iter && !abort_flag) mbar_arrive_expect_tx(smem_u32(&xb.pfull[buf]), PtXch::SLOT_BYTES);
+      if (threadIdx.x == 0 && it + 2 < n_iter && !abort_flag)
+        mbar_arrive_expect_tx(smem_u32(&xb.pfull[buf]), PtXch::SLOT_BYTES);
       uint4 pv[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) pv[v] = ld_shared_v4(PtXch::addr(sX, buf, r, half * 4 + v));
       tmem_ld_wait(dr);
-      const uint64_t* dlt_row = reinterpret_cast<const uint64_t*>(&dlt_s[s][half * 32]);
       const uint32_t pw[16] = {pv[0].x, pv[0].y, pv[0].z, pv[0].w, pv[1].x, pv[1].y, pv[1].z, pv[1].w,
                                pv[2].x, pv[2].y, pv[2].z, pv[2].w, pv[3].x, pv[3].y, pv[3].z, pv[3].w};
       uint32_t dk[16];
@@ -279,7 +307,8 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       for (int i = 0; i < 16; ++i) {
         const int c0 = 2 * i;
         const float2 pp = E::unpack(pw[i]);
-        const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[c0]), __uint_as_float(dr[c0 + 1])), dlt_row[i]);
+        const uint64_t dl2 = f2_pack(__shfl_sync(0xffffffffu, dl_cur, c0), __shfl_sync(0xffffffffu, dl_cur, c0 + 1));
+        const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[c0]), __uint_as_float(dr[c0 + 1])), dl2);
         float ds0, ds1;
         f2_unpack(f2_mul(f2_pack(pp.x, pp.y), d2), ds0, ds1);
         dk[i] = E::pack(ds0, ds1);
@@ -320,18 +349,30 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
 }
 
 // D = 256, dV half (cluster rank 0): K in tensor memory as the A operand of
-// S^T = K Q^T (copied in by the row threads), so shared memory holds only
-// Q/dO stages (three of 64 KB, enough to hide the loads' latency).  Tensor
-// memory: dV (256 columns), K (128), S^T (two buffers of 64).  The row threads
-// turn S^T into P^T (16-bit pairs), write it over the columns they read and
-// into the partner CTA's hand-off slot, and the MMA warp issues dV += P^T dO,
-// then S^T of the tile after next into the same buffer.
+// S^T = K Q^T (copied in by the row threads), so shared memory holds only the
+// Q and dO rings.  Tensor memory: dV (256 columns), K (128), S^T (two buffers
+// of 64).  The row threads turn S^T into P^T (16-bit pairs) and write it over
+// the columns they read and into a local staging slot; the MMA warp copies
+// the slot to the partner CTA with one bulk copy (so the row threads do not
+// wait on remote stores), issues dV += P^T dO, then S^T of the tile after
+// next into the same buffer.  Half of the exponentials use a polynomial on
+// the FMA pipe: with only the P^T work left on these row threads, the MUFU
+// unit would otherwise set their pace.
 struct Dv256Geom {
   static constexpr int D = 256, BK = 128, BQ = 64, NCH = 4;
-  static constexpr int Q_BYTES = NCH * BQ * 128;  // 32 KB
-  static constexpr int STAGES_FIT = (kMaxDynSmem - kSmemReserve - 1024) / (2 * Q_BYTES);
-  static constexpr int STAGES = STAGES_FIT > 3 ? 3 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * 2 * Q_BYTES;
+  static constexpr int Q_BYTES = NCH * BQ * 128;  // one Q or dO tile, 32 KB
+  static constexpr int NQ = 3, NO = 3;            // Q and dO ring slots
+  static constexpr int STAGE_OFF = (NQ + NO) * Q_BYTES;  // P^T staging slots (the hand-off layout)
+  static constexpr int SMEM_BYTES = 1024 + STAGE_OFF + PtXch::BYTES;
+  // element pairs (of 16 per thread and query tile) whose exponentials use
+  // the polynomial on the FMA pipe instead of the MUFU unit
+#ifndef GBATTN_DV256_POLY
+  static constexpr int POLY = 8;
+#else
+  static constexpr int POLY = GBATTN_DV256_POLY;
+#endif
+  static_assert(POLY >= 0 && POLY <= 16, "polynomial share");
+  static_assert(SMEM_BYTES + 1024 <= kMaxDynSmem, "shared memory budget (1 KB left for static variables)");
   static constexpr int DV_COL = 0, K_COL = 256, ST_COL = 384;  // S^T: 2 x 64
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_COMPUTE_WARPS = 8;
@@ -339,7 +380,7 @@ struct Dv256Geom {
   static constexpr int PRODUCER_WARP = NUM_COMPUTE_WARPS;
   static constexpr int MMA_WARP = NUM_COMPUTE_WARPS + 1;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 2);
-  static_assert(STAGES >= 3, "three Q/dO stages");
+  static_assert(NQ >= 3, "S^T runs two query tiles ahead of dV");
   static_assert(ST_COL + 2 * BQ <= TMEM_COLS, "tensor memory budget");
 };
 
@@ -348,18 +389,20 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
                                            const int bhk, const int kt, PtXchBars& xb) {
   using Gm = Dv256Geom;
   using E = Elem<BF16>;
-  constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
+  constexpr int D = Gm::D, BQ = Gm::BQ, BK = Gm::BK, NQ = Gm::NQ, NO = Gm::NO, NCT = Gm::NCT;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_kready, bar_stfull[ST], bar_stempty[ST], bar_sfull[2], bar_pready[2], bar_accdone;
-  __shared__ __align__(16) float nlse_s[ST][BQ];  // -lse per query column
+  __shared__ uint64_t bar_kready, bar_qfull[NQ], bar_qempty[NQ], bar_ofull[NO], bar_oempty[NO], bar_sfull[2],
+      bar_pready[2], bar_accdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ0 = sbase;
-  const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
+  const uint32_t sdO0 = sQ0 + NQ * Gm::Q_BYTES;
+  const uint32_t sStage = sbase + Gm::STAGE_OFF;                   // P^T staging slots
+  const uint32_t sX1 = cluster_map(sbase + Dk256Geom::XCH_OFF, 1);  // the dK CTA's hand-off slots
 
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int k0 = kt * BK;
@@ -373,9 +416,13 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_kready), NCT);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(smem_u32(&bar_stfull[s]), 33);  // TMA expect_tx arrive + 32 producer lanes
-      mbar_init(smem_u32(&bar_stempty[s]), 1);
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(smem_u32(&bar_qfull[s]), 1);   // TMA expect_tx arrive
+      mbar_init(smem_u32(&bar_qempty[s]), 1);  // S^T's commit
+    }
+    for (int s = 0; s < NO; ++s) {
+      mbar_init(smem_u32(&bar_ofull[s]), 1);
+      mbar_init(smem_u32(&bar_oempty[s]), 1);  // dV's commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_sfull[i]), 1);
@@ -394,6 +441,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
   cluster_sync_all();  // both CTAs' mbarriers are initialised before any remote arrival
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
 
   if (warp == Gm::PRODUCER_WARP) {
     // ---------------- producer (whole warp) ----------------
@@ -402,67 +450,75 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       tma_prefetch_desc(&tmdO);
     }
     __syncwarp();
-    RingPos<ST> st;
-    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
-    int gi = 0, qtile = qw.first(qt_start);
-    // the per-query values of an iteration are loaded one iteration ahead, so
-    // their latency overlaps the wait for a free stage
-    float pre[BQ / 32];
-    auto load_pre = [&]() {
-      const int zq = b * p.Hq + hk * p.G + gi;
-#pragma unroll
-      for (int t = 0; t < BQ / 32; ++t) {
-        const int qi = qtile * BQ + lane + 32 * t;
-        pre[t] = qi < p.Lq ? -p.lse[static_cast<size_t>(zq) * p.Lq + qi] : -INFINITY;
-      }
-    };
-    if (n_iter > 0) load_pre();
-    for (int it = 0; it < n_iter; ++it, st.next()) {
-      const int s = st.slot;
-      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 131);
+    RingPos<NQ> rq;
+    RingPos<NO> ro;
+    // the Q and dO loads walk the (head, query tile) list separately: a
+    // walker carries state under a mask
+    auto wq = qw, wo = qw;
+    int gq = 0, tq = wq.first(qt_start);  // query head in the group and query tile of the next Q load
+    int go = 0, to = wo.first(qt_start);  // and of the next dO load
+    auto load_q = [&](int i) {
+      if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, kDevTimeoutBase + 131);
       __syncwarp();
-      const int q0 = qtile * BQ;
-      const int zq = b * p.Hq + hk * p.G + gi;
-      mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
-      for (int c = 0; c < NCH; ++c) {
-        tma_load_3d_w(sQ0 + s * Gm::Q_BYTES + c * BQ * 128, &tmQ, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
-        tma_load_3d_w(sdO0 + s * Gm::Q_BYTES + c * BQ * 128, &tmdO, smem_u32(&bar_stfull[s]), c * 64, q0, zq);
-      }
-#pragma unroll
-      for (int t = 0; t < BQ / 32; ++t) nlse_s[s][lane + 32 * t] = pre[t];
-      mbar_arrive(smem_u32(&bar_stfull[s]));
-      qtile = qw.next(qtile);
-      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
-      if (it + 1 < n_iter) load_pre();
+      const uint32_t bar = smem_u32(&bar_qfull[rq.slot]);
+      mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
+      load_tile256(sQ0 + rq.slot * Gm::Q_BYTES, &tmQ, bar, tq * BQ, b * p.Hq + hk * p.G + gq);
+      rq.next();
+      tq = wq.next(tq);
+      if (tq >= p.n_qtiles) tq = wq.first(qt_start), ++gq;
+    };
+    auto load_o = [&](int i) {
+      if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, kDevTimeoutBase + 139);
+      __syncwarp();
+      const uint32_t bar = smem_u32(&bar_ofull[ro.slot]);
+      mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
+      load_tile256(sdO0 + ro.slot * Gm::Q_BYTES, &tmdO, bar, to * BQ, b * p.Hq + hk * p.G + go);
+      ro.next();
+      to = wo.next(to);
+      if (to >= p.n_qtiles) to = wo.first(qt_start), ++go;
+    };
+    // in the order the MMA warp needs them: Q runs two query tiles ahead of dO
+    for (int i = 0; i < 2 && i < n_iter; ++i) load_q(i);
+    for (int it = 0; it < n_iter; ++it) {
+      load_o(it);
+      if (it + 2 < n_iter) load_q(it + 2);
     }
-    for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
-      mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
+    for (int i = (n_iter > NQ ? n_iter - NQ : 0); i < n_iter; ++i)
+      mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1, p.limit_ns);
+    for (int i = (n_iter > NO ? n_iter - NO : 0); i < n_iter; ++i)
+      mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1, p.limit_ns);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
     constexpr uint32_t IDESC_ACC = make_idesc_f16(128, D, BF16, false, true);
-    const uint64_t dQk = make_sdesc_sw128(sQ0, 16, 1024);         // Q stage 0, K-major
-    const uint64_t dOm = make_sdesc_sw128(sdO0, BQ * 128, 1024);  // dO stage 0, MN-major
-    RingPos<ST> st, st_s;  // stages of the next dV and of the next S^T
+    const uint64_t dQk = make_sdesc_sw128(sQ0, 16, 1024);         // Q slot 0, K-major
+    const uint64_t dOm = make_sdesc_sw128(sdO0, BQ * 128, 1024);  // dO slot 0, MN-major
+    RingPos<NQ> rq;
+    RingPos<NO> ro;
+    // S^T(it) = K Q^T into buffer it & 1 (K from tensor memory)
     auto issue_s = [&](int it) {
-      const int s = st_s.slot;
-      mbar_wait(smem_u32(&bar_stfull[s]), st_s.phase, g, kDevTimeoutBase + 132);
+      mbar_wait(smem_u32(&bar_qfull[rq.slot]), rq.phase, g, kDevTimeoutBase + 132);
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qo = s * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t qo = rq.slot * Gm::Q_BYTES + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
         mma_ts_w(tmem + Gm::ST_COL + (it & 1) * BQ, tmem + Gm::K_COL + kk * 8, sdesc_add(dQk, qo), IDESC_S,
                  kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_sfull[it & 1]));
-      st_s.next();
+      mma_commit_w(smem_u32(&bar_qempty[rq.slot]));
+      rq.next();
     };
     mbar_wait(smem_u32(&bar_kready), 0, g, kDevTimeoutBase + 133);
     for (int it = 0; it < 2 && it < n_iter; ++it) issue_s(it);
-    for (int it = 0; it < n_iter; ++it, st.next()) {
-      const int s = st.slot, buf = it & 1;
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
       mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 134);
+      // P^T(it) is staged: to the dK CTA's slot, completing on its pfull
+      bulk_s2cluster_w(sX1 + buf * PtXch::SLOT_BYTES, sStage + buf * PtXch::SLOT_BYTES, PtXch::SLOT_BYTES,
+                       cluster_map(smem_u32(&xb.pfull[buf]), 1));
+      mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, kDevTimeoutBase + 135);
       __syncwarp();
       tc_fence_after_sync();
       // A operand: queries 32h..32h+31 of warpgroup h as pairs in columns
@@ -470,10 +526,11 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
       for (int kk = 0; kk < BQ / 16; ++kk) {
         const uint32_t acol = Gm::ST_COL + buf * BQ + (kk >> 1) * 32 + (kk & 1) * 8;
-        mma_ts_w(tmem + Gm::DV_COL, tmem + acol, sdesc_add(dOm, s * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
+        mma_ts_w(tmem + Gm::DV_COL, tmem + acol, sdesc_add(dOm, ro.slot * Gm::Q_BYTES + kk * 2048), IDESC_ACC,
                  (it > 0 || kk > 0) ? 1u : 0u);
       }
-      mma_commit_w(smem_u32(&bar_stempty[s]));
+      mma_commit_w(smem_u32(&bar_oempty[ro.slot]));
+      ro.next();
       // S^T(it+2) overwrites P^T(it) behind the dV MMAs that read it
       if (it + 2 < n_iter) issue_s(it + 2);
     }
@@ -489,7 +546,6 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const int qmin = kj - p.off;
-    const uint32_t sX1 = cluster_map(sbase + Dk256Geom::XCH_OFF, 1);  // the dK CTA's hand-off slots
     {
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::T*>(p.k) +
                                                         (static_cast<size_t>(bhk) * p.kv_pitch + kj) * D + half * 128);
@@ -508,15 +564,20 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_kready));
     }
-    RingPos<ST> st;
-    auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
-    int qtile = qw.first(qt_start);
-    for (int it = 0; it < n_iter; ++it, st.next()) {
-      const int s = st.slot, buf = it & 1;
+    // -lse of query half*32 + lane of a query tile (-inf past Lq)
+    auto nlse_of = [&](int qt, int gq) {
+      const int qi = qt * BQ + half * 32 + lane;
+      return qi < p.Lq ? -p.lse[static_cast<size_t>(b * p.Hq + hk * p.G + gq) * p.Lq + qi] : -INFINITY;
+    };
+    int gi = 0, qtile = qw.first(qt_start);
+    float nl = n_iter > 0 ? nlse_of(qtile, gi) : 0.f;
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
       const int q0 = qtile * BQ;
+      const float nl_cur = nl;
       qtile = qw.next(qtile);
-      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start);
-      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 135);
+      if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
+      if (it + 1 < n_iter) nl = nlse_of(qtile, gi);  // next query tile's, in flight during this one
       mbar_wait(smem_u32(&bar_sfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 136);
       __syncwarp();
       tc_fence_after_sync();
@@ -525,15 +586,20 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       tmem_ld32(scol, sr);
       tmem_ld_wait(sr);
       const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
-      const uint64_t* nlse_row = reinterpret_cast<const uint64_t*>(&nlse_s[s][half * 32]);
       const int qc0 = q0 + half * 32;
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c0 = 2 * i;
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), sl2x2, nlse_row[i]), x0, x1);
-        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        float x0, x1, p0, p1;
+        const uint64_t nl2 = f2_pack(__shfl_sync(0xffffffffu, nl_cur, c0), __shfl_sync(0xffffffffu, nl_cur, c0 + 1));
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), sl2x2, nl2), x0, x1);
+        if ((i + 1) * Gm::POLY / 16 > i * Gm::POLY / 16) {  // POLY of the 16 pairs, spread evenly
+          ex2_poly2(x0, x1, p0, p1);
+        } else {
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
+        }
         if (need_mask) {
           if (qc0 + c0 < qmin) p0 = 0.f;
           if (qc0 + c0 + 1 < qmin) p1 = 0.f;
@@ -541,14 +607,15 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
         pk[i] = E::pack(p0, p1);
       }
       tmem_st16(scol, pk);
-      // P^T(it) to the dK CTA: four 16-byte chunks of this thread's key row,
-      // once that CTA has used the slot's previous contents
+      // P^T(it) into staging slot buf (four 16-byte chunks of this thread's
+      // key row), once the dK CTA has used the slot's previous contents (so
+      // their copy has completed too); visible to the bulk copy after the
+      // proxy fence
       if (it >= 2) mbar_wait(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, kDevTimeoutBase + 138);
-      const uint32_t full1 = cluster_map(smem_u32(&xb.pfull[buf]), 1);
 #pragma unroll
       for (int v = 0; v < 4; ++v)
-        st_async_v4(PtXch::addr(sX1, buf, r, half * 4 + v), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3],
-                    full1);
+        st_shared_v4(PtXch::addr(sStage, buf, r, half * 4 + v), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready[buf]));

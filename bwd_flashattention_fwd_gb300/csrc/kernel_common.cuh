@@ -91,22 +91,28 @@ struct KeptWalk {
   int base = 0;
   uint32_t bits = 0u;
   __device__ __forceinline__ int first(int lo) {
-    if (!MASKED) return lo;
-    base = lo - 32;
-    bits = 0u;
-    return next(lo - 1);
+    if constexpr (!MASKED) {
+      return lo;
+    } else {
+      base = lo - 32;
+      bits = 0u;
+      return next(lo - 1);
+    }
   }
   __device__ __forceinline__ int next(int x) {
-    if (!MASKED) return x + 1;
-    while (bits == 0u) {
-      base += 32;
-      if (base >= hi) return hi;
-      const int y = base + static_cast<int>(threadIdx.x & 31u);
-      bits = __ballot_sync(0xffffffffu, y < hi && keep(y));
+    if constexpr (!MASKED) {
+      return x + 1;
+    } else {
+      while (bits == 0u) {
+        base += 32;
+        if (base >= hi) return hi;
+        const int y = base + static_cast<int>(threadIdx.x & 31u);
+        bits = __ballot_sync(0xffffffffu, y < hi && keep(y));
+      }
+      const int i = __ffs(static_cast<int>(bits)) - 1;
+      bits &= bits - 1u;
+      return base + i;
     }
-    const int i = __ffs(static_cast<int>(bits)) - 1;
-    bits &= bits - 1u;
-    return base + i;
   }
 };
 

@@ -119,14 +119,18 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t local_addr, uint32_t ra
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
-// Asynchronous 16-byte store into another CTA's shared memory; its bytes
-// count against the transaction count of `cluster_bar` (an mbarrier of that
-// CTA) when they land.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t cluster_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-               "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
-               : "memory");
+// Bulk copy of `bytes` from this CTA's shared memory to another CTA's
+// (cluster address), completing on that CTA's mbarrier `cluster_bar`; one
+// elected lane of the calling warp issues it.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2cluster_w(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(cluster_bar)
+      : "memory");
 }
 // Arrive on an mbarrier of another CTA of the cluster with the default
 // (CTA-scope) semantics: for a "buffer free" signal sent after the values read
@@ -386,6 +390,9 @@ __device__ __forceinline__ void tmem_st_wait() {
 // ---------------------------------------------------------------------------
 // Small math helpers
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
