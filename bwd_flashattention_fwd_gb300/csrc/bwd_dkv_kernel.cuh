@@ -32,16 +32,23 @@
 namespace gbattn {
 
 // P^T of one query tile handed from the dV CTA to the dK CTA of a cluster:
-// 128 key rows x 64 queries of 16-bit values, 128 bytes per row as eight
-// 16-byte chunks (chunk j holds queries 8j..8j+7), chunk j of row r stored at
-// position j ^ (r & 7) so that the 32 rows of a warp spread over all banks.
-// Two slots: the dV CTA may run one query tile ahead.
+// 128 key rows x 64 queries of 16-bit values, as eight 2 KB blocks, one per
+// row warp (warp w = 4 * half + quad holds key rows 32 * quad .. +31 and
+// queries 32 * half .. +31 in both CTAs), so each warp sends its own block
+// with one bulk copy.  In a block, lane l's 64 bytes (four 16-byte chunks of
+// eight queries) start at 64 l, chunk c stored at position c ^ ((l >> 1) & 3)
+// so that eight consecutive lanes cover all banks.  Two slots: the dV CTA may
+// run one query tile ahead.
 struct PtXch {
   static constexpr int SLOT_BYTES = 128 * 128;
+  static constexpr int BLOCK_BYTES = 32 * 64;
   static constexpr int SLOTS = 2;
   static constexpr int BYTES = SLOTS * SLOT_BYTES;
-  __device__ __forceinline__ static uint32_t addr(uint32_t base, int slot, int r, int chunk) {
-    return base + slot * SLOT_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4);
+  __device__ __forceinline__ static uint32_t block(uint32_t base, int slot, int warp) {
+    return base + slot * SLOT_BYTES + warp * BLOCK_BYTES;
+  }
+  __device__ __forceinline__ static uint32_t addr(uint32_t base, int slot, int warp, int lane, int chunk) {
+    return block(base, slot, warp) + lane * 64 + ((chunk ^ ((lane >> 1) & 3)) << 4);
   }
 };
 
@@ -298,7 +305,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
         mbar_arrive_expect_tx(smem_u32(&xb.pfull[buf]), PtXch::SLOT_BYTES);
       uint4 pv[4];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) pv[v] = ld_shared_v4(PtXch::addr(sX, buf, r, half * 4 + v));
+      for (int v = 0; v < 4; ++v) pv[v] = ld_shared_v4(PtXch::addr(sX, buf, warp, lane, v));
       tmem_ld_wait(dr);
       const uint32_t pw[16] = {pv[0].x, pv[0].y, pv[0].z, pv[0].w, pv[1].x, pv[1].y, pv[1].z, pv[1].w,
                                pv[2].x, pv[2].y, pv[2].z, pv[2].w, pv[3].x, pv[3].y, pv[3].z, pv[3].w};
@@ -352,10 +359,10 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
 // S^T = K Q^T (copied in by the row threads), so shared memory holds only the
 // Q and dO rings.  Tensor memory: dV (256 columns), K (128), S^T (two buffers
 // of 64).  The row threads turn S^T into P^T (16-bit pairs) and write it over
-// the columns they read and into a local staging slot; the MMA warp copies
-// the slot to the partner CTA with one bulk copy (so the row threads do not
-// wait on remote stores), issues dV += P^T dO, then S^T of the tile after
-// next into the same buffer.  Half of the exponentials use a polynomial on
+// the columns they read and into a local staging slot, which each warp sends
+// to the partner CTA with one bulk copy of its block (so no thread waits on
+// remote stores); the MMA warp issues dV += P^T dO, then S^T of the tile
+// after next into the same buffer.  Half of the exponentials use a polynomial on
 // the FMA pipe: with only the P^T work left on these row threads, the MUFU
 // unit would otherwise set their pace.
 struct Dv256Geom {
@@ -515,9 +522,6 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
       mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 134);
-      // P^T(it) is staged: to the dK CTA's slot, completing on its pfull
-      bulk_s2cluster_w(sX1 + buf * PtXch::SLOT_BYTES, sStage + buf * PtXch::SLOT_BYTES, PtXch::SLOT_BYTES,
-                       cluster_map(smem_u32(&xb.pfull[buf]), 1));
       mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, kDevTimeoutBase + 135);
       __syncwarp();
       tc_fence_after_sync();
@@ -607,15 +611,19 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
         pk[i] = E::pack(p0, p1);
       }
       tmem_st16(scol, pk);
-      // P^T(it) into staging slot buf (four 16-byte chunks of this thread's
-      // key row), once the dK CTA has used the slot's previous contents (so
-      // their copy has completed too); visible to the bulk copy after the
-      // proxy fence
+      // P^T(it) into this warp's block of staging slot buf, once the dK CTA
+      // has used the slot's previous contents (so their copy has completed
+      // too), then to the dK CTA's slot with one bulk copy per warp,
+      // completing on its pfull (the proxy fence makes the stores visible to
+      // the copy)
       if (it >= 2) mbar_wait(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, kDevTimeoutBase + 138);
 #pragma unroll
       for (int v = 0; v < 4; ++v)
-        st_shared_v4(PtXch::addr(sStage, buf, r, half * 4 + v), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        st_shared_v4(PtXch::addr(sStage, buf, warp, lane, v), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
       fence_proxy_async_smem();
+      __syncwarp();
+      bulk_s2cluster_w(PtXch::block(sX1, buf, warp), PtXch::block(sStage, buf, warp), PtXch::BLOCK_BYTES,
+                       cluster_map(smem_u32(&xb.pfull[buf]), 1));
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready[buf]));
