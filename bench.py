@@ -87,16 +87,20 @@ KERNEL_FILES = {
     "bwd_dkv": "bwd_dkv2_kernel.cuh",
     "bwd_dq": "bwd_dq3_kernel.cuh",
 }
+# head dimension 256 runs other kernels for the same phases
+KERNEL_FILES_D256 = dict(KERNEL_FILES, fwd="fwd_kernel.cuh", bwd_dkv="bwd_dkv_kernel.cuh", bwd_dq="bwd_dq_kernel.cuh")
 
 
-def kernel_source_hash(kernel: str | None = None) -> str:
-    """Hash of the sources that define a kernel (its own file, the shared
-    device headers and the launch code), or of all sources."""
+def kernel_source_hash(kernel: str | None = None, D: int = 128) -> str:
+    """Hash of the sources that define a phase's kernel at head dimension D
+    (its own file, the shared device headers and the launch code), or of all
+    sources."""
     csrc = os.path.join(ROOT, "bwd_flashattention_fwd_gb300", "csrc")
     if kernel is None:
         files = sorted(glob.glob(os.path.join(csrc, "*")))
     else:
-        files = [os.path.join(csrc, n) for n in (KERNEL_FILES[kernel], "kernel_common.cuh", "ptx.cuh", "inst.cu")]
+        own = (KERNEL_FILES_D256 if D == 256 else KERNEL_FILES)[kernel]
+        files = [os.path.join(csrc, n) for n in (own, "kernel_common.cuh", "ptx.cuh", "inst.cu")]
     h = hashlib.sha256()
     for p in files:
         with open(p, "rb") as f:
@@ -104,13 +108,13 @@ def kernel_source_hash(kernel: str | None = None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, D: int = 128):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None).  Line format:
     `<kernel> <workload> <bytes_per_launch> <source_hash>`."""
     if kernel not in KERNEL_FILES or not os.path.exists(TRAFFIC_FILE):
         return None
-    cur = kernel_source_hash(kernel)
+    cur = kernel_source_hash(kernel, D)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
@@ -396,12 +400,12 @@ def run_ours(args):
         kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
                       "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
                       "avg_ms": avg[n], "algorithmic": fl,
-                      "traffic": recorded_traffic(n, w.name) if bm is None and not kv_cap else None}
+                      "traffic": recorded_traffic(n, w.name, w.D) if bm is None and not kv_cap else None}
     db = F.delta_bytes(w.B, w.Hq, w.Lq, w.D)
     ach = db / (avg["delta"] * 1e-3) / 1e9
     kernels["delta"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": ach / peaks["hbm_gbs"], "avg_ms": avg["delta"], "algorithmic": db,
-                        "traffic": recorded_traffic("delta", w.name)}
+                        "traffic": recorded_traffic("delta", w.name, w.D)}
     dominant = max(mm_phases, key=lambda n: avg[n])
     roof = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
