@@ -34,6 +34,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -91,10 +92,18 @@ KERNEL_FILES = {
 KERNEL_FILES_D256 = dict(KERNEL_FILES, fwd="fwd_kernel.cuh", bwd_dkv="bwd_dkv_kernel.cuh", bwd_dq="bwd_dq_kernel.cuh")
 
 
+def _code_only(text: bytes) -> bytes:
+    """Source text without // and /* */ comments, trailing spaces and blank
+    lines, so that an edit touching only comments keeps a kernel's hash."""
+    t = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    t = re.sub(rb"//[^\n]*", b"", t)
+    return b"\n".join(line.rstrip() for line in t.split(b"\n") if line.strip())
+
+
 def kernel_source_hash(kernel: str | None = None, D: int = 128) -> str:
-    """Hash of the sources that define a phase's kernel at head dimension D
-    (its own file, the shared device headers and the launch code), or of all
-    sources."""
+    """Hash of the code (comments excluded) that defines a phase's kernel at
+    head dimension D (its own file, the shared device headers and the launch
+    code), or of all sources."""
     csrc = os.path.join(ROOT, "bwd_flashattention_fwd_gb300", "csrc")
     if kernel is None:
         files = sorted(glob.glob(os.path.join(csrc, "*")))
@@ -104,7 +113,7 @@ def kernel_source_hash(kernel: str | None = None, D: int = 128) -> str:
     h = hashlib.sha256()
     for p in files:
         with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+            h.update(os.path.basename(p).encode() + _code_only(f.read()))
     return h.hexdigest()[:16]
 
 

@@ -21,10 +21,11 @@
 // is issued after the MMAs that read them by the same thread (tcgen05 MMAs of
 // one thread run in issue order).
 //
-// Warp roles (320 threads): warps 0-7 row threads -- warp w owns TMEM lanes
-// 32*(w%4)..+31 (key rows) and query columns 32*(w/4)..+31 of each tile;
-// warp 8 producer (TMA for Q/dO tiles, plain loads for the per-query
-// lse/delta values); warp 9 MMA issuer and TMEM owner.
+// Warp roles (320 threads per CTA): warps 0-7 row threads -- warp w owns
+// TMEM lanes 32*(w%4)..+31 (key rows) and query columns 32*(w/4)..+31 of
+// each tile, and loads the lse / delta values of its queries itself;
+// warp 8 producer (TMA for the Q and dO rings); warp 9 MMA issuer and TMEM
+// owner.
 #pragma once
 
 #include "kernel_common.cuh"
@@ -55,8 +56,8 @@ struct PtXch {
 // mbarriers of the hand-off, in the shared memory of both CTAs (the kernel
 // declares them, so they sit at the same offset in either CTA).  pfull, in
 // the dK CTA: one local arrival that expects the slot's bytes, which the dV
-// CTA's asynchronous stores complete (the bytes are visible to a thread that
-// sees the phase complete, as for a TMA load).  pfree, in the dV CTA: one
+// CTA's bulk copies complete (the bytes are visible to a thread that sees the
+// phase complete, as for a TMA load).  pfree, in the dV CTA: one
 // arrival per warp of the dK CTA's row threads once they have used the
 // slot's values.
 struct PtXchBars {
