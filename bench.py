@@ -65,6 +65,11 @@ DEFAULT_WORKLOAD = "qwen3_8b_gqa_l8192_d128"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
+TENSOR_PIPE_FILE = os.path.join(ROOT, "profiles", "tensor_pipe_per_launch.txt")
+# dense 16-bit tensor-core work one SM completes per clock (kind::f16 MMAs with
+# fp32 accumulation: an M=128, N=256, K=16 MMA is 1 Mi FLOP in 128 clocks)
+TENSOR_FLOP_PER_CLK_SM = 8192
+LONG_RUN_STEPS = 100
 
 
 # ---------------------------------------------------------------------------
@@ -117,14 +122,14 @@ def kernel_source_hash(kernel: str | None = None, D: int = 128) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str, D: int = 128):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None).  Line format:
-    `<kernel> <workload> <bytes_per_launch> <source_hash>`."""
-    if kernel not in KERNEL_FILES or not os.path.exists(TRAFFIC_FILE):
+def recorded_figure(path: str, kernel: str, workload: str, D: int = 128):
+    """A per-launch figure from a committed ncu summary, if it was taken on
+    the current kernel sources (else None).  Line format:
+    `<kernel> <workload> <value> <source_hash>`."""
+    if kernel not in KERNEL_FILES or not os.path.exists(path):
         return None
     cur = kernel_source_hash(kernel, D)
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         for line in f:
             parts = line.split()
             if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
@@ -132,40 +137,89 @@ def recorded_traffic(kernel: str, workload: str, D: int = 128):
     return None
 
 
+def recorded_traffic(kernel: str, workload: str, D: int = 128):
+    """DRAM bytes (read + write) per launch, from the committed ncu summary."""
+    return recorded_figure(TRAFFIC_FILE, kernel, workload, D)
+
+
+def recorded_tensor_pipe(kernel: str, workload: str, D: int = 128):
+    """ncu's sm__pipe_tensor_cycles_active (% of peak, active SMs) per launch."""
+    return recorded_figure(TENSOR_PIPE_FILE, kernel, workload, D)
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms while the timed region runs."""
+    """nvidia-smi sampled every 50 ms on a reader thread that stamps each
+    sample with its arrival time.  Start it before the warm-up (the tool
+    takes a while to print its first sample), bracket each timed region with
+    begin() / end(), and window() keeps the samples taken inside it."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_S = 0.05
 
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.samples = []  # (arrival time, fields)
+        self.t_begin = self.t_end = None
 
     def start(self):
+        import atexit
+        import threading
+
+        atexit.register(self.stop)  # no sampler outlives the bench, whatever ends it
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
-                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms",
+                 str(int(self.PERIOD_S * 1000)), "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
 
-    def stop(self) -> dict:
+        def read():
+            for line in self.proc.stdout:
+                self.samples.append((time.perf_counter(), [x.strip() for x in line.split(",")]))
+
+        self.thread = threading.Thread(target=read, daemon=True)
+        self.thread.start()
+
+    def wait_first(self, timeout_s: float = 5.0):
+        """Block until the tool has printed a sample (or the timeout passes)."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.samples and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.01)
+
+    def begin(self):
+        self.t_begin = time.perf_counter()
+
+    def end(self):
+        self.t_end = time.perf_counter()
+
+    def stop(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+
+    def window(self, t_begin=None, t_end=None) -> dict:
+        """Statistics of the samples that arrived between t_begin and t_end
+        (default: the last begin() / end()), plus one sampling period after
+        the end for a region shorter than the period."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
+        t0 = self.t_begin if t_begin is None else t_begin
+        t1 = (self.t_end if t_end is None else t_end) + self.PERIOD_S
         sm, smax, power, reasons = [], [], [], set()
-        for line in out.splitlines():
-            p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+        for t, p in list(self.samples):
+            if not (t0 <= t <= t1) or len(p) < 9:
                 continue
             try:
                 sm.append(float(p[1]))
@@ -177,7 +231,8 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm),
+                "window_s": round(t1 - t0, 4)}
 
 
 def physical_gpu_index(local_rank: int) -> int:
@@ -248,6 +303,63 @@ def cpu_baseline(w: Workload, rows: int) -> dict:
     return {"value": credited / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"fp64 oracle fwd+delta+bwd on the last {rows} query rows of head (b=0,hq=0) and the "
                       f"keys they see ({credited:.3g} credited FLOP per run, {n} runs, {dt:.3f} s each)"}
+
+
+ORACLE_TABLE = ("llama_gqa_l2048_d128", "qwen3_8b_gqa_l8192_d128", "gqa_l8192_d256", "ragged_mha_q4064_k4112_d96")
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        return [{"api": d.get("internal_api"), "threads": d.get("num_threads")} for d in threadpool_info()]
+    except ImportError:
+        return {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS") if k in os.environ} or \
+            "library default (one thread per core)"
+
+
+def run_oracle_table(args):
+    """The fp64 oracle on each full workload, timed on the host cores.  Each
+    (batch, KV head) group is an independent problem the oracle loops over,
+    so one group (its G query heads with their K/V head) is timed and the
+    whole workload's time is that x B x Hkv."""
+    import oracle.attention as A
+    from bwd_flashattention_fwd_gb300.inputs import to_f64
+
+    rows = []
+    for name in ORACLE_TABLE:
+        w = WORKLOADS[name]
+        G = w.Hq // w.Hkv
+        q, k, v, do = make_inputs(w, "cpu")
+        qs, dos = to_f64(q[:1, :G]), to_f64(do[:1, :G])
+        ks, vs = to_f64(k[:1, :1]), to_f64(v[:1, :1])
+        t0 = time.perf_counter()
+        o, _, _ = A.forward(qs, ks, vs, w.scale, w.causal)
+        A.delta(o, dos)
+        A.backward(qs, ks, vs, o, dos, w.scale, w.causal)
+        dt = time.perf_counter() - t0
+        groups = w.B * w.Hkv
+        full_s = dt * groups
+        credited = F.credited_fwd_bwd(w.B, w.Hq, w.Lq, w.Lk, w.D, w.causal)
+        rows.append({"workload": name, "group_s": dt, "groups": groups, "full_s": full_s,
+                     "tflops_credited": credited / full_s / 1e12})
+        print(json.dumps(rows[-1]), flush=True)
+    print(json.dumps({"oracle_table": rows, "cores": cpu_cores(), "cpu_model": cpu_model(),
+                      "blas_threads": blas_threads(),
+                      "method": "fp64 oracle fwd + delta + bwd on one (batch, KV head) group, x B x Hkv"}),
+          flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -353,28 +465,50 @@ def run_ours(args):
         if ev is not None:
             ev[-1].record(stream)
 
+    clocks = ClockSampler(physical_gpu_index(local_rank))
+    clocks.start()
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         step()
     torch.cuda.synchronize(dev)
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during warm-up")
+    clocks.wait_first()
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    clocks = ClockSampler(physical_gpu_index(local_rank))
     replicas.barrier(dev)
     torch.cuda.synchronize(dev)
-    clocks.start()
+    clocks.begin()
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)  # L2 flush between steps, outside the step's events
         step(events[i])
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall
+    clocks.end()
     replicas.barrier(dev)
-    clk = clocks.stop()
+    clk = clocks.window()
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during the timed steps")
+
+    # the same steps over a longer region (power and clocks settle), reported
+    # beside the K-step value, never in place of it
+    long_run = None
+    if args.steps < LONG_RUN_STEPS and not args.no_long_run:
+        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(LONG_RUN_STEPS)]
+        torch.cuda.synchronize(dev)
+        t_l0 = time.perf_counter()
+        for i in range(LONG_RUN_STEPS):
+            flush.fill_(i & 0xFF)
+            lev[i][0].record(stream)
+            step()
+            lev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        lclk_rec = clocks.window(t_l0, time.perf_counter())
+        if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
+            raise RuntimeError("device-side wait timed out during the long run")
+        long_run = {"steps": LONG_RUN_STEPS, "ms_per_step": statistics.mean(a.elapsed_time(b) for a, b in lev),
+                    "clocks": lclk_rec}
 
     per_phase = {n: [] for n in phase_names}
     step_ms = []
@@ -392,7 +526,15 @@ def run_ours(args):
     value_flops, _, max_s = replicas.aggregate_throughput(credited * args.steps, local_s, dev)
     value = value_flops / 1e12
     peaks = load_peaks()
+    if long_run is not None:
+        long_run["value"] = credited / (long_run["ms_per_step"] * 1e-3) / 1e12
+        long_run["unit"] = UNIT
+        long_run["pct_of_bf16_peak"] = 100.0 * long_run["value"] / peaks["bf16_tflops"]
+        long_run["pct_of_bf16_peak_sustained"] = 100.0 * long_run["value"] / peaks["bf16_tflops_sustained"]
     avg = {n: statistics.mean(v) for n, v in per_phase.items()}
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # clock-independent ceiling of the tensor pipe at the clock the run held
+    pipe_tflops = (TENSOR_FLOP_PER_CLK_SM * n_sms * clk["sm_mhz"] * 1e6 / 1e12) if clk.get("sm_mhz") else None
 
     # roofline per kernel (algorithmic work / average launch time)
     kernels = {}
@@ -406,10 +548,15 @@ def run_ours(args):
             continue
         fl = F.kernel_flops_pairs(n, w.B, w.Hq, w.D, pairs)
         ach = fl / (avg[n] * 1e-3) / 1e12
-        kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
-                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
+        plain = bm is None and not kv_cap
+        kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                      "frac_sustained": ach / peaks["bf16_tflops_sustained"],
                       "avg_ms": avg[n], "algorithmic": fl,
-                      "traffic": recorded_traffic(n, w.name, w.D) if bm is None and not kv_cap else None}
+                      "traffic": recorded_traffic(n, w.name, w.D) if plain else None,
+                      "ncu_tensor_pipe_pct": recorded_tensor_pipe(n, w.name, w.D) if plain else None}
+        if pipe_tflops:
+            kernels[n]["frac_of_clock_ceiling"] = ach / pipe_tflops
     db = F.delta_bytes(w.B, w.Hq, w.Lq, w.D)
     ach = db / (avg["delta"] * 1e-3) / 1e9
     kernels["delta"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -418,7 +565,17 @@ def run_ours(args):
     dominant = max(mm_phases, key=lambda n: avg[n])
     roof = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
-    roof["peak_kind"] = f"bf16 dense, sustained ({peaks['source']})"
+    if kernels[dominant]["bound"] == "tensor":
+        roof["peak_kind"] = f"bf16 dense, burst ({peaks['source']}; the timed region is tens of milliseconds)"
+        roof["peak_sustained"] = peaks["bf16_tflops_sustained"]
+        roof["frac_sustained"] = kernels[dominant]["frac_sustained"]
+        roof["ncu_tensor_pipe_pct"] = kernels[dominant]["ncu_tensor_pipe_pct"]
+        if pipe_tflops:
+            roof["clock_ceiling"] = {"tflops": pipe_tflops, "frac": kernels[dominant]["frac_of_clock_ceiling"],
+                                     "basis": f"{TENSOR_FLOP_PER_CLK_SM} FLOP/clk/SM x {n_sms} SMs x median "
+                                              f"sampled SM clock {clk['sm_mhz']} MHz"}
+    else:
+        roof["peak_kind"] = f"HBM copy bandwidth ({peaks['source']})"
 
     # end to end through the public API with host buffers
     e2e = None
@@ -454,6 +611,7 @@ def run_ours(args):
         "phase_ms": avg,
         "roofline": roof,
         "kernels": kernels,
+        "long_run": long_run,
         "e2e": e2e,
         # fwd, delta, dK/dV, dQ; the decode path adds
         # the combine and the dQ reduction
@@ -462,6 +620,7 @@ def run_ours(args):
         "wall_s_timed_region": t_wall,
         "kernel_source_hash": kernel_source_hash(),
     }
+    clocks.stop()
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
     elif rank == 0:
@@ -606,23 +765,27 @@ def run_lce(args):
         if ev is not None:
             ev[2].record(stream)
 
+    clocks = ClockSampler(physical_gpu_index(local_rank))
+    clocks.start()
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         step()
     torch.cuda.synchronize(dev)
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during warm-up")
+    clocks.wait_first()
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = ClockSampler(physical_gpu_index(local_rank))
     replicas.barrier(dev)
     torch.cuda.synchronize(dev)
-    clocks.start()
+    clocks.begin()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         step(events[i])
     torch.cuda.synchronize(dev)
+    clocks.end()
     replicas.barrier(dev)
-    clk = clocks.stop()
+    clocks.stop()
+    clk = clocks.window()
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during the timed steps")
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
@@ -709,12 +872,18 @@ def main(argv=None) -> int:
     ap.add_argument("--lce", action="store_true", help="fused linear cross-entropy step instead of attention")
     ap.add_argument("--lce-workload", default="lce_qwen3_8b_n8192", choices=sorted(LCE_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-long-run", action="store_true",
+                    help=f"skip the extra {LONG_RUN_STEPS}-step run reported beside a shorter timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the fp64 oracle on every full workload (host cores; no GPU)")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")
     ap.add_argument("--ref-rows", type=int, default=128, help="query rows per reference-arm step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.oracle_table:
+        return run_oracle_table(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.lce:

@@ -19,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgbattn.so")
+CHECKS_LIB = os.path.join(PKG, "libgbattn_checks.so")  # device checks of the kernels' math helpers (tests only)
 HEAD_DIMS = (64, 96, 128, 256)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -49,7 +50,7 @@ def _run(cmd):
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile (if stale) and return the path of libgbattn.so."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _sources_mtime():
+    if not force and all(os.path.exists(p) and os.path.getmtime(p) >= _sources_mtime() for p in (LIB, CHECKS_LIB)):
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
@@ -61,15 +62,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     for unit in ("api", "lce"):
         jobs.append([nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, unit + ".cu"), "-o",
                      os.path.join(BUILD, unit + ".o")])
+    checks_obj = os.path.join(BUILD, "checks.o")
+    jobs.append([nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, "checks.cu"), "-o", checks_obj])
     with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         outs = list(ex.map(_run, jobs))
     if verbose:
         for o in outs:
             sys.stdout.write(o)
-    objs = [j[-1] for j in jobs]
+    objs = [j[-1] for j in jobs if j[-1] != checks_obj]
     tmp = LIB + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"])
     os.replace(tmp, LIB)
+    tmp = CHECKS_LIB + ".tmp"
+    _run([nvcc, *ARCH, "-shared", "-o", tmp, checks_obj])
+    os.replace(tmp, CHECKS_LIB)
     return LIB
 
 

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/gbattn.h"
+#include "kernel_common.cuh"
 #include "launch.h"
 
 namespace gbattn {
@@ -451,6 +452,20 @@ attn_status_t noalloc_setup(int* dev_out) {
   return ATTN_OK;
 }
 
+// Whether the device's scratch address has been looked up already.
+bool noalloc_ready() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  return g_noalloc_ptr[dev] != nullptr;
+}
+
+// The scratch's status word on the current device, or null before set-up.
+int* noalloc_status_word(int dev) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  return g_noalloc_ptr[dev] ? reinterpret_cast<int*>(g_noalloc_ptr[dev]) : nullptr;
+}
+
 }  // namespace
 
 extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
@@ -464,6 +479,15 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
   const attn_status_t s = check_attention(B, Hq, Hkv, Lq, Lk, D, scale, causal, dtype);
   if (s != ATTN_OK) return s;
   if (static_cast<long long>(B) * Hq * Lq > kNoAllocMaxRows) return ATTN_ERR_UNSUPPORTED;
+  // The first call on a device looks the scratch address up, which may load
+  // the module: not allowed while the stream is being captured.
+  if (!noalloc_ready()) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();  // an implicit-capture error must not linger for later calls
+      return ATTN_ERR_INVALID_ARG;
+    }
+  }
   int dev = 0;
   const attn_status_t ss = noalloc_setup(&dev);
   if (ss != ATTN_OK) return ss;
@@ -486,6 +510,53 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
   return finish(dispatch_bwd(a));
 }
 
+// ---------------------------------------------------------------------------
+// attn_wait_probe: a check of the failure-reporting path.  One CTA waits,
+// with the same bounded wait as every kernel of the library, on an mbarrier
+// that nothing ever completes; when the wait limit runs out the wait records
+// its code in the status word and returns, and the kernel ends.
+// ---------------------------------------------------------------------------
+namespace gbattn {
+namespace probe {
+
+constexpr int kProbeCode = kDevTimeoutBase + 99;
+
+__global__ void attn_wait_probe_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);  // one arrival expected; none is ever made
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitGuard g{&abort_flag, status, limit_ns};
+  mbar_wait(smem_u32(&bar), 0, g, kProbeCode);
+  __syncthreads();
+}
+
+// Reads the status word at `p` (device memory) and clears it: 1 if a wait had
+// run out, 0 if not, -1 on a CUDA error.  Neither call allocates.
+int take_status_word(int* p) {
+  int h = 0;
+  if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (h == 0) return 0;
+  if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return -1;
+  return 1;
+}
+
+}  // namespace probe
+}  // namespace gbattn
+
+extern "C" attn_status_t attn_wait_probe(cudaStream_t stream) {
+  int dev, num_sms, *status;
+  EncodeTiledFn enc;
+  const attn_status_t ds = device_state(&dev, &enc, &status, &num_sms);
+  if (ds != ATTN_OK) return ds;
+  probe::attn_wait_probe_kernel<<<1, 32, 0, stream>>>(status, wait_limit_ns());
+  return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 extern "C" attn_status_t attn_last_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
   int dev = 0;
@@ -495,14 +566,15 @@ extern "C" attn_status_t attn_last_device_status(cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(g_mu);
     p = g_status[dev];
   }
-  if (!p) return ATTN_OK;
-  int h = 0;
-  if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (h != 0) {
-    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_ERR_TIMEOUT;
+  // the allocating entry points' word, then the word in attn_bwd_noalloc's scratch
+  int timed_out = 0;
+  for (int* w : {p, noalloc_status_word(dev)}) {
+    if (!w) continue;
+    const int r = probe::take_status_word(w);
+    if (r < 0) return ATTN_ERR_CUDA;
+    timed_out |= r;
   }
-  return ATTN_OK;
+  return timed_out ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 extern "C" const char* attn_status_string(attn_status_t s) {

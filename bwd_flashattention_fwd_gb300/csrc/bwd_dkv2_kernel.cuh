@@ -181,9 +181,9 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
     }
-    mbar_wait_drain(smem_u32(&bar_v), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_v), 0);
     for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
-      mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1);
   } else if (warp == Gm::S_MMA_WARP) {
     // ---------------- S^T = K Q^T issuer (A operand K from tensor memory) ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     // Every S^T MMA completed before the last P^T / dS^T was ready, so this
     // commit covers all MMAs of the CTA.
     mma_commit_w(smem_u32(&bar_accdone));
-    mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_accdone), 0);
     __syncwarp();
   } else {
     // ---------------- key-row threads ----------------

@@ -201,9 +201,9 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       if (it + 2 < n_iter) load_o(it + 2);
     }
     for (int i = (n_iter > NQ ? n_iter - NQ : 0); i < n_iter; ++i)
-      mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1);
     for (int i = (n_iter > NO ? n_iter - NO : 0); i < n_iter; ++i)
-      mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t IDESC_DP = make_idesc_f16(128, BQ, BF16, false, false);
@@ -250,7 +250,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       if (it + 2 < n_iter) issue_dp(it + 2);
     }
     mma_commit_w(smem_u32(&bar_accdone));
-    mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_accdone), 0);
     __syncwarp();
   } else {
     // ---------------- key-row threads ----------------
@@ -492,9 +492,9 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       if (it + 2 < n_iter) load_q(it + 2);
     }
     for (int i = (n_iter > NQ ? n_iter - NQ : 0); i < n_iter; ++i)
-      mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1);
     for (int i = (n_iter > NO ? n_iter - NO : 0); i < n_iter; ++i)
-      mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
@@ -540,7 +540,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       if (it + 2 < n_iter) issue_s(it + 2);
     }
     mma_commit_w(smem_u32(&bar_accdone));
-    mbar_wait_drain(smem_u32(&bar_accdone), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_accdone), 0);
     __syncwarp();
   } else {
     // ---------------- key-row threads ----------------

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         if (!wrapped && kv.phase == 0) break;  // before the first stage issued
         kv.phase ^= 1u;
       }
-      mbar_wait_drain(smem_u32(&bar_kvfull[kv.slot]), kv.phase, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_kvfull[kv.slot]), kv.phase);
     }
     __syncwarp();
   } else if (warp == Gm::S_MMA_WARP) {

@@ -169,9 +169,9 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
                       (j0 + jt) * BK, zkv);
     }
     for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
-      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1);
     for (int j = (nk > VST ? nk - VST : 0); j < nk; ++j)
-      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1);
     __syncwarp();
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- S / dP issuer (whole warp, one elected lane issues) ----------------
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     // Every S / dP MMA completed before the last dS was ready, so this commit
     // covers all MMAs of the CTA.
     mma_commit_w(smem_u32(&bar_dqdone));
-    mbar_wait_drain(smem_u32(&bar_dqdone), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_dqdone), 0);
     __syncwarp();
   } else {
     const int quad = warp & 3;   // TMEM lane quadrant (query rows)

@@ -192,9 +192,9 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
         tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, (t0 + i) * BK, bhk);
       }
     }
-    mbar_wait_drain(smem_u32(&bar_q), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_q), 0);
     for (int i = (n_t > ST ? n_t - ST : 0); i < n_t; ++i)
-      mbar_wait_drain(smem_u32(&bar_kvfull[i % ST]), (i / ST) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_kvfull[i % ST]), (i / ST) & 1);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, RQ, BF16, false, false);

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int u = 0; u < ST && u < issued; ++u) {
       if (st.slot == 0) st.phase ^= 1u;
       st.slot = (st.slot == 0 ? ST : st.slot) - 1;
-      mbar_wait_drain(smem_u32(&bar_kvfull[st.slot]), st.phase, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_kvfull[st.slot]), st.phase);
     }
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(352, 1)
       if (n_kv == 0) mma_commit_w(smem_u32(&bar_qfree));  // nothing reads this item's Q
       mma_commit_w(smem_u32(&bar_done));
     }
-    if (r > 0) mbar_wait_drain(smem_u32(&bar_done), (r - 1) & 1, p.limit_ns);
+    if (r > 0) mbar_wait_drain(smem_u32(&bar_done), (r - 1) & 1);
     __syncwarp();
   } else {
     // ---------------- softmax warpgroups ----------------

@@ -159,9 +159,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     // Do not leave the CTA while a copy may still be landing.
     for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
-      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1);
     for (int j = (nk > VST ? nk - VST : 0); j < nk; ++j)
-      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1);
     __syncwarp();
   } else if (warp == 5) {
     // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     // Wait for every MMA of this CTA before tensor memory is released.
     mma_commit_w(smem_u32(&bar_drain));
-    mbar_wait_drain(smem_u32(&bar_drain), 0, p.limit_ns);
+    mbar_wait_drain(smem_u32(&bar_drain), 0);
     __syncwarp();
   } else {
     // ---------------- softmax warps ----------------

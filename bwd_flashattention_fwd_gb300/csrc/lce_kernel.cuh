@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
     for (int u = 0; u < ST && u < issued; ++u) {
       if (st.slot == 0) st.phase ^= 1u;
       st.slot = (st.slot == 0 ? ST : st.slot) - 1;
-      mbar_wait_drain(smem_u32(&bar_full[st.slot]), st.phase, p.limit_ns);
+      mbar_wait_drain(smem_u32(&bar_full[st.slot]), st.phase);
     }
     __syncwarp();
   } else if (warp == 5) {
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
       mma_commit_w(smem_u32(&bar_accfull[b]));
     }
     // every MMA of the CTA is complete before tensor memory is released
-    if (u > 0) mbar_wait_drain(smem_u32(&bar_accfull[(u - 1) & 1]), ((u - 1) >> 1) & 1, p.limit_ns);
+    if (u > 0) mbar_wait_drain(smem_u32(&bar_accfull[(u - 1) & 1]), ((u - 1) >> 1) & 1);
     __syncwarp();
   } else {
     // ---------------- epilogue: thread = row of the tile ----------------

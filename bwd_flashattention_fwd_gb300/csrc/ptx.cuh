@@ -91,11 +91,15 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, const W
 
 // Bounded wait that ignores the abort flag.  Used only at the end of a CTA, so
 // that no asynchronous copy or MMA is still in flight when the CTA releases its
-// shared and tensor memory.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+// shared and tensor memory.  Its limit is fixed and generous (4 s), separate
+// from the pipeline waits' configurable limit: a copy or MMA that was issued
+// completes on its own, so a short pipeline limit must not cut this wait off.
+constexpr uint64_t kDrainLimitNs = 4000000000ull;
+
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > limit_ns) return;
+    if (global_timer_ns() - t0 > kDrainLimitNs) return;
   }
 }
 
@@ -451,7 +455,10 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // relative error on [-1/2, 1/2] (fitted by a Remez exchange; max relative
 // error 7.5e-5, below the 2^-9 half-ulp of bf16 and the 2^-11 of fp16 that P
 // is rounded to), and the exponent n added to the result's exponent field.
-// Inputs below -126 are clamped there (the result is then < 1.2e-38).
+// Inputs below -126 are clamped there.  At the bottom edge, x in [-126,
+// -125.9999], the polynomial's value just below 1 meets the smallest exponent
+// and is encoded as a subnormal, which doubles the error there (1.44e-4
+// relative); those results are below 1.2e-38.
 // Used where the MUFU unit is shared with a warp that issues tensor-core
 // instructions: MUFU traffic on a sub-partition delays that warp's issue.
 __device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& y1) {

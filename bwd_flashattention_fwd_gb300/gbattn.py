@@ -26,7 +26,7 @@ ATTN_DTYPE_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_delta", "attn_bwd", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc",
             "attn_fwd_masked", "attn_bwd_masked", "attn_fwd_ex", "attn_bwd_ex", "attn_decode_workspace_bytes",
-            "attn_fwd_decode", "attn_bwd_decode", "attn_last_device_status", "attn_status_string",
+            "attn_fwd_decode", "attn_bwd_decode", "attn_last_device_status", "attn_wait_probe", "attn_status_string",
             "lce_workspace_bytes", "lce_fwd", "lce_bwd")
 
 _lib = None
@@ -85,6 +85,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lce_bwd.restype = ci
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = ci
+    lib.attn_wait_probe.argtypes = [vp]
+    lib.attn_wait_probe.restype = ci
     lib.attn_status_string.argtypes = [ci]
     lib.attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -113,6 +115,36 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _require(call: str, dense=(), sliced=(), f32=(), u8=(), i32=()):
+    """Reject tensors the C ABI cannot take before any pointer crosses it.
+    dense: 16-bit tensors that must be contiguous (one dtype for all of them
+    and for `sliced`); sliced: 16-bit tensors whose layout the caller has
+    checked separately (k / v slices of a cache); f32 / u8 / i32: contiguous
+    float32 / uint8 / int32 tensors.  Every tensor must be on the current CUDA
+    device.  None entries are skipped."""
+    half = None
+    dev = None
+    groups = ((dense, None, True), (sliced, None, False), (f32, torch.float32, True), (u8, torch.uint8, True),
+              (i32, torch.int32, True))
+    for ts, want, contig in groups:
+        for t in ts:
+            if t is None:
+                continue
+            if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+                raise ValueError(f"{call}: every tensor must be a CUDA tensor; got {getattr(t, 'device', type(t))}")
+            dev = torch.cuda.current_device() if dev is None else dev
+            if t.device.index != dev:
+                raise ValueError(f"{call}: every tensor must be on the current CUDA device (cuda:{dev}); got {t.device}")
+            if contig and not t.is_contiguous():
+                raise ValueError(f"{call}: tensor of shape {tuple(t.shape)} strides {t.stride()} is not contiguous")
+            if want is None:
+                half = half or t.dtype
+                if t.dtype not in (torch.bfloat16, torch.float16) or t.dtype != half:
+                    raise TypeError(f"{call}: 16-bit tensors must all be bfloat16 or all float16; got {t.dtype}")
+            elif t.dtype != want:
+                raise TypeError(f"{call}: expected {want}, got {t.dtype}")
+
+
 def _check(status: int, call: str, check: bool) -> int:
     if check and status != ATTN_OK:
         raise AttnError(status, call)
@@ -121,6 +153,7 @@ def _check(status: int, call: str, check: bool) -> int:
 
 def attn_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None, check: bool = True) -> int:
     """O and base-2 LSE of causal/non-causal GQA attention (writes o, lse)."""
+    _require("attn_fwd", dense=(q, k, v, o), f32=(lse,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Lq, Lk, D,
@@ -130,6 +163,7 @@ def attn_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None, check: bo
 
 def attn_bwd_delta(o, dO, delta, stream=None, check: bool = True) -> int:
     """delta = rowsum(dO * O) in float32 (writes delta)."""
+    _require("attn_bwd_delta", dense=(o, dO), f32=(delta,))
     B, Hq, Lq, D = o.shape
     st = load_library().attn_bwd_delta(_ptr(o), _ptr(dO), _ptr(delta), B, Hq, Lq, D, _dtype_code(o),
                                        _stream_handle(stream))
@@ -139,6 +173,7 @@ def attn_bwd_delta(o, dO, delta, stream=None, check: bool = True) -> int:
 def attn_bwd(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bool, stream=None,
              check: bool = True) -> int:
     """dQ, dK, dV of the attention (writes dq, dk, dv)."""
+    _require("attn_bwd", dense=(q, k, v, o, dO, dq, dk, dv), f32=(lse, delta))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
@@ -149,6 +184,7 @@ def attn_bwd(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bool,
 
 def attn_bwd_dq(q, k, v, dO, lse, delta, dq, scale: float, causal: bool, stream=None, check: bool = True) -> int:
     """dQ only (the query-row-owning half of attn_bwd)."""
+    _require("attn_bwd_dq", dense=(q, k, v, dO, dq), f32=(lse, delta))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(delta), _ptr(dq), B, Hq,
@@ -160,6 +196,7 @@ def attn_bwd_dq(q, k, v, dO, lse, delta, dq, scale: float, causal: bool, stream=
 def attn_bwd_dkv(q, k, v, dO, lse, delta, dk, dv, scale: float, causal: bool, stream=None,
                  check: bool = True) -> int:
     """dK and dV only (the key-row-owning half of attn_bwd)."""
+    _require("attn_bwd_dkv", dense=(q, k, v, dO, dk, dv), f32=(lse, delta))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_bwd_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(delta), _ptr(dk),
@@ -172,6 +209,7 @@ def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, scale: float, causal: bool
                      check: bool = True) -> int:
     """attn_bwd for callers that cannot allocate device memory: delta and the
     status word live in the library's fixed scratch array (B*Hq*Lq <= 2**20)."""
+    _require("attn_bwd_noalloc", dense=(q, k, v, o, dO, dq, dk, dv), f32=(lse,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
@@ -183,6 +221,7 @@ def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, scale: float, causal: bool
 def attn_fwd_masked(q, k, v, o, lse, block_mask, scale: float, causal: bool, stream=None,
                     check: bool = True) -> int:
     """attn_fwd with a uint8 block mask [ceil(Lq/128), ceil(Lk/128)] on the device."""
+    _require("attn_fwd_masked", dense=(q, k, v, o), f32=(lse,), u8=(block_mask,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(block_mask), B, Hq,
@@ -194,6 +233,7 @@ def attn_fwd_masked(q, k, v, o, lse, block_mask, scale: float, causal: bool, str
 def attn_bwd_masked(q, k, v, o, dO, lse, delta, block_mask, dq, dk, dv, scale: float, causal: bool, stream=None,
                     check: bool = True) -> int:
     """attn_bwd with the block mask of attn_fwd_masked."""
+    _require("attn_bwd_masked", dense=(q, k, v, o, dO, dq, dk, dv), f32=(lse, delta), u8=(block_mask,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
@@ -220,6 +260,7 @@ def attn_fwd_ex(q, k, v, o, lse, scale: float, causal: bool, block_mask=None, kv
                 check: bool = True) -> int:
     """attn_fwd with an optional block mask and k / v sliced from a longer
     cache (kv_pitch None: taken from the tensors' strides)."""
+    _require("attn_fwd_ex", dense=(q, o), sliced=(k, v), f32=(lse,), u8=(block_mask,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     pitch = kv_row_pitch(k, v) if kv_pitch is None else int(kv_pitch)
@@ -232,6 +273,7 @@ def attn_fwd_ex(q, k, v, o, lse, scale: float, causal: bool, block_mask=None, kv
 def attn_bwd_ex(q, k, v, o, dO, lse, delta, dq, dk, dv, scale: float, causal: bool, block_mask=None, kv_pitch=None,
                 stream=None, check: bool = True) -> int:
     """attn_bwd with the options of attn_fwd_ex (dk, dv contiguous)."""
+    _require("attn_bwd_ex", dense=(q, o, dO, dq, dk, dv), sliced=(k, v), f32=(lse, delta), u8=(block_mask,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     pitch = kv_row_pitch(k, v) if kv_pitch is None else int(kv_pitch)
@@ -257,6 +299,7 @@ def decode_workspace(q, k) -> torch.Tensor:
 
 def attn_fwd_decode(q, k, v, o, lse, workspace, scale: float, causal: bool, stream=None, check: bool = True) -> int:
     """attn_fwd for short query lengths (G * Lq <= 128), key range split over CTAs."""
+    _require("attn_fwd_decode", dense=(q, k, v, o), f32=(lse,), u8=(workspace,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
@@ -268,6 +311,7 @@ def attn_fwd_decode(q, k, v, o, lse, workspace, scale: float, causal: bool, stre
 def attn_bwd_decode(q, k, v, o, dO, lse, delta, dq, dk, dv, workspace, scale: float, causal: bool, stream=None,
                     check: bool = True) -> int:
     """attn_bwd for short query lengths (G * Lq <= 128)."""
+    _require("attn_bwd_decode", dense=(q, k, v, o, dO, dq, dk, dv), f32=(lse, delta), u8=(workspace,))
     B, Hq, Lq, D = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     st = load_library().attn_bwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta),
@@ -292,6 +336,7 @@ def lce_workspace(hidden, weight) -> torch.Tensor:
 
 def lce_fwd(hidden, weight, targets, loss, lse, workspace, stream=None, check: bool = True) -> int:
     """Per-row linear cross-entropy loss and natural-log lse (writes loss, lse)."""
+    _require("lce_fwd", dense=(hidden, weight), f32=(loss, lse), u8=(workspace,), i32=(targets,))
     N, Dm = hidden.shape
     st = load_library().lce_fwd(_ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss), _ptr(lse), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), N, Dm, weight.shape[0],
@@ -301,6 +346,8 @@ def lce_fwd(hidden, weight, targets, loss, lse, workspace, stream=None, check: b
 
 def lce_bwd(hidden, weight, targets, lse, dloss, dhidden, dweight, workspace, stream=None, check: bool = True) -> int:
     """dhidden and dweight of sum_i dloss[i] * loss[i] (writes both)."""
+    _require("lce_bwd", dense=(hidden, weight, dhidden, dweight), f32=(lse, dloss), u8=(workspace,),
+             i32=(targets,))
     N, Dm = hidden.shape
     st = load_library().lce_bwd(_ptr(hidden), _ptr(weight), _ptr(targets), _ptr(lse), _ptr(dloss), _ptr(dhidden),
                                 _ptr(dweight), _ptr(workspace), workspace.numel() * workspace.element_size(), N, Dm,
@@ -310,6 +357,13 @@ def lce_bwd(hidden, weight, targets, lse, dloss, dhidden, dweight, workspace, st
 
 def attn_last_device_status(stream=None) -> int:
     return load_library().attn_last_device_status(_stream_handle(stream))
+
+
+def attn_wait_probe(stream=None, check: bool = True) -> int:
+    """Launch the failure-reporting check: one wait that can only run out
+    (after GBATTN_WAIT_LIMIT_NS); the next attn_last_device_status reports
+    ATTN_ERR_TIMEOUT."""
+    return _check(load_library().attn_wait_probe(_stream_handle(stream)), "attn_wait_probe", check)
 
 
 def attn_status_string(status: int) -> str:

@@ -212,7 +212,8 @@ attn_status_t attn_bwd_decode(const void* q, const void* k, const void* v, const
  *   1,048,576) are rejected with ATTN_ERR_UNSUPPORTED before anything runs.
  *   Set-up: the first call on each device looks up the scratch array's device
  *   address (with that device current); make that first call before any
- *   stream capture.
+ *   stream capture.  A first call on a device made while `stream` is being
+ *   captured is refused with ATTN_ERR_INVALID_ARG and changes nothing.
  *   Sharing: every call on a device uses the same scratch array, and the
  *   array keeps the last call's contents (the status word is cleared at the
  *   start of each call; delta is fully rewritten).  Calls whose work overlaps
@@ -220,19 +221,34 @@ attn_status_t attn_bwd_decode(const void* q, const void* k, const void* v, const
  *   on the scratch and give wrong results; order them on one stream.
  *   Errors: argument and launch errors as for attn_bwd.  A bounded device wait
  *   that runs out is recorded in the scratch's status word, which
- *   attn_last_device_status does not read.
+ *   attn_last_device_status reads and clears (reading it allocates nothing).
  */
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq,
                                int Lk, int D, float scale, int causal, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
- * Synchronises `stream`, then reports and clears the device status word of the
- * current device: ATTN_ERR_TIMEOUT if a bounded device-side wait ran out in a
- * kernel since the last call, ATTN_ERR_CUDA if the stream reported an error,
- * ATTN_OK otherwise.
+ * Synchronises `stream`, then reports and clears the device status words of the
+ * current device (the one the entry points above share, and the one in
+ * attn_bwd_noalloc's scratch): ATTN_ERR_TIMEOUT if a bounded device-side wait
+ * ran out in a kernel since the last call, ATTN_ERR_CUDA if the stream
+ * reported an error, ATTN_OK otherwise.  A failure is a typed error, never a
+ * silent change of behaviour ("When the Bottleneck Moved", section 3: what
+ * the implementation does not support fails with a typed error).
  */
 attn_status_t attn_last_device_status(cudaStream_t stream);
+
+/*
+ * A check of the failure-reporting path; it computes nothing.  Launches one
+ * CTA that waits, with the bounded wait every kernel of this library uses, on
+ * an mbarrier that nothing ever completes.  When the wait limit runs out
+ * (environment variable GBATTN_WAIT_LIMIT_NS, read once per process, in
+ * nanoseconds; default 2 s) the wait records its code in the device status
+ * word and the kernel returns, so the next attn_last_device_status(stream)
+ * returns ATTN_ERR_TIMEOUT and the context stays usable.  Neither faults nor
+ * hangs the GPU.  Returns ATTN_ERR_CUDA if the launch fails, else ATTN_OK.
+ */
+attn_status_t attn_wait_probe(cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t s);

@@ -62,16 +62,6 @@ def backward(h: np.ndarray, w: np.ndarray, t: np.ndarray, lse: np.ndarray, dloss
     return g @ w, g.T @ h
 
 
-def flops_forward(N: int, V: int, Dm: int) -> float:
-    """One matrix product H W^T: 2 N V Dm."""
-    return 2.0 * N * V * Dm
-
-
-def flops_backward(N: int, V: int, Dm: int) -> float:
-    """Recomputed logits, g W and g^T H: three products of 2 N V Dm."""
-    return 3.0 * flops_forward(N, V, Dm)
-
-
 # ---------------------------------------------------------------------------
 # Helpers for large problems: the same definitions evaluated on chosen rows or
 # vocabulary entries, with the weight matrix decoded one vocabulary chunk at a

@@ -104,6 +104,21 @@ def test_binding_raises_on_error(lib):
         gbattn._check(gbattn.ATTN_ERR_UNSUPPORTED, "attn_fwd", True)
 
 
+def test_binding_rejects_host_tensors_before_the_abi():
+    """The wrappers check their tensors before any pointer reaches the
+    library: host tensors, wrong dtypes and mixed 16-bit types are refused."""
+    import torch
+
+    q = torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16)
+    lse = torch.zeros((1, 2, 8), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gbattn.attn_fwd(q, q, q, q, lse, 0.125, True)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gbattn.attn_bwd_delta(q, q, lse)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gbattn.lce_fwd(q[0, 0], q[0, 0], lse[0, 0].int(), lse[0, 0], lse[0, 0], lse)
+
+
 def fwd_masked(lib, mask=FAKE, D=128, Lq=300, Lk=300):
     return lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, mask, 1, 4, 2, Lq, Lk, D, ctypes.c_float(0.1), 1, 1,
                                None)

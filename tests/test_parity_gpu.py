@@ -59,11 +59,22 @@ def assert_abs(gpu, ref, atol, what):
         raise AssertionError(f"{what}: max abs err {err.max():.3g} at {idx}: gpu {g[idx]} ref {ref[idx]}")
 
 
+def nan_like(t, shape=None, dtype=None):
+    """An output buffer filled with NaN, so that an element no kernel writes
+    stays non-finite and fails the checks."""
+    return torch.full(t.shape if shape is None else shape, float("nan"), dtype=t.dtype if dtype is None else dtype,
+                      device=t.device)
+
+
 def run_chain(w: Workload, q, k, v, do):
-    """fwd -> delta -> bwd through the C ABI on the current stream."""
-    o, lse = gbattn.forward(q, k, v, w.scale, w.causal)
-    dlt = gbattn.delta(o, do)
-    dq, dk, dv = gbattn.backward(q, k, v, o, do, lse, dlt, w.scale, w.causal)
+    """fwd -> delta -> bwd through the C ABI on the current stream, into
+    NaN-filled outputs."""
+    rows = (w.B, w.Hq, w.Lq)
+    o, lse, dlt = nan_like(q), nan_like(q, rows, torch.float32), nan_like(q, rows, torch.float32)
+    dq, dk, dv = nan_like(q), nan_like(k), nan_like(v)
+    gbattn.attn_fwd(q, k, v, o, lse, w.scale, w.causal)
+    gbattn.attn_bwd_delta(o, do, dlt)
+    gbattn.attn_bwd(q, k, v, o, do, lse, dlt, dq, dk, dv, w.scale, w.causal)
     assert gbattn.attn_last_device_status() == gbattn.ATTN_OK
     return o, lse, dlt, dq, dk, dv
 
@@ -115,6 +126,27 @@ SMALL.append(Workload("grid_gqa32_8_l64_d128", B=1, Hq=32, Hkv=8, Lq=64, Lk=64, 
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
 def test_chain_matches_oracle(w):
+    check_full(w)
+
+
+# Problems with more work items than a GB300 has SMs, compared on every output
+# element: the persistent forward (items of 256 query rows) and dQ (items of
+# 128 query rows) kernels launch one CTA per SM, so only here does a CTA run
+# several items -- the next-item prefetch, the item-boundary hand-over and the
+# snake order of the work list.  Outputs start as NaN, so an item no CTA
+# writes fails.  The first is the B2 Hq32 Hkv8 L2048 D128 workload itself
+# (512 forward items, 1024 dQ items).
+MULTI_ITEM = [
+    WORKLOADS["llama_gqa_l2048_d128"],
+    Workload("multi_item_ragged_q1100_k1300_d96_fp16", B=2, Hq=16, Hkv=4, Lq=1100, Lk=1300, D=96, dtype="fp16",
+             std=0.5, seed=3101),
+    Workload("multi_item_dense_l900_d64", B=3, Hq=16, Hkv=2, Lq=900, Lk=900, D=64, causal=False, seed=3102),
+    Workload("multi_key_tile_l1536_d256", B=1, Hq=8, Hkv=2, Lq=1536, Lk=1536, D=256, seed=3103),
+]
+
+
+@pytest.mark.parametrize("w", MULTI_ITEM, ids=[w.name for w in MULTI_ITEM])
+def test_multi_item_every_element(w):
     check_full(w)
 
 
@@ -219,8 +251,8 @@ def check_sampled(w: Workload):
     rng = np.random.default_rng(w.seed)
     q, k, v, do = make_inputs(w, "cuda")
     o, lse, dlt, dq, dk, dv = run_chain(w, q, k, v, do)
-    for t in (o, lse, dlt, dq, dk, dv):
-        assert torch.isfinite(t).all()
+    for t, name in ((o, "o"), (lse, "lse"), (dlt, "delta"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        assert torch.isfinite(t).all(), f"{name}: elements left unwritten (NaN) or non-finite"
     qd, kd, vd, dod = (to_f64(t) for t in (q, k, v, do))
     G = w.Hq // w.Hkv
     heads = sorted({(0, 0), (w.B - 1, w.Hq - 1), (w.B // 2, w.Hq // 2)})
@@ -269,10 +301,9 @@ def test_long_context_memory_and_sampled_parity():
     Lq x Lk buffer), and sampled outputs match the oracle."""
     w = MEMORY_CHECK
     q, k, v, do = make_inputs(w, "cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq, w.Lq), dtype=torch.float32, device="cuda")
-    dlt = torch.empty_like(lse)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rows = (w.B, w.Hq, w.Lq)
+    o, lse, dlt = nan_like(q), nan_like(q, rows, torch.float32), nan_like(q, rows, torch.float32)
+    dq, dk, dv = nan_like(q), nan_like(k), nan_like(v)
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats()
     base = torch.cuda.memory_allocated()
@@ -285,6 +316,8 @@ def test_long_context_memory_and_sampled_parity():
     assert torch.cuda.max_memory_allocated() == base
     assert free0 - free1 <= 4 * 2**20, (free0 - free1)
     assert gbattn.attn_last_device_status() == gbattn.ATTN_OK
+    for t, name in ((o, "o"), (lse, "lse"), (dlt, "delta"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        assert torch.isfinite(t).all(), f"{name}: elements left unwritten (NaN) or non-finite"
     rng = np.random.default_rng(1)
     rows = _sample_rows(w.Lq, rng)
     qd, kd, vd, dod = (to_f64(t) for t in (q, k, v, do))
@@ -295,3 +328,21 @@ def test_long_context_memory_and_sampled_parity():
     o_full[0, 5, rows] = o_ref
     dq_ref = A.backward_query_rows(qd, kd, vd, o_full, dod, w.scale, True, 0, 5, rows)
     assert_close(to_f64(dq)[0, 5, rows], dq_ref, "bf16", "dQ")
+
+
+def test_binding_rejects_bad_layouts():
+    """Non-contiguous tensors, a float32 tensor where a 16-bit one belongs and
+    mixed 16-bit types are refused by the binding before the C ABI."""
+    w = Workload("layout", B=1, Hq=2, Hkv=1, Lq=64, Lk=64, D=64, seed=6200)
+    q, k, v, do = make_inputs(w, "cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 2, 64), dtype=torch.float32, device="cuda")
+    qt = q.transpose(2, 3).contiguous().transpose(2, 3)  # same shape, D not the fastest axis
+    with pytest.raises(ValueError, match="not contiguous"):
+        gbattn.attn_fwd(qt, k, v, o, lse, w.scale, True)
+    with pytest.raises(TypeError):
+        gbattn.attn_fwd(q.float(), k, v, o, lse, w.scale, True)
+    with pytest.raises(TypeError):
+        gbattn.attn_fwd(q, k.half(), v, o, lse, w.scale, True)
+    with pytest.raises(TypeError):
+        gbattn.attn_fwd(q, k, v, o, lse.double(), w.scale, True)
