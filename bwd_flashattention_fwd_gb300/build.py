@@ -2,8 +2,9 @@
 
 The kernel instantiations compile as one translation unit per head dimension
 (inst.cu with -DGBATTN_HEAD_DIM=<D>), in parallel, plus the C-ABI unit and
-the linear cross-entropy unit (lce.cu); the objects link, with cuBLAS, into
-bwd_flashattention_fwd_gb300/libgbattn.so.
+the linear cross-entropy unit (lce.cu); the objects link into
+bwd_flashattention_fwd_gb300/libgbattn.so (no library besides the CUDA
+runtime).  checks.cu becomes libgbattn_checks.so, a test aid.
 """
 
 from __future__ import annotations
@@ -71,7 +72,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stdout.write(o)
     objs = [j[-1] for j in jobs if j[-1] != checks_obj]
     tmp = LIB + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"])
+    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)
     tmp = CHECKS_LIB + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-o", tmp, checks_obj])

@@ -1,22 +1,16 @@
 // C ABI of the linear cross-entropy calls (declared in include/gblce.h):
 // validation, tensor maps, the logits-tile kernels of lce_kernel.cuh and, in
-// the backward, two cuBLAS GEMMs per vocabulary chunk.
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// the backward, the two gradient products of lce_gemm_kernel.cuh per
+// vocabulary chunk.
 #include "../../include/gblce.h"
 #include "launch.h"
+#include "lce_gemm_kernel.cuh"
 #include "lce_kernel.cuh"
 
 namespace gbattn {
 namespace {
 
 constexpr int kLceVocabChunk = 16384;  // vocabulary entries per backward chunk (64 tiles)
-constexpr int kMaxLceDevices = 64;
-
-std::mutex g_lce_mu;
-cublasHandle_t g_cublas[kMaxLceDevices] = {};
 
 size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
@@ -73,10 +67,25 @@ int launch_logits(const LceParams& p, const CUtensorMap& tmH, const CUtensorMap&
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
-cublasHandle_t cublas_for(int dev) {
-  std::lock_guard<std::mutex> lock(g_lce_mu);
-  if (!g_cublas[dev] && cublasCreate(&g_cublas[dev]) != CUBLAS_STATUS_SUCCESS) g_cublas[dev] = nullptr;
-  return g_cublas[dev];
+template <bool BF16, bool A_MN>
+int launch_gemm(const LceGemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int num_sms,
+                cudaStream_t stream) {
+  auto kern = lce_gemm_kernel<BF16, A_MN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LceGemmGeom::SMEM_BYTES) !=
+      cudaSuccess)
+    return kLaunchCudaError;
+  const long long tiles = static_cast<long long>(p.n_mt) * p.n_nt;
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  kern<<<grid, LceGemmGeom::NUM_THREADS, LceGemmGeom::SMEM_BYTES, stream>>>(tmA, tmB, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
+template <bool BF16>
+int launch_gemm_pair(const LceGemmParams& dh, const CUtensorMap& tmGk, const CUtensorMap& tmWn,
+                     const LceGemmParams& dw, const CUtensorMap& tmGm, const CUtensorMap& tmHn, int num_sms,
+                     cudaStream_t stream) {
+  const int r = launch_gemm<BF16, false>(dh, tmGk, tmWn, num_sms, stream);
+  return r != kLaunchOk ? r : launch_gemm<BF16, true>(dw, tmGm, tmHn, num_sms, stream);
 }
 
 attn_status_t finish(int r) {
@@ -149,17 +158,17 @@ extern "C" attn_status_t lce_bwd(const void* hidden, const void* weight, const i
   EncodeTiledFn enc;
   const attn_status_t ds = shared_device_state(&dev, &enc, &status, &num_sms);
   if (ds != ATTN_OK) return ds;
-  if (dev >= kMaxLceDevices) return ATTN_ERR_CUDA;
-  cublasHandle_t h = cublas_for(dev);
-  if (!h || cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return ATTN_ERR_CUDA;
   const bool bf16 = dtype == ATTN_DTYPE_BF16;
-  const cudaDataType_t t16 = bf16 ? CUDA_R_16BF : CUDA_R_16F;
-  CUtensorMap tmH, tmW;
-  if (!lce_map(enc, &tmH, hidden, N, Dm, LceGeom::BM, bf16) || !lce_map(enc, &tmW, weight, V, Dm, LceGeom::BN, bf16))
-    return ATTN_ERR_INVALID_ARG;
   const int ldg = chunk_cols(V);
   void* g = workspace;
   float* dh32 = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(static_cast<size_t>(N) * ldg * 2));
+  // logits tiles (K-major H and W); the products: g K-major [N][ldg] for dH,
+  // g MN-major (read transposed) for dW, W and H MN-major
+  CUtensorMap tmH, tmW, tmGk, tmGm, tmWn, tmHn;
+  if (!lce_map(enc, &tmH, hidden, N, Dm, LceGeom::BM, bf16) || !lce_map(enc, &tmW, weight, V, Dm, LceGeom::BN, bf16) ||
+      !lce_map(enc, &tmGk, g, N, ldg, LceGemmGeom::BM, bf16) || !lce_map(enc, &tmGm, g, N, ldg, 64, bf16) ||
+      !lce_map(enc, &tmWn, weight, V, Dm, 64, bf16) || !lce_map(enc, &tmHn, hidden, N, Dm, 64, bf16))
+    return ATTN_ERR_INVALID_ARG;
   LceParams p{};
   p.N = N, p.Dm = Dm, p.V = V;
   p.n_rt = (N + LceGeom::BM - 1) / LceGeom::BM;
@@ -167,30 +176,33 @@ extern "C" attn_status_t lce_bwd(const void* hidden, const void* weight, const i
   p.lse = lse, p.dloss = dloss, p.g = g, p.ldg = ldg;
   p.status = status;
   p.limit_ns = shared_wait_limit_ns();
-  const float one = 1.f, zero = 0.f;
+  const int n_ht = (Dm + LceGemmGeom::BN - 1) / LceGemmGeom::BN;  // tiles along the hidden size
   for (int v0 = 0; v0 < V; v0 += ldg) {
     const int vc = V - v0 < ldg ? V - v0 : ldg;
+    const bool first = v0 == 0, last = v0 + vc >= V;
     p.v0 = v0, p.v_end = v0 + vc, p.n_vt = vocab_tiles(vc);
-    const int r = bf16 ? launch_logits<true, true>(p, tmH, tmW, num_sms, stream)
-                       : launch_logits<false, true>(p, tmH, tmW, num_sms, stream);
+    int r = bf16 ? launch_logits<true, true>(p, tmH, tmW, num_sms, stream)
+                 : launch_logits<false, true>(p, tmH, tmW, num_sms, stream);
     if (r != kLaunchOk) return finish(r);
-    const char* wchunk = static_cast<const char*>(weight) + static_cast<size_t>(v0) * Dm * 2;
-    // dhidden (fp32, [N, Dm] row-major) (+)= g [N, vc] W[v0 : v0 + vc]
-    if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, Dm, N, vc, &one, wchunk, t16, Dm, g, t16, ldg, v0 == 0 ? &zero : &one,
-                     dh32, CUDA_R_32F, Dm, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return ATTN_ERR_CUDA;
-    // dweight[v0 : v0 + vc] ([vc, Dm] row-major) = g^T hidden
-    char* dwchunk = static_cast<char*>(dweight) + static_cast<size_t>(v0) * Dm * 2;
-    if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, Dm, vc, N, &one, hidden, t16, Dm, g, t16, ldg, &zero, dwchunk, t16,
-                     Dm, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return ATTN_ERR_CUDA;
+    // dhidden (+)= g [N, vc] W[v0 : v0 + vc]: fp32 sum over the chunks in the
+    // workspace, rounded to 16 bits into dhidden by the last chunk
+    LceGemmParams dh{};
+    dh.M = N, dh.N = Dm, dh.n_mt = p.n_rt, dh.n_nt = n_ht, dh.n_kt = (vc + LceGemmGeom::BK - 1) / LceGemmGeom::BK;
+    dh.b_k0 = v0;
+    dh.acc_in = first ? nullptr : dh32;
+    dh.acc_out = last ? nullptr : dh32;
+    dh.out16 = last ? dhidden : nullptr;
+    dh.ldc = Dm, dh.status = status, dh.limit_ns = p.limit_ns;
+    // dweight[v0 : v0 + vc] = g^T hidden
+    LceGemmParams dw{};
+    dw.M = vc, dw.N = Dm, dw.n_mt = (vc + LceGemmGeom::BM - 1) / LceGemmGeom::BM, dw.n_nt = n_ht;
+    dw.n_kt = (N + LceGemmGeom::BK - 1) / LceGemmGeom::BK;
+    dw.b_k0 = 0;
+    dw.out16 = static_cast<char*>(dweight) + static_cast<size_t>(v0) * Dm * 2;
+    dw.ldc = Dm, dw.status = status, dw.limit_ns = p.limit_ns;
+    r = bf16 ? launch_gemm_pair<true>(dh, tmGk, tmWn, dw, tmGm, tmHn, num_sms, stream)
+             : launch_gemm_pair<false>(dh, tmGk, tmWn, dw, tmGm, tmHn, num_sms, stream);
+    if (r != kLaunchOk) return finish(r);
   }
-  const long long n4 = static_cast<long long>(N) * Dm / 4;
-  long long blocks = (n4 + 255) / 256;
-  if (blocks > static_cast<long long>(num_sms) * 8) blocks = static_cast<long long>(num_sms) * 8;
-  if (bf16)
-    lce_cast_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dh32, dhidden, n4);
-  else
-    lce_cast_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dh32, dhidden, n4);
-  return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return ATTN_OK;
 }

@@ -13,7 +13,8 @@
 //     row into lse and loss (the online-softmax merge);
 //   GRAD = true (backward): g = dloss * (exp(z - lse) - [v == target]) for one
 //     chunk of the vocabulary, rounded to 16 bits and written out; the two
-//     products dH += g W_chunk and dW_chunk = g^T H are plain GEMMs.
+//     products dH += g W_chunk and dW_chunk = g^T H follow in
+//     lce_gemm_kernel.cuh.
 //
 // Persistent CTAs walk the tiles vocabulary-major (all row tiles of a
 // vocabulary tile, then the next), so the CTAs running at one time share a few
@@ -275,18 +276,6 @@ __global__ void __launch_bounds__(256)
   lse[row] = l;
   const int t = targets[row];
   loss[row] = (t >= 0 && t < V) ? l - tgt_logit[row] : 0.f;
-}
-
-// fp32 -> 16-bit, four elements per thread.
-template <bool BF16>
-__global__ void __launch_bounds__(256) lce_cast_kernel(const float* __restrict__ src, void* __restrict__ dst,
-                                                       long long n4) {
-  using E = Elem<BF16>;
-  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * 256) {
-    const float4 v = reinterpret_cast<const float4*>(src)[i];
-    reinterpret_cast<uint2*>(dst)[i] = make_uint2(E::pack(v.x, v.y), E::pack(v.z, v.w));
-  }
 }
 
 }  // namespace gbattn

@@ -453,7 +453,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // 1.5 * 2^23 rounds x to an integer held in the low mantissa bits), then a
 // degree-3 polynomial for 2^f whose coefficients minimise the maximum
 // relative error on [-1/2, 1/2] (fitted by a Remez exchange; max relative
-// error 7.5e-5, below the 2^-9 half-ulp of bf16 and the 2^-11 of fp16 that P
+// error 7.5e-5, below the 2^-8 relative rounding error of bf16 and the 2^-11 of fp16 that P
 // is rounded to), and the exponent n added to the result's exponent field.
 // Inputs below -126 are clamped there.  At the bottom edge, x in [-126,
 // -125.9999], the polynomial's value just below 1 meets the smallest exponent

@@ -27,14 +27,15 @@
  *   one (max, sum) pair per row and 256-entry vocabulary tile there; the
  *   backward keeps one chunk of g (16384 vocabulary entries, 16-bit) and an
  *   fp32 dhidden accumulator.
- * Products: the logits tiles and their epilogues run in this library's
- *   tcgen05 kernels; the backward's two plain products per vocabulary chunk
- *   (dhidden += g W_chunk, dweight_chunk = g^T hidden) are cuBLAS GEMMs with
- *   fp32 accumulation.  The first call on a device creates a cuBLAS handle.
+ * Products: every product runs in this library's tcgen05 kernels: the
+ *   logits tiles with their epilogues, and the backward's two products per
+ *   vocabulary chunk (dhidden += g W_chunk with an fp32 sum across chunks,
+ *   rounded to 16 bits once at the end; dweight_chunk = g^T hidden, fp32
+ *   accumulation, rounded to 16 bits).  No other library is called.
  * Errors: a null or misaligned pointer, N, Dm or V < 1, a bad dtype or a small
  *   workspace is ATTN_ERR_INVALID_ARG; Dm % 64 != 0 is ATTN_ERR_UNSUPPORTED;
- *   a failed launch or cuBLAS call is ATTN_ERR_CUDA.  A target >= V is
- *   treated like a negative one (ignored row).
+ *   a failed launch is ATTN_ERR_CUDA.  A target >= V is treated like a
+ *   negative one (ignored row).
  */
 #ifndef GBLCE_H_
 #define GBLCE_H_

@@ -84,27 +84,50 @@ def forward_rows(h_rows: np.ndarray, t_rows: np.ndarray, w_chunk, V: int):
     return np.where(valid, lse - zt, 0.0), lse
 
 
-def dhidden_rows(h_rows, t_rows, dloss_rows, w_chunk, V: int, chunk: int = 16384):
-    """dH for the given rows: (dloss * (softmax - onehot)) W."""
+def grad_logits_rows(h_rows, t_rows, dloss_rows, w_chunk, V: int, chunk: int = 16384) -> np.ndarray:
+    """g = dloss * (softmax - onehot) for the given rows, [n, V]."""
     z = logits_rows(h_rows, w_chunk, V, chunk)
     _, lse = forward_rows(h_rows, t_rows, w_chunk, V)
     g = np.exp(z - lse[:, None])
     valid = t_rows >= 0
     g[np.arange(len(t_rows))[valid], t_rows[valid]] -= 1.0
     g *= np.where(valid, dloss_rows, 0.0)[:, None]
+    return g
+
+
+def dhidden_rows(h_rows, t_rows, dloss_rows, w_chunk, V: int, chunk: int = 16384):
+    """dH for the given rows: (dloss * (softmax - onehot)) W."""
+    g = grad_logits_rows(h_rows, t_rows, dloss_rows, w_chunk, V, chunk)
     out = np.zeros((h_rows.shape[0], h_rows.shape[1]))
     for v0 in range(0, V, chunk):
         out += g[:, v0:v0 + chunk] @ w_chunk(v0, min(V, v0 + chunk))
     return out
 
 
-def dweight_entries(h: np.ndarray, t: np.ndarray, dloss: np.ndarray, w_chunk, V: int, entries):
-    """dW for the given vocabulary entries (needs every row's lse)."""
+def lse_rows(h: np.ndarray, w_chunk, V: int, block: int = 1024) -> np.ndarray:
+    """The natural-log lse of every row of h, a block of rows at a time (each
+    row's whole logits row is formed, as in forward_rows)."""
+    out = np.empty(h.shape[0])
+    for r0 in range(0, h.shape[0], block):
+        z = logits_rows(h[r0:r0 + block], w_chunk, V)
+        m = z.max(axis=1)
+        out[r0:r0 + block] = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    return out
+
+
+def grad_logits_entries(h: np.ndarray, t: np.ndarray, dloss: np.ndarray, w_chunk, V: int, entries) -> np.ndarray:
+    """Columns `entries` of g for every row, [N, len(entries)] (needs every
+    row's lse)."""
     entries = np.asarray(entries)
-    _, lse = forward_rows(h, t, w_chunk, V)
+    lse = lse_rows(h, w_chunk, V)
     z = h @ np.concatenate([w_chunk(v, v + 1) for v in entries]).T  # [N, len(entries)]
     g = np.exp(z - lse[:, None])
     valid = t >= 0
     g -= (t[:, None] == entries[None, :]) & valid[:, None]
     g *= np.where(valid, dloss, 0.0)[:, None]
-    return g.T @ h
+    return g
+
+
+def dweight_entries(h: np.ndarray, t: np.ndarray, dloss: np.ndarray, w_chunk, V: int, entries):
+    """dW for the given vocabulary entries: g[:, entries]^T H."""
+    return grad_logits_entries(h, t, dloss, w_chunk, V, entries).T @ h

@@ -38,7 +38,7 @@ def test_traffic_file_lines_are_well_formed():
 def test_clock_window_keeps_samples_inside_the_region():
     c = bench.ClockSampler(0)
     c.proc = object()  # stands in for the running tool
-    row = lambda mhz, cap: ["0", str(mhz), "2070", "500", "0x0", "Not Active", "Not Active", "Not Active", cap]
+    row = lambda mhz, cap: ["t", str(mhz), "2070", "500", "0x0", "Not Active", "Not Active", "Not Active", cap]
     c.samples = [(0.9, row(1000, "Not Active")), (1.02, row(2070, "Not Active")), (1.04, row(1900, "Active")),
                  (1.2, row(1500, "Not Active"))]
     c.t_begin, c.t_end = 1.0, 1.03

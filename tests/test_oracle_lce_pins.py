@@ -180,3 +180,9 @@ def test_chunked_helpers_match_whole_problem():
                                rtol=1e-12, atol=1e-13)
     ent = [0, 3, 36]
     np.testing.assert_allclose(L.dweight_entries(h, t, dloss, chunk, 37, ent), dw[ent], rtol=1e-12, atol=1e-13)
+    g = L.grad_logits(h, w, t, lse, dloss)
+    np.testing.assert_allclose(L.grad_logits_rows(h[rows], t[rows], dloss[rows], chunk, 37, chunk=10), g[rows],
+                               rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(L.grad_logits_entries(h, t, dloss, chunk, 37, ent), g[:, ent], rtol=1e-12,
+                               atol=1e-14)
+    np.testing.assert_allclose(L.lse_rows(h, chunk, 37, block=4), lse, rtol=1e-13)
