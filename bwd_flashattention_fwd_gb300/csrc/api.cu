@@ -535,14 +535,12 @@ __global__ void attn_wait_probe_kernel(int* status, uint64_t limit_ns) {
   __syncthreads();
 }
 
-// Reads the status word at `p` (device memory) and clears it: 1 if a wait had
-// run out, 0 if not, -1 on a CUDA error.  Neither call allocates.
-int take_status_word(int* p) {
-  int h = 0;
-  if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
-  if (h == 0) return 0;
-  if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return -1;
-  return 1;
+// Reads the status word at `p` (device memory) into *code and clears it;
+// false on a CUDA error.  Neither call allocates.
+bool take_status_word(int* p, int* code) {
+  *code = 0;
+  if (cudaMemcpy(code, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return false;
+  return *code == 0 || cudaMemset(p, 0, sizeof(int)) == cudaSuccess;
 }
 
 }  // namespace probe
@@ -566,15 +564,17 @@ extern "C" attn_status_t attn_last_device_status(cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(g_mu);
     p = g_status[dev];
   }
-  // the allocating entry points' word, then the word in attn_bwd_noalloc's scratch
-  int timed_out = 0;
+  // the allocating entry points' word, then the word in attn_bwd_noalloc's
+  // scratch; a failed index check (debug build) outranks a timeout
+  attn_status_t st = ATTN_OK;
   for (int* w : {p, noalloc_status_word(dev)}) {
+    int code = 0;
     if (!w) continue;
-    const int r = probe::take_status_word(w);
-    if (r < 0) return ATTN_ERR_CUDA;
-    timed_out |= r;
+    if (!probe::take_status_word(w, &code)) return ATTN_ERR_CUDA;
+    if (code >= kDevBoundsBase) st = ATTN_ERR_DEVICE_CHECK;
+    else if (code != 0 && st == ATTN_OK) st = ATTN_ERR_TIMEOUT;
   }
-  return timed_out ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  return st;
 }
 
 extern "C" const char* attn_status_string(attn_status_t s) {
@@ -584,6 +584,7 @@ extern "C" const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_DEVICE_CHECK: return "ATTN_ERR_DEVICE_CHECK";
     default: return "ATTN_ERR_UNKNOWN";
   }
 }

@@ -114,10 +114,15 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
   static_assert(BK == kMaskBlock && 2 * BQ == kMaskBlock, "key tile = mask block, query tile = half a block");
   // query tile qt is computed (block mask)
-  auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
+  auto keep = [&](int qt) { return !MASKED || mask_keep(p, qt >> 1, kt); };
   // (query head, computed query tile) iterations; every warp counts them itself
   const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / dq / lse /
+  // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  [[maybe_unused]] const size_t n_krows = static_cast<size_t>(p.B) * p.Hkv * p.Lk;
+  [[maybe_unused]] const size_t n_kvbuf = (static_cast<size_t>(p.B) * p.Hkv - 1) * p.kv_pitch + p.Lk;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -174,8 +179,8 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
         const int c = lane + 32 * t;
         const int qi = q0 + c;
         const size_t row = static_cast<size_t>(zq) * p.Lq + qi;
-        nlse_s[s][c] = qi < p.Lq ? -p.lse[row] : -INFINITY;
-        dlt_s[s][c] = qi < p.Lq ? p.delta[row] : 0.f;
+        nlse_s[s][c] = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 14) ? -p.lse[row] : -INFINITY;
+        dlt_s[s][c] = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 15) ? p.delta[row] : 0.f;
       }
       mbar_arrive(smem_u32(&bar_stfull[s]));
       qtile = qw.next(qtile);
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (kj < p.Lk) x = src[v];
+        if (kj < p.Lk && dbg_in_range(kin * D + half * HALF + 8 * v, 8, n_kvbuf * D, p.status, 16)) x = src[v];
         ka[4 * v + 0] = x.x, ka[4 * v + 1] = x.y, ka[4 * v + 2] = x.z, ka[4 * v + 3] = x.w;
       }
       // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
@@ -385,12 +390,14 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept query tile: dK = dV = 0
       }
-      if (kj < p.Lk) store_row32<BF16>(dkrow + c * 32, rr, p.scale);
+      if (kj < p.Lk && dbg_in_range(krow * D + c * 32, 32, n_krows * D, p.status, 17))
+        store_row32<BF16>(dkrow + c * 32, rr, p.scale);
       if (n_iter > 0) {
         tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
         tmem_ld_wait(rr);
       }
-      if (kj < p.Lk) store_row32<BF16>(dvrow + c * 32, rr, 1.f);
+      if (kj < p.Lk && dbg_in_range(krow * D + c * 32, 32, n_krows * D, p.status, 18))
+        store_row32<BF16>(dvrow + c * 32, rr, 1.f);
     }
   }
 

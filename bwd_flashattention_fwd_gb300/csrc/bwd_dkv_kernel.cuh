@@ -125,9 +125,14 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
   // query tile qt is computed (block mask: the CTA's 128 keys are one mask
   // column, a 64-row query tile half a mask row)
-  auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
+  auto keep = [&](int qt) { return !MASKED || mask_keep(p, qt >> 1, kt); };
   const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);  // (query head, query tile) iterations
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / dq / lse /
+  // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  [[maybe_unused]] const size_t n_krows = static_cast<size_t>(p.B) * p.Hkv * p.Lk;
+  [[maybe_unused]] const size_t n_kvbuf = (static_cast<size_t>(p.B) * p.Hkv - 1) * p.kv_pitch + p.Lk;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -270,7 +275,9 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint4 x = make_uint4(0u, 0u, 0u, 0u);
-          if (kj < p.Lk) x = src[c * 4 + v];
+          if (kj < p.Lk && dbg_in_range((static_cast<size_t>(bhk) * p.kv_pitch + kj) * D + half * 128 + 8 * (c * 4 + v),
+                                        8, n_kvbuf * D, p.status, 19))
+            x = src[c * 4 + v];
           t16[4 * v + 0] = x.x, t16[4 * v + 1] = x.y, t16[4 * v + 2] = x.z, t16[4 * v + 3] = x.w;
         }
         tmem_st16(tmem + lrow + Gm::V_COL + half * 64 + c * 16, t16);
@@ -282,7 +289,8 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     // delta of query half*32 + lane of a query tile (0 past Lq)
     auto delta_of = [&](int qt, int gq) {
       const int qi = qt * BQ + half * 32 + lane;
-      return qi < p.Lq ? p.delta[static_cast<size_t>(b * p.Hq + hk * p.G + gq) * p.Lq + qi] : 0.f;
+      const size_t row = static_cast<size_t>(b * p.Hq + hk * p.G + gq) * p.Lq + qi;
+      return qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 20) ? p.delta[row] : 0.f;
     };
     int gi = 0, qtile = qw.first(qt_start);
     float dl = n_iter > 0 ? delta_of(qtile, gi) : 0.f;
@@ -344,7 +352,8 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
         for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept query tile: dK = 0
       }
-      if (kj < p.Lk) store_row32<BF16>(dst + c * 32, rr, p.scale);
+      if (kj < p.Lk && dbg_in_range((static_cast<size_t>(bhk) * p.Lk + kj) * D + c * 32, 32, n_krows * D, p.status, 21))
+        store_row32<BF16>(dst + c * 32, rr, p.scale);
     }
   }
 
@@ -417,9 +426,14 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
   const int qt_start = CAUSAL ? max(0, k0 - p.off) / BQ : 0;
   // query tile qt is computed (block mask: the CTA's 128 keys are one mask
   // column, a 64-row query tile half a mask row)
-  auto keep = [&](int qt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt >> 1, kt); };
+  auto keep = [&](int qt) { return !MASKED || mask_keep(p, qt >> 1, kt); };
   const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);  // (query head, query tile) iterations
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / dq / lse /
+  // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  [[maybe_unused]] const size_t n_krows = static_cast<size_t>(p.B) * p.Hkv * p.Lk;
+  [[maybe_unused]] const size_t n_kvbuf = (static_cast<size_t>(p.B) * p.Hkv - 1) * p.kv_pitch + p.Lk;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -560,7 +574,9 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint4 x = make_uint4(0u, 0u, 0u, 0u);
-          if (kj < p.Lk) x = src[c * 4 + v];
+          if (kj < p.Lk && dbg_in_range((static_cast<size_t>(bhk) * p.kv_pitch + kj) * D + half * 128 + 8 * (c * 4 + v),
+                                        8, n_kvbuf * D, p.status, 22))
+            x = src[c * 4 + v];
           t16[4 * v + 0] = x.x, t16[4 * v + 1] = x.y, t16[4 * v + 2] = x.z, t16[4 * v + 3] = x.w;
         }
         tmem_st16(tmem + lrow + Gm::K_COL + half * 64 + c * 16, t16);
@@ -572,7 +588,8 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     // -lse of query half*32 + lane of a query tile (-inf past Lq)
     auto nlse_of = [&](int qt, int gq) {
       const int qi = qt * BQ + half * 32 + lane;
-      return qi < p.Lq ? -p.lse[static_cast<size_t>(b * p.Hq + hk * p.G + gq) * p.Lq + qi] : -INFINITY;
+      const size_t row = static_cast<size_t>(b * p.Hq + hk * p.G + gq) * p.Lq + qi;
+      return qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 23) ? -p.lse[row] : -INFINITY;
     };
     int gi = 0, qtile = qw.first(qt_start);
     float nl = n_iter > 0 ? nlse_of(qtile, gi) : 0.f;
@@ -643,7 +660,8 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
         for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept query tile: dV = 0
       }
-      if (kj < p.Lk) store_row32<BF16>(dst + c * 32, rr, 1.f);
+      if (kj < p.Lk && dbg_in_range((static_cast<size_t>(bhk) * p.Lk + kj) * D + c * 32, 32, n_krows * D, p.status, 24))
+        store_row32<BF16>(dst + c * 32, rr, 1.f);
     }
   }
 

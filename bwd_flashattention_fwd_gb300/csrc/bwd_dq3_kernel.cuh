@@ -138,10 +138,15 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   };
   static_assert(BQ == kMaskBlock && 2 * BK == kMaskBlock, "query tile = mask block, key tile = half a block");
   // key tile j of query tile qt is computed (block mask)
-  auto keep = [&](int qt, int j) { return !MASKED || mask_keep(p.bmask, p.nkb, qt, j >> 1); };
+  auto keep = [&](int qt, int j) { return !MASKED || mask_keep(p, qt, j >> 1); };
   // number of computed key tiles of query tile qt (warp-collective)
   auto n_kept = [&](int qt) { return count_kept<MASKED>([&](int j) { return keep(qt, j); }, 0, n_kv_of(qt)); };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / dq / lse /
+  // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  [[maybe_unused]] const size_t n_krows = static_cast<size_t>(p.B) * p.Hkv * p.Lk;
+  [[maybe_unused]] const size_t n_kvbuf = (static_cast<size_t>(p.B) * p.Hkv - 1) * p.kv_pitch + p.Lk;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -377,8 +382,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       const int n_kv = n_kv_of(it.qt);
       const int nk = n_kept(it.qt);
       const size_t row = static_cast<size_t>(it.bh) * p.Lq + qi;
-      const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
-      const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
+      const float lse_r = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 7) ? p.lse[row] : 0.f;
+      const float dlt_r = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 8) ? p.delta[row] : 0.f;
       const uint64_t nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
       const int lim = CAUSAL ? min(qi + p.off, p.Lk - 1) : p.Lk - 1;
       auto kw = kept_walk<MASKED>([&](int j) { return keep(it.qt, j); }, n_kv);
@@ -456,7 +461,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept key tile: dQ = 0
         }
-        if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+        if (qi < p.Lq && dbg_in_range(row * D + c * 32, 32, n_qrows * D, p.status, 9))
+          store_row32<BF16>(dqrow + c * 32, rr, p.scale);
       }
       // The next item's first dQ MMA overwrites these columns; it is issued
       // after this thread's next dS arrival, which follows these loads.

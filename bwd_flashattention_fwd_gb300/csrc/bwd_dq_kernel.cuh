@@ -104,9 +104,14 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
   static_assert(!(MASKED && DECODE), "no block mask on the decode path");
   static_assert(BQ == kMaskBlock && kMaskBlock % BK == 0, "query tile = mask block");
   // key tile jt is computed (block mask), and the number of computed tiles (warp-collective)
-  auto keep = [&](int jt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt, jt * BK / kMaskBlock); };
+  auto keep = [&](int jt) { return !MASKED || mask_keep(p, qt, jt * BK / kMaskBlock); };
   const int nk = count_kept<MASKED>(keep, 0, n_kv);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / dq / lse /
+  // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  [[maybe_unused]] const size_t n_krows = static_cast<size_t>(p.B) * p.Hkv * p.Lk;
+  [[maybe_unused]] const size_t n_kvbuf = (static_cast<size_t>(p.B) * p.Hkv - 1) * p.kv_pitch + p.Lk;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -242,8 +247,8 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
     const size_t row = static_cast<size_t>(bh) * p.Lq + qi;
-    const float lse_r = qi < p.Lq ? p.lse[row] : 0.f;
-    const float dlt_r = qi < p.Lq ? p.delta[row] : 0.f;
+    const float lse_r = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 10) ? p.lse[row] : 0.f;
+    const float dlt_r = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 11) ? p.delta[row] : 0.f;
     const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
     auto kw = kept_walk<MASKED>(keep, n_kv);
     int jt = kw.first(0);  // key tile of the j-th computed tile
@@ -284,13 +289,16 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     tc_fence_after_sync();
     if constexpr (DECODE) {
       // this split's share of row bh * Lq + qi, unscaled
-      float* dst = p.ws + ((static_cast<size_t>(blockIdx.y) * gridDim.x + bh) * p.Lq + qi) * D;
+      const size_t x = (static_cast<size_t>(blockIdx.y) * gridDim.x + bh) * p.Lq + qi;
+      const size_t n_ws_rows = static_cast<size_t>(gridDim.y) * gridDim.x * p.Lq;  // splits x packed rows
+      float* dst = p.ws + x * D;
 #pragma unroll 1
       for (int c = half; c < D / 32; c += 2) {
         uint32_t rr[32];
         tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
         tmem_ld_wait(rr);
-        if (qi < p.Lq) store_row32_f32(dst + c * 32, rr, 1.f);
+        if (qi < p.Lq && dbg_in_range(x * D + c * 32, 32, n_ws_rows * D, p.status, 12))
+          store_row32_f32(dst + c * 32, rr, 1.f);
       }
     } else {
       typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
@@ -304,7 +312,8 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept key tile: dQ = 0
         }
-        if (qi < p.Lq) store_row32<BF16>(dqrow + c * 32, rr, p.scale);
+        if (qi < p.Lq && dbg_in_range(row * D + c * 32, 32, n_qrows * D, p.status, 13))
+          store_row32<BF16>(dqrow + c * 32, rr, p.scale);
       }
     }
   }

@@ -135,6 +135,11 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
   const int t0 = static_cast<int>(blockIdx.y) * p.split_tiles;
   const int n_t = min(p.n_ktiles - t0, p.split_tiles);  // key tiles t0 .. t0 + n_t - 1
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / dq / lse /
+  // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
+  [[maybe_unused]] const size_t n_krows = static_cast<size_t>(p.B) * p.Hkv * p.Lk;
+  [[maybe_unused]] const size_t n_kvbuf = (static_cast<size_t>(p.B) * p.Hkv - 1) * p.kv_pitch + p.Lk;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -176,8 +181,8 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
     for (int t = 0; t < RQ / 32; ++t) {
       const int c = lane + 32 * t;
       const size_t row = static_cast<size_t>(bhk) * p.Lq + c;
-      nlse_s[c] = c < p.Lq ? -p.lse[row] : -INFINITY;
-      dlt_s[c] = c < p.Lq ? p.delta[row] : 0.f;
+      nlse_s[c] = c < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 25) ? -p.lse[row] : -INFINITY;
+      dlt_s[c] = c < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 26) ? p.delta[row] : 0.f;
     }
     mbar_arrive(smem_u32(&bar_q));
     for (int i = 0; i < n_t; ++i) {
@@ -307,10 +312,12 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
         uint32_t rr[32];
         tmem_ld32(tmem + lrow + Gm::DK_COL + c * 32, rr);
         tmem_ld_wait(rr);
-        if (kj < p.Lk) store_row32<BF16>(dkrow + c * 32, rr, p.scale);
+        if (kj < p.Lk && dbg_in_range(krow * D + c * 32, 32, n_krows * D, p.status, 27))
+          store_row32<BF16>(dkrow + c * 32, rr, p.scale);
         tmem_ld32(tmem + lrow + Gm::DV_COL + c * 32, rr);
         tmem_ld_wait(rr);
-        if (kj < p.Lk) store_row32<BF16>(dvrow + c * 32, rr, 1.f);
+        if (kj < p.Lk && dbg_in_range(krow * D + c * 32, 32, n_krows * D, p.status, 28))
+          store_row32<BF16>(dvrow + c * 32, rr, 1.f);
       }
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_accfree));

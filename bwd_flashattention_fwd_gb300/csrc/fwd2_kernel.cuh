@@ -113,13 +113,15 @@ __global__ void __launch_bounds__(352, 1)
   const int nqb = (p.Lq + kMaskBlock - 1) / kMaskBlock;
   // key tile j is visible to query tile t of pair pt as far as the block mask goes
   auto keep_t = [&](int pt, int t, int j) {
-    return !MASKED || (2 * pt + t < nqb && mask_keep(p.bmask, p.nkb, 2 * pt + t, j >> 1));
+    return !MASKED || (2 * pt + t < nqb && mask_keep(p, 2 * pt + t, j >> 1));
   };
   // key tile j is computed for the pair (either query tile keeps it)
   auto keep = [&](int pt, int j) { return !MASKED || keep_t(pt, 0, j) || keep_t(pt, 1, j); };
   // computed key tiles of pair pt (warp-collective)
   auto n_kept = [&](int pt) { return count_kept<MASKED>([&](int j) { return keep(pt, j); }, 0, n_kv_of(pt)); };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / o / lse
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -392,9 +394,11 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
+        if (qi < p.Lq && dbg_in_range((static_cast<size_t>(bh) * p.Lq + qi) * D + c * 32, 32, n_qrows * D, p.status, 1))
+          store_row32<BF16>(orow + c * 32, rr, inv_l);
       }
-      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
+      if (qi < p.Lq && dbg_in_range(static_cast<size_t>(bh) * p.Lq + qi, 1, n_qrows, p.status, 2))
+        p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
       // the next item's first P V overwrites O_t after this warpgroup's next
       // P arrival, which follows these loads
       tc_fence_before_sync();

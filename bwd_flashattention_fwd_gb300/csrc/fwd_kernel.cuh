@@ -95,9 +95,11 @@ __global__ void __launch_bounds__(192, 1)
   static_assert(!(MASKED && DECODE), "no block mask on the decode path");
   static_assert(BQ == kMaskBlock && kMaskBlock % BK == 0, "query tile = mask block");
   // key tile jt is computed (block mask), and the number of computed tiles (warp-collective)
-  auto keep = [&](int jt) { return !MASKED || mask_keep(p.bmask, p.nkb, qt, jt * BK / kMaskBlock); };
+  auto keep = [&](int jt) { return !MASKED || mask_keep(p, qt, jt * BK / kMaskBlock); };
   const int nk = count_kept<MASKED>(keep, 0, n_kv);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // extents for the debug build's index checks: rows of q / o / lse
+  [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -293,14 +295,16 @@ __global__ void __launch_bounds__(192, 1)
       const bool empty = !(l > 0.f);
       const float inv_l = empty ? 0.f : 1.f / l;
       const size_t x = (static_cast<size_t>(blockIdx.y) * gridDim.x + bh) * p.Lq + qi;
+      const size_t n_ws_rows = static_cast<size_t>(gridDim.y) * gridDim.x * p.Lq;  // splits x packed rows
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
         tmem_ld32(tmem + lrow + Gm::O_COL + c * 32, rr);
         tmem_ld_wait(rr);
-        if (qi < p.Lq) store_row32_f32(p.ws + x * D + c * 32, rr, inv_l);
+        if (qi < p.Lq && dbg_in_range(x * D + c * 32, 32, n_ws_rows * D, p.status, 3))
+          store_row32_f32(p.ws + x * D + c * 32, rr, inv_l);
       }
-      if (qi < p.Lq) p.ws_lse[x] = empty ? -INFINITY : m + log2f(l);
+      if (qi < p.Lq && dbg_in_range(x, 1, n_ws_rows, p.status, 4)) p.ws_lse[x] = empty ? -INFINITY : m + log2f(l);
     } else {
       const bool empty = MASKED && !(l > 0.f);  // the row saw no key: O = 0, lse = +inf
       const float inv_l = empty ? 0.f : 1.f / l;
@@ -316,9 +320,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (qi < p.Lq) store_row32<BF16>(orow + c * 32, rr, inv_l);
+        if (qi < p.Lq && dbg_in_range((static_cast<size_t>(bh) * p.Lq + qi) * D + c * 32, 32, n_qrows * D, p.status, 5))
+          store_row32<BF16>(orow + c * 32, rr, inv_l);
       }
-      if (qi < p.Lq) p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
+      if (qi < p.Lq && dbg_in_range(static_cast<size_t>(bh) * p.Lq + qi, 1, n_qrows, p.status, 6))
+        p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
     }
   }
 

@@ -11,11 +11,36 @@
 namespace gbattn {
 
 // Status codes a kernel may record in the device status word (the first
-// nonzero code wins).  Values >= 100 identify which bounded wait ran out.
+// nonzero code wins).  Values 100..199 identify which bounded wait ran out,
+// values >= 200 which index check of a debug build failed.
 enum : int {
   kDevOk = 0,
   kDevTimeoutBase = 100,
+  kDevBoundsBase = 200,
 };
+
+// Debug build (compiled with -DGBATTN_DEBUG_CHECKS): every plain global load
+// and store of the kernels first checks that the elements it touches,
+// [first, first + count), lie inside the tensor's extent [0, extent).  A
+// failed check records kDevBoundsBase + site in the status word and the
+// access is skipped -- nothing traps, and the host reads the code through
+// attn_last_device_status.  In the normal build the check is a constant
+// `true` and compiles away.
+#ifdef GBATTN_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ bool dbg_in_range(size_t first, size_t count, size_t extent, int* status, int site) {
+  if constexpr (!kDebugChecks) {
+    return true;
+  } else {
+    if (first + count <= extent && first + count >= first) return true;
+    if (status) atomicCAS(status, 0, kDevBoundsBase + site);
+    return false;
+  }
+}
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxDynSmem = 232448;                       // 227 KB per CTA on sm_103a
@@ -75,9 +100,13 @@ __device__ __forceinline__ void store_row32_f32(float* dst, const uint32_t (&r)[
                        __uint_as_float(r[4 * q + 2]) * mul, __uint_as_float(r[4 * q + 3]) * mul);
 }
 
-// Block-mask entry (query block qb, key block kb); nonzero keeps the pair.
-__device__ __forceinline__ bool mask_keep(const uint8_t* m, int nkb, int qb, int kb) {
-  return __ldg(m + static_cast<size_t>(qb) * nkb + kb) != 0;
+// Block-mask entry (query block qb, key block kb) of the launch parameters
+// p (FwdParams or BwdParams); nonzero keeps the pair.
+template <class Params>
+__device__ __forceinline__ bool mask_keep(const Params& p, int qb, int kb) {
+  const size_t i = static_cast<size_t>(qb) * p.nkb + kb;
+  const size_t n = static_cast<size_t>((p.Lq + kMaskBlock - 1) / kMaskBlock) * p.nkb;
+  return dbg_in_range(i, 1, n, p.status, 40) && __ldg(p.bmask + i) != 0;
 }
 
 // Walks the indices x in [lo, hi) for which keep(x) holds, in increasing

@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(LceGemmGeom::NUM_THREADS, 1)
         tmem_ld32(acc + c * 32, rr);
         tmem_ld_wait(rr);
         const int col = nt * BN + c * 32;
-        if (row < p.M && col < p.N) {
+        if (row < p.M && col < p.N &&
+            dbg_in_range(static_cast<size_t>(row) * p.ldc + col, 32, static_cast<size_t>(p.M) * p.ldc, p.status, 46)) {
           const size_t off = static_cast<size_t>(row) * p.ldc + col;
           if (p.acc_in) {
             const float4* src = reinterpret_cast<const float4*>(p.acc_in + off);

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
       const int row = rt * BM + r;
       const int tv0 = p.v0 + vt * BN;  // vocabulary entry of column 0
       const int n_valid = min(BN, p.v_end - tv0);
-      const int tgt = row < p.N ? p.targets[row] : -1;
+      const int tgt = row < p.N && dbg_in_range(row, 1, p.N, p.status, 41) ? p.targets[row] : -1;
       mbar_wait(smem_u32(&bar_accfull[b]), (u >> 1) & 1, g, kDevTimeoutBase + 44);
       __syncwarp();
       tc_fence_after_sync();
@@ -208,13 +208,15 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
         // accumulator read: the MMA warp may reuse it
         tc_fence_before_sync();
         mbar_arrive(smem_u32(&bar_accempty[b]));
-        if (row < p.N) {
+        if (row < p.N && dbg_in_range(static_cast<size_t>(vt) * p.N + row, 1, static_cast<size_t>(p.n_vt) * p.N,
+                                      p.status, 42)) {
           p.part[static_cast<size_t>(vt) * p.N + row] = make_float2(m, s);
           if (tc >= 0 && tc < n_valid) p.tgt_logit[row] = zt;
         }
       } else {
-        const float nl2 = row < p.N ? -p.lse[row] * kLog2e : 0.f;
-        const float d = (row < p.N && tgt >= 0 && tgt < p.V) ? p.dloss[row] : 0.f;
+        const float nl2 = row < p.N && dbg_in_range(row, 1, p.N, p.status, 43) ? -p.lse[row] * kLog2e : 0.f;
+        const float d = (row < p.N && tgt >= 0 && tgt < p.V && dbg_in_range(row, 1, p.N, p.status, 44)) ? p.dloss[row]
+                                                                                                     : 0.f;
         const int tc = tgt - tv0;
         typename E::T* grow = reinterpret_cast<typename E::T*>(p.g) +
                               static_cast<size_t>(row) * p.ldg + (tv0 - p.v0);
@@ -235,7 +237,8 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
             if (c0 + 1 >= n_valid) g1 = 0.f;
             pk[i] = E::pack(g0, g1);
           }
-          if (row < p.N) {
+          if (row < p.N && dbg_in_range(static_cast<size_t>(row) * p.ldg + (tv0 - p.v0) + c * 32, 32,
+                                        static_cast<size_t>(p.N) * p.ldg, p.status, 45)) {
             uint4* dst = reinterpret_cast<uint4*>(grow + c * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);

@@ -89,6 +89,28 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, const W
   mbar_wait_slow(bar, parity, g, code);
 }
 
+// Bounded wait until a shared-memory counter that another warp of the CTA
+// raises reaches v (the same limit and abort rules as mbar_wait).  A counter
+// that only grows cannot confuse one wait with a later one, which an
+// mbarrier's two phases can when its arrivals run ahead of the waiter.
+static __device__ __noinline__ void wait_count_slow(const volatile int* c, int v, const WaitGuard& g, int code) {
+  const uint64_t t0 = global_timer_ns();
+  uint32_t it = 0;
+  while (*c < v) {
+    if (*g.abort_flag) return;
+    if ((++it & 63u) == 0u && global_timer_ns() - t0 > g.limit_ns) {
+      if (g.status) atomicCAS(g.status, 0, code);
+      *g.abort_flag = 1;
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void wait_count(const volatile int* c, int v, const WaitGuard& g, int code) {
+  if (*c >= v) return;
+  wait_count_slow(c, v, g, code);
+}
+
 // Bounded wait that ignores the abort flag.  Used only at the end of a CTA, so
 // that no asynchronous copy or MMA is still in flight when the CTA releases its
 // shared and tensor memory.  Its limit is fixed and generous (4 s), separate

@@ -15,12 +15,15 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgbattn.so")
+# the debug build: the same kernels with index checks (GBATTN_DEBUG_CHECKS)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libgbattn_debug.so")
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
 ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_DEVICE_CHECK = 5
 ATTN_DTYPE_FP16 = 0
 ATTN_DTYPE_BF16 = 1
 
@@ -38,11 +41,15 @@ class AttnError(RuntimeError):
         super().__init__(f"{call} failed: {status_string(status)} ({status})")
 
 
-def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libgbattn.so once and declare its C signatures."""
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libgbattn.so once and declare its C signatures.  With
+    GBATTN_DEBUG=1 in the environment the process uses the debug build
+    (libgbattn_debug.so) instead."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = DEBUG_LIB_PATH if os.environ.get("GBATTN_DEBUG") == "1" else LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is not built; run bwd_flashattention_fwd_gb300.build.build() (or __graft_entry__.build())"

@@ -28,6 +28,12 @@
  *   an error, never a silent change of implementation.  Device-side waits are
  *   bounded; a wait that runs out records ATTN_ERR_TIMEOUT in a device status
  *   word that attn_last_device_status() reports.
+ * Debug build.  libgbattn_debug.so (the same sources compiled with
+ *   GBATTN_DEBUG_CHECKS) checks every plain global load and store of its
+ *   kernels against the extent of the tensor it addresses; an index outside
+ *   is skipped, not performed, and recorded, so attn_last_device_status()
+ *   returns ATTN_ERR_DEVICE_CHECK.  Nothing traps.  Same interface, same
+ *   results, slower.
  */
 #ifndef GBATTN_H_
 #define GBATTN_H_
@@ -45,7 +51,8 @@ typedef enum {
   ATTN_ERR_INVALID_ARG = 1,
   ATTN_ERR_UNSUPPORTED = 2,
   ATTN_ERR_CUDA = 3,
-  ATTN_ERR_TIMEOUT = 4
+  ATTN_ERR_TIMEOUT = 4,
+  ATTN_ERR_DEVICE_CHECK = 5 /* debug build only: a kernel's index check failed */
 } attn_status_t;
 
 typedef enum { ATTN_DTYPE_FP16 = 0, ATTN_DTYPE_BF16 = 1 } attn_dtype_t;
@@ -231,8 +238,9 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
  * Synchronises `stream`, then reports and clears the device status words of the
  * current device (the one the entry points above share, and the one in
  * attn_bwd_noalloc's scratch): ATTN_ERR_TIMEOUT if a bounded device-side wait
- * ran out in a kernel since the last call, ATTN_ERR_CUDA if the stream
- * reported an error, ATTN_OK otherwise.  A failure is a typed error, never a
+ * ran out in a kernel since the last call, ATTN_ERR_DEVICE_CHECK if an index
+ * check of the debug build failed, ATTN_ERR_CUDA if the stream reported an
+ * error, ATTN_OK otherwise.  A failure is a typed error, never a
  * silent change of behaviour ("When the Bottleneck Moved", section 3: what
  * the implementation does not support fails with a typed error).
  */

@@ -93,7 +93,7 @@ def test_delta_rejects_on_host(lib):
 
 def test_status_strings(lib):
     names = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
-             4: "ATTN_ERR_TIMEOUT"}
+             4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_DEVICE_CHECK"}
     for code, name in names.items():
         assert gbattn.status_string(code) == name
     assert gbattn.status_string(99) == "ATTN_ERR_UNKNOWN"
