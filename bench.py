@@ -448,6 +448,7 @@ def run_ours(args):
     if args.decode:
         if bm is not None or kv_cap:
             raise SystemExit("--decode takes neither --block-mask nor --kv-capacity")
+        split_names, split_calls = None, None
         ws_dec = gbattn.decode_workspace(q, k)
         phase_names = ("fwd", "delta", "bwd")
         calls = (
@@ -456,15 +457,24 @@ def run_ours(args):
             lambda: gbattn.attn_bwd_decode(q, k, v, o, do, lse, dlt, dq, dk, dv, ws_dec, sc, causal, stream),
         )
     elif bm is None and not kv_cap:
-        phase_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
+        # the step: attn_fwd, attn_bwd_delta, attn_bwd (its dQ kernel fills
+        # the SMs the dK/dV kernel's last wave frees); the kernels are timed
+        # one by one in a second pass, through attn_bwd_dkv and attn_bwd_dq
+        phase_names = ("fwd", "delta", "bwd")
         calls = (
             lambda: gbattn.attn_fwd(q, k, v, o, lse, sc, causal, stream),
             lambda: gbattn.attn_bwd_delta(o, do, dlt, stream),
+            lambda: gbattn.attn_bwd(q, k, v, o, do, lse, dlt, dq, dk, dv, sc, causal, stream),
+        )
+        split_names = ("fwd", "delta", "bwd_dkv", "bwd_dq")
+        split_calls = (
+            calls[0], calls[1],
             lambda: gbattn.attn_bwd_dkv(q, k, v, do, lse, dlt, dk, dv, sc, causal, stream),
             lambda: gbattn.attn_bwd_dq(q, k, v, do, lse, dlt, dq, sc, causal, stream),
         )
     else:
         # attn_bwd_ex launches the dK/dV kernel, then the dQ kernel
+        split_names, split_calls = None, None
         phase_names = ("fwd", "delta", "bwd")
         calls = (
             lambda: gbattn.attn_fwd_ex(q, k, v, o, lse, sc, causal, block_mask=bm, stream=stream),
@@ -532,6 +542,20 @@ def run_ours(args):
         for j, n in enumerate(phase_names):
             per_phase[n].append(ev[j].elapsed_time(ev[j + 1]))
         step_ms.append(ev[0].elapsed_time(ev[-1]))
+    # the kernels one by one (the same number of steps), for the per-kernel rooflines
+    split = None
+    if split_calls is not None:
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(split_calls) + 1)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            for j, c in enumerate(split_calls):
+                sev[i][j].record(stream)
+                c()
+            sev[i][-1].record(stream)
+        torch.cuda.synchronize(dev)
+        if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
+            raise RuntimeError("device-side wait timed out in the per-kernel pass")
+        split = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in sev) for j, n in enumerate(split_names)}
     local_s = sum(step_ms) / 1e3
     if bm is None:
         pairs = F.visible_pairs(w.Lq, w.Lk, w.causal)
@@ -548,6 +572,7 @@ def run_ours(args):
         long_run["pct_of_bf16_peak"] = 100.0 * long_run["value"] / peaks["bf16_tflops"]
         long_run["pct_of_bf16_peak_sustained"] = 100.0 * long_run["value"] / peaks["bf16_tflops_sustained"]
     avg = {n: statistics.mean(v) for n, v in per_phase.items()}
+    kavg = dict(avg, **split) if split else avg  # per-kernel times
     clocks.stop()  # the tool exits and flushes its last lines
     clk = clocks.window()
     if long_run is not None:
@@ -558,31 +583,31 @@ def run_ours(args):
 
     # roofline per kernel (algorithmic work / average launch time)
     kernels = {}
-    mm_phases = [n for n in phase_names if n != "delta"]
+    mm_phases = [n for n in (split_names or phase_names) if n != "delta"]
     for n in mm_phases:
         if args.decode:  # bound by the key/value range read
             by = F.decode_bytes(n, w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D)
-            ach = by / (avg[n] * 1e-3) / 1e9
+            ach = by / (kavg[n] * 1e-3) / 1e9
             kernels[n] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": ach / peaks["hbm_gbs"], "avg_ms": avg[n], "algorithmic": by, "traffic": None}
+                          "frac": ach / peaks["hbm_gbs"], "avg_ms": kavg[n], "algorithmic": by, "traffic": None}
             continue
         fl = F.kernel_flops_pairs(n, w.B, w.Hq, w.D, pairs)
-        ach = fl / (avg[n] * 1e-3) / 1e12
+        ach = fl / (kavg[n] * 1e-3) / 1e12
         plain = bm is None and not kv_cap
         kernels[n] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
                       "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
                       "frac_sustained": ach / peaks["bf16_tflops_sustained"],
-                      "avg_ms": avg[n], "algorithmic": fl,
+                      "avg_ms": kavg[n], "algorithmic": fl,
                       "traffic": recorded_traffic(n, w.name, w.D) if plain else None,
                       "ncu_tensor_pipe_pct": recorded_tensor_pipe(n, w.name, w.D) if plain else None}
         if pipe_tflops:
             kernels[n]["frac_of_clock_ceiling"] = ach / pipe_tflops
     db = F.delta_bytes(w.B, w.Hq, w.Lq, w.D)
-    ach = db / (avg["delta"] * 1e-3) / 1e9
+    ach = db / (kavg["delta"] * 1e-3) / 1e9
     kernels["delta"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": ach / peaks["hbm_gbs"], "avg_ms": avg["delta"], "algorithmic": db,
+                        "frac": ach / peaks["hbm_gbs"], "avg_ms": kavg["delta"], "algorithmic": db,
                         "traffic": recorded_traffic("delta", w.name, w.D)}
-    dominant = max(mm_phases, key=lambda n: avg[n])
+    dominant = max(mm_phases, key=lambda n: kavg[n])
     roof = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
     if kernels[dominant]["bound"] == "tensor":
@@ -629,6 +654,7 @@ def run_ours(args):
         "pct_of_bf16_peak_sustained": 100.0 * value / ws / peaks["bf16_tflops_sustained"],
         "peaks": peaks,
         "phase_ms": avg,
+        "kernel_ms": split,  # each kernel timed on its own (None: the phases are the kernels)
         "roofline": roof,
         "kernels": kernels,
         "long_run": long_run,

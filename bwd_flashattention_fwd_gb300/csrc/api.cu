@@ -1,6 +1,7 @@
 // C ABI of libgbattn.so (declared in include/gbattn.h): argument validation,
 // the per-device status word, and dispatch to the per-head-dimension
 // launchers.  Validation is synchronous and touches no device memory.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -19,6 +20,19 @@ std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
 int* g_status[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
+
+// Work counters of the persistent dQ kernel: kSchedSlots pairs of ints per
+// device, zero between launches (each launch's last CTA resets its pair).
+// Calls take the slots in turn, so backward calls in flight at the same
+// time on one device use different counters unless more than kSchedSlots
+// of them overlap.
+constexpr int kSchedSlots = 64;
+int* g_sched[kMaxDevices] = {};
+std::atomic<unsigned> g_sched_next[kMaxDevices];
+
+int* sched_slot(int* pool, std::atomic<unsigned>& next) {
+  return pool + 2 * (next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
+}
 
 uint64_t wait_limit_ns() {
   static const uint64_t v = [] {
@@ -51,6 +65,10 @@ attn_status_t device_state(int* dev_out, EncodeTiledFn* enc, int** status, int* 
     int* p = nullptr;
     if (cudaMalloc(&p, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
     if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int* sp = nullptr;
+    if (cudaMalloc(&sp, 2 * kSchedSlots * sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemset(sp, 0, 2 * kSchedSlots * sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_sched[dev] = sp;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ERR_CUDA;
     g_num_sms[dev] = sms;
@@ -214,6 +232,7 @@ attn_status_t bwd_call(const void* q, const void* k, const void* v, const void* 
   a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = delta;
   a.block_mask = block_mask, a.kv_pitch = kv_pitch;
   a.dq = dq, a.dk = dk, a.dv = dv;
+  a.sched = sched_slot(g_sched[dev], g_sched_next[dev]);
   a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();
@@ -383,6 +402,7 @@ attn_status_t bwd_part(bool dq_part, const void* q, const void* k, const void* v
   if (ds != ATTN_OK) return ds;
   a.q = q, a.k = k, a.v = v, a.dO = dO, a.lse = lse, a.delta = delta;
   a.dq = dq, a.dk = dk, a.dv = dv;
+  a.sched = sched_slot(g_sched[dev], g_sched_next[dev]);
   a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();
@@ -413,7 +433,11 @@ extern "C" attn_status_t attn_bwd_dkv(const void* q, const void* k, const void* 
 namespace {
 
 constexpr long long kNoAllocMaxRows = 1LL << 20;  // B * Hq * Lq, i.e. 4 MiB of delta
-constexpr size_t kNoAllocHeaderBytes = 256;        // status word, padded to the alignment
+// header: the status word at 0, the dQ kernel's work counters at 256
+// (kSchedSlots pairs of ints, zero between launches), padded to 1 KB
+constexpr size_t kNoAllocSchedOffset = 256;
+constexpr size_t kNoAllocHeaderBytes = 1024;
+static_assert(kNoAllocSchedOffset + 2 * kSchedSlots * sizeof(int) <= kNoAllocHeaderBytes, "scratch header");
 constexpr size_t kNoAllocBytes = kNoAllocHeaderBytes + sizeof(float) * static_cast<size_t>(kNoAllocMaxRows);
 
 // Loaded with the library on every GPU that uses it, and kept until exit.
@@ -423,6 +447,7 @@ std::mutex g_noalloc_mu;
 EncodeTiledFn g_noalloc_encode = nullptr;
 unsigned char* g_noalloc_ptr[kMaxDevices] = {};
 int g_noalloc_sms[kMaxDevices] = {};
+std::atomic<unsigned> g_noalloc_sched_next[kMaxDevices];
 
 // Once per device, with that device current: the device address of the
 // scratch array (host code only sees a stand-in for the symbol), the SM count
@@ -502,6 +527,7 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
   a.status = status;
   a.q = q, a.k = k, a.v = v, a.o = o, a.dO = dO, a.lse = lse, a.delta = dlt, a.delta_out = dlt;
   a.dq = dq, a.dk = dk, a.dv = dv;
+  a.sched = sched_slot(reinterpret_cast<int*>(scratch + kNoAllocSchedOffset), g_noalloc_sched_next[dev]);
   a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();

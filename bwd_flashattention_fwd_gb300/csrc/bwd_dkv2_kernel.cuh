@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   const uint32_t sQ0 = sbase + Gm::V_BYTES;
   const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
 
+  // A dQ kernel launched behind this one may start filling the SMs this grid
+  // frees as soon as every CTA of it is running (it reads none of its outputs).
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int bhk = blockIdx.x;  // b * Hkv + hk
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int kt = blockIdx.y;

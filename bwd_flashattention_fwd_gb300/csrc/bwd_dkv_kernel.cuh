@@ -693,6 +693,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DkvPairGeom::NUM_THR
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                         const BwdParams p) {
   __shared__ PtXchBars xb;
+  // A dQ kernel launched behind this one may start filling the SMs this grid
+  // frees as soon as every CTA of it is running (it reads none of its outputs).
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int bhk = static_cast<int>(blockIdx.x >> 1), kt = static_cast<int>(blockIdx.y);
   if (cluster_ctarank() == 1)
     dk256_tile<BF16, CAUSAL, MASKED>(tmQ, tmdO, p, bhk, kt, xb);

@@ -23,12 +23,15 @@
 //     dP two tiles ahead of the row threads.
 //
 // Persistent: one CTA per SM walks a list of (query tile, head) work items,
-// heaviest query tiles first, dealt to the CTAs in alternating (snake) order
-// so every CTA gets a similar amount of work.  While a CTA works on item i,
-// its producer warp prefetches item i+1's Q and dO tiles into shared memory
-// with TMA, so starting the next item costs a shared-to-tensor-memory copy
-// instead of a global-memory round trip.  Barrier phases count key tiles and
-// items over the CTA's whole life.
+// heaviest query tiles first, each CTA taking the next item from a global
+// counter when it needs one, so a CTA that starts late (the kernel is
+// launched to fill the SMs the dK/dV kernel frees in its last wave) simply
+// takes fewer items.  The producer warp takes the items and hands their
+// indices to the other warps through a four-slot ring in shared memory.
+// While a CTA works on item i, its producer warp prefetches item i+1's Q and
+// dO tiles into shared memory with TMA, so starting the next item costs a
+// shared-to-tensor-memory copy instead of a global-memory round trip.
+// Barrier phases count key tiles and items over the CTA's whole life.
 //
 // Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
 // 32*(w%4)..+31 (query rows) and key columns 32*(w/4)..+31 of each 64-key
@@ -100,12 +103,7 @@ __device__ __forceinline__ Dq3Item dq3_item(int w, int BH, int n_qtiles) {
   const int t = w / BH;
   return {n_qtiles - 1 - t, w - t * BH};
 }
-// Item of this CTA's round r (snake order over the CTAs), or -1 past the end.
-__device__ __forceinline__ int dq3_round_item(int r, int n_items) {
-  const int nc = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const int w = r * nc + ((r & 1) ? nc - 1 - c : c);
-  return w < n_items ? w : -1;
-}
+constexpr int kDq3ItemRing = 4;  // rounds whose item index a CTA keeps in shared memory
 
 template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
@@ -118,7 +116,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_qbfull, bar_qbfree, bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_sfree,
-      bar_dpfull[NDP], bar_dsready[NDP], bar_dqdone;
+      bar_dpfull[NDP], bar_dsready[NDP], bar_dqdone, bar_mfin[2];
+  __shared__ uint64_t bar_item[kDq3ItemRing];
+  __shared__ volatile int item_ring[kDq3ItemRing];  // work item of round r in slot r % 4 (-1: no more)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -142,6 +142,12 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   // number of computed key tiles of query tile qt (warp-collective)
   auto n_kept = [&](int qt) { return count_kept<MASKED>([&](int j) { return keep(qt, j); }, 0, n_kv_of(qt)); };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // the work item of round r, as the producer published it; -1 ends the
+  // CTA's loop (also once a wait has run out, so no loop outlives an abort)
+  auto round_item = [&](int r) {
+    mbar_wait(smem_u32(&bar_item[r % kDq3ItemRing]), (r / kDq3ItemRing) & 1, g, kDevTimeoutBase + 76);
+    return abort_flag ? -1 : item_ring[r % kDq3ItemRing];
+  };
   // extents for the debug build's index checks: rows of q / dq / lse /
   // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
   [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
@@ -164,6 +170,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       mbar_init(smem_u32(&bar_dsready[i]), Gm::NCT);
     }
     mbar_init(smem_u32(&bar_dqdone), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bar_mfin[i]), 1);
+    for (int i = 0; i < kDq3ItemRing; ++i) mbar_init(smem_u32(&bar_item[i]), 1);
     fence_mbar_init();
   }
   if (warp == Gm::S_MMA_WARP) {
@@ -192,12 +200,27 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         tma_load_3d_w(sDOb + c * BQ * 128, &tmdO, smem_u32(&bar_qbfull), c * 64, it.qt * BQ, it.bh);
       }
     };
+    // the next item from the global counter (warp-collective), -1 past the end
+    auto take_item = [&]() {
+      int t = 0;
+      if (lane == 0) t = atomicAdd(p.sched, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      return t < n_items ? t : -1;
+    };
+    auto publish = [&](int r, int w) {
+      if (lane == 0) {
+        item_ring[r % kDq3ItemRing] = w;
+        mbar_arrive(smem_u32(&bar_item[r % kDq3ItemRing]));
+      }
+      __syncwarp();
+    };
     RingPos<ST> kv;  // stage of the next key tile
     bool wrapped = false;  // the ring has been filled once: stages must be freed first
     int r = 0;
-    int w = dq3_round_item(0, n_items);
+    int w = take_item();
+    publish(0, w);
     if (w >= 0) load_q(w);
-    for (; w >= 0; ++r) {
+    for (; w >= 0 && !abort_flag; ++r) {
       const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
       const int b = it.bh / p.Hq, hq = it.bh - b * p.Hq;
       const int zkv = b * p.Hkv + hq / p.G;
@@ -218,13 +241,14 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         kv.next();
       }
       // The row threads copied this item's Q / dO out of the buffer when the
-      // item started: prefetch the next item's.
-      w = dq3_round_item(r + 1, n_items);
-      if (w >= 0) {
-        mbar_wait(smem_u32(&bar_qbfree), r & 1, g, kDevTimeoutBase + 72);
-        __syncwarp();
-        load_q(w);
-      }
+      // item started (after every MMA of round r - 1 had completed, so every
+      // warp has read round r - 1's slot): round r + 1 may take the slot of
+      // round r - 3, and the buffer the next item's Q / dO.
+      w = take_item();
+      mbar_wait(smem_u32(&bar_qbfree), r & 1, g, kDevTimeoutBase + 72);
+      __syncwarp();
+      publish(r + 1, w);
+      if (w >= 0) load_q(w);
     }
     // the last ST issued stages (fewer if the ring never wrapped)
     for (int u = 0; u < ST; ++u) {
@@ -243,7 +267,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     RingPos<ST> kv;       // stage of the next key tile
     uint32_t sphase = 0;  // parity of the S buffer's next use
     bool first = true;
-    for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
+    for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
       const int nk = n_kept(dq3_item(w, BH, p.n_qtiles).qt);
       // this item's Q is in tensor memory
       mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 63);
@@ -265,6 +289,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         mma_commit_w(smem_u32(&bar_kvempty[s]));
       }
     }
+    // every MMA this warp issued is complete before tensor memory is released
+    mma_commit_w(smem_u32(&bar_mfin[0]));
+    mbar_wait_drain(smem_u32(&bar_mfin[0]), 0);
     __syncwarp();
   } else if (warp == Gm::DQ_MMA_WARP) {
     // ---------------- dQ += dS K and dP = dO V^T issuer ----------------
@@ -290,7 +317,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       kv_dp.next();
       db_dp.next();
     };
-    for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
+    for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
       const int nk = n_kept(dq3_item(w, BH, p.n_qtiles).qt);
       // this item's dO is in tensor memory
       mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 66);
@@ -317,6 +344,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       // this commit covers all of the item's MMAs.
       mma_commit_w(smem_u32(&bar_dqdone));
     }
+    mma_commit_w(smem_u32(&bar_mfin[1]));
+    mbar_wait_drain(smem_u32(&bar_mfin[1]), 0);
     __syncwarp();
   } else {
     // ---------------- row threads ----------------
@@ -374,8 +403,8 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_qready));
     };
-    if (dq3_round_item(0, n_items) >= 0) copy_q(0);
-    for (int r = 0, w = dq3_round_item(0, n_items); w >= 0; w = dq3_round_item(++r, n_items)) {
+    if (round_item(0) >= 0) copy_q(0);
+    for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
       const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
       const int q0 = it.qt * BQ;
       const int qi = q0 + rr_;
@@ -449,7 +478,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       tc_fence_after_sync();
       // the next item's Q and dO first, so that its first S and dP products
       // run while this item's dQ is read out and stored
-      if (dq3_round_item(r + 1, n_items) >= 0) copy_q(r + 1);
+      if (round_item(r + 1) >= 0) copy_q(r + 1);
       typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
 #pragma unroll 1
       for (int c = half; c < D / 32; c += 2) {
@@ -475,6 +504,18 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   if (warp == Gm::S_MMA_WARP) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    // Launched behind the dK/dV kernel, this grid may not finish before it.
+    grid_dependency_wait();
+    // The last CTA to finish puts the work counter back to zero: every CTA
+    // has taken its last item by now.
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      p.sched[0] = 0;
+      p.sched[1] = 0;
+      __threadfence();
+    }
   }
 }
 

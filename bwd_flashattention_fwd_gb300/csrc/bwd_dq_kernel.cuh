@@ -324,6 +324,9 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
   }
+  // Launched behind the dK/dV kernel, this grid may not finish before it:
+  // one CTA waiting for it suffices, and holds only its own SM.
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) grid_dependency_wait();
 }
 
 }  // namespace gbattn

@@ -185,8 +185,11 @@ int dkv2_impl(const AttnArgs& a) {
 }
 
 // D <= 128: Q and dO held in tensor memory as MMA A operands (bwd_dq3_kernel.cuh).
+// behind_dkv: launched right behind the dK/dV kernel on the same stream as a
+// programmatic dependent, so its CTAs fill the SMs the dK/dV kernel's last
+// wave frees (it reads none of that kernel's outputs).
 template <bool BF16, bool CAUSAL, bool MASKED>
-int dq3_impl(const AttnArgs& a) {
+int dq3_impl(const AttnArgs& a, bool behind_dkv) {
   constexpr int DD = kD <= 128 ? kD : 128;
   using Gm = Dq3Geom<DD>;
   CUtensorMap tq, tdo, tk, tv;
@@ -201,17 +204,28 @@ int dq3_impl(const AttnArgs& a) {
   const long long n_items = static_cast<long long>(p.n_qtiles) * a.B * a.Hq;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
+  p.sched = a.sched;
   auto kern = attn_bwd_dq3_kernel<DD, BF16, CAUSAL, MASKED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
     return kLaunchCudaError;
-  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tdo, tk, tv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(Gm::NUM_THREADS);
+  cfg.dynamicSmemBytes = Gm::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = behind_dkv ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, tq, tdo, tk, tv, p) != cudaSuccess) return kLaunchCudaError;
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
 template <bool BF16, bool CAUSAL>
-int dq_impl(const AttnArgs& a) {
+int dq_impl(const AttnArgs& a, bool behind_dkv = false) {
   if constexpr (kD <= 128) {
-    return a.block_mask ? dq3_impl<BF16, CAUSAL, true>(a) : dq3_impl<BF16, CAUSAL, false>(a);
+    return a.block_mask ? dq3_impl<BF16, CAUSAL, true>(a, behind_dkv) : dq3_impl<BF16, CAUSAL, false>(a, behind_dkv);
   } else {
     using Gm = DqGeom<kD>;
     CUtensorMap tq, tk, tv, tdo;
@@ -223,11 +237,23 @@ int dq_impl(const AttnArgs& a) {
     p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
     p.n_ktiles = (a.Lk + Gm::BK - 1) / Gm::BK;
     const dim3 grid(a.B * a.Hq, p.n_qtiles);
-    if (a.block_mask)
-      return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL, false, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES,
-                    a.stream, tq, tk, tv, tdo, p);
-    return launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tk,
-                  tv, tdo, p);
+    auto kern = a.block_mask ? attn_bwd_dq_kernel<kD, BF16, CAUSAL, false, true> : attn_bwd_dq_kernel<kD, BF16, CAUSAL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+      return kLaunchCudaError;
+    // behind the dK/dV kernel: the hardware hands this grid's CTAs to the
+    // SMs that kernel's last wave frees (its CTAs run in any order anyway)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Gm::NUM_THREADS);
+    cfg.dynamicSmemBytes = Gm::SMEM_BYTES;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = behind_dkv ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, p) != cudaSuccess) return kLaunchCudaError;
+    return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
   }
 }
 
@@ -243,7 +269,7 @@ int dkv_all(const AttnArgs& a) {
 template <bool BF16, bool CAUSAL>
 int bwd_impl(const AttnArgs& a) {
   const int r = dkv_all<BF16, CAUSAL>(a);
-  return r == kLaunchOk ? dq_impl<BF16, CAUSAL>(a) : r;
+  return r == kLaunchOk ? dq_impl<BF16, CAUSAL>(a, /*behind_dkv=*/true) : r;
 }
 
 // Decode-shaped forward (G * Lq <= 128): the single-tile forward kernel on

@@ -89,6 +89,9 @@ struct BwdParams {
   // decode variant of the dQ kernel (as in FwdParams): fp32 partial dQ rows
   int qmod, split_tiles;
   float* ws;
+  // persistent dQ kernel: its work counter and the count of CTAs that have
+  // finished (two ints, zero at launch; the last CTA puts them back to zero)
+  int* sched;
 };
 
 // fp32 row of 32 values (128 bytes, 16-byte aligned) to global memory, scaled.

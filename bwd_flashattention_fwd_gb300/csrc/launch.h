@@ -45,6 +45,9 @@ struct AttnArgs {
   int64_t kv_pitch = 0;
   // decode calls: caller's fp32 workspace (see decode_layout)
   float* workspace = nullptr;
+  // the persistent dQ kernel's work counter: two ints in device memory, zero
+  // between launches (one slot of the library's per-device pool)
+  int* sched = nullptr;
 };
 
 // Decode-shaped calls (G * Lq <= 128): each KV head's G query heads x Lq rows

@@ -166,6 +166,17 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched right behind this one on
+// the same stream with programmatic serialization may start once every CTA
+// of this grid has signalled (or exited); the dependent grid's wait returns
+// once this grid has completed and its memory is visible.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // Named barriers (sub-CTA groups of whole warps)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

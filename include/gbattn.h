@@ -93,6 +93,12 @@ attn_status_t attn_bwd_delta(const void* o, const void* dO, float* delta, int B,
  *   S = Q K^T,  P = exp2(S * scale * log2(e) - lse),  dP = dO V^T,
  *   dS = P * (dP - delta),
  * and accumulate dQ = scale * dS K, dK = scale * dS^T Q, dV = P^T dO.
+ * The dQ kernel is launched behind the dK/dV kernel as a programmatic
+ * dependent on the same stream, so it fills the SMs the dK/dV kernel's last
+ * wave leaves idle; the call still completes as a whole in stream order.
+ * Its CTAs take work from a counter in a per-device pool of 64 that calls
+ * use in turn: at most 64 backward calls (attn_bwd, attn_bwd_dq and their
+ * variants) may be in flight on one device at the same time.
  *   q, k, v, o, dO: inputs (dtype; o is accepted for interface symmetry and is
  *   only read through delta).  lse from attn_fwd and delta from attn_bwd_delta
  *   of the same (q, k, v, scale, causal): float32 [B,Hq,Lq].
@@ -211,8 +217,9 @@ attn_status_t attn_bwd_decode(const void* q, const void* k, const void* v, const
  *
  * What it does: delta = rowsum(dO * O) (as attn_bwd_delta), then the dK/dV
  * and dQ kernels (as attn_bwd), with delta and the device status word kept in
- * a fixed scratch array that is part of the library image: 256 bytes of
- * header plus room for B*Hq*Lq <= 1,048,576 delta values (4 MiB), held on
+ * a fixed scratch array that is part of the library image: 1 KB of header
+ * (the status word and the dQ kernel's work counters) plus room for
+ * B*Hq*Lq <= 1,048,576 delta values (4 MiB), held on
  * every GPU that loads the library until the process exits.  The call makes
  * no cudaMalloc, cudaFree or other allocating call.
  *   Arguments as for attn_bwd, without delta.  Larger problems (B*Hq*Lq above
