@@ -252,6 +252,22 @@ class ClockSampler:
                 "window_s": round(t1 - t0, 4)}
 
 
+def gemm_canary(dev, n: int = 8192, reps: int = 3) -> float:
+    """TFLOP/s of a bf16 n x n x n library GEMM (torch.matmul), timed with
+    CUDA events: run before and after the timed steps, it shows whether the
+    clocks moved between them.  A measurement aid, not part of the step."""
+    a = torch.randn((n, n), device=dev, dtype=torch.bfloat16)
+    b = torch.randn((n, n), device=dev, dtype=torch.bfloat16)
+    torch.matmul(a, b)  # warm
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        torch.matmul(a, b)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    return 2.0 * n ** 3 * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
+
 def physical_gpu_index(local_rank: int) -> int:
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids = [x.strip() for x in vis.split(",") if x.strip()]
@@ -501,6 +517,7 @@ def run_ours(args):
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during warm-up")
     clocks.wait_first()
+    canary_before = gemm_canary(dev)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     replicas.barrier(dev)
@@ -573,6 +590,7 @@ def run_ours(args):
         long_run["pct_of_bf16_peak_sustained"] = 100.0 * long_run["value"] / peaks["bf16_tflops_sustained"]
     avg = {n: statistics.mean(v) for n, v in per_phase.items()}
     kavg = dict(avg, **split) if split else avg  # per-kernel times
+    canary_after = gemm_canary(dev)
     clocks.stop()  # the tool exits and flushes its last lines
     clk = clocks.window()
     if long_run is not None:
@@ -663,6 +681,8 @@ def run_ours(args):
         # the combine and the dQ reduction
         "gpu_launches": args.steps * (1 + 1 + n_dkv + 1 + (2 if args.decode else 0)),
         "clocks": clk,
+        # a bf16 8192^3 cuBLAS GEMM just before and just after the timed steps
+        "gemm_canary_tflops": {"before": canary_before, "after": canary_after},
         "wall_s_timed_region": t_wall,
         "kernel_source_hash": kernel_source_hash(),
     }

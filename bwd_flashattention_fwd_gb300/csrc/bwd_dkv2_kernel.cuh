@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_v, bar_kready, bar_stfull[ST], bar_stempty[ST], bar_sfull, bar_sfree, bar_dpfull[2],
-      bar_pready[2], bar_accdone;
+      bar_pready[2], bar_accdone, bar_sdone;
   __shared__ __align__(16) float nlse_s[ST][BQ];  // -lse per query column
   __shared__ __align__(16) float dlt_s[ST][BQ];
   __shared__ uint32_t tmem_slot;
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       mbar_init(smem_u32(&bar_pready[i]), NCT);
     }
     mbar_init(smem_u32(&bar_accdone), 1);
+    mbar_init(smem_u32(&bar_sdone), 1);
     fence_mbar_init();
   }
   if (warp == Gm::S_MMA_WARP) {
@@ -166,10 +167,13 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     RingPos<ST> st;                  // stage of iteration it
     auto qw = kept_walk<MASKED>(keep, p.n_qtiles);
     int gi = 0, qtile = qw.first(qt_start);  // query head in the group and query tile of iteration it
+    int ni = 0;  // stages issued; after an abort (a wait ran out) no further copy is issued
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 81);
       __syncwarp();
+      if (abort_flag) break;
+      ++ni;
       const int q0 = qtile * BQ;
       const int zq = b * p.Hq + hk * p.G + gi;
       mbar_arrive_expect_tx_w(smem_u32(&bar_stfull[s]), 2 * Gm::Q_BYTES);
@@ -189,8 +193,10 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
     }
+    // V and the last ST stages issued (a stage is refilled only after its
+    // release, so each holds at most one copy in flight)
     mbar_wait_drain(smem_u32(&bar_v), 0);
-    for (int it = (n_iter > ST ? n_iter - ST : 0); it < n_iter; ++it)
+    for (int it = (ni > ST ? ni - ST : 0); it < ni; ++it)
       mbar_wait_drain(smem_u32(&bar_stfull[it % ST]), (it / ST) & 1);
   } else if (warp == Gm::S_MMA_WARP) {
     // ---------------- S^T = K Q^T issuer (A operand K from tensor memory) ----------------
@@ -215,6 +221,9 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       mma_commit_w(smem_u32(&bar_sfull));
       mma_commit_w(smem_u32(&bar_stempty[s]));
     }
+    // every MMA this warp issued is complete before tensor memory is released
+    mma_commit_w(smem_u32(&bar_sdone));
+    mbar_wait_drain(smem_u32(&bar_sdone), 0);
     __syncwarp();
   } else if (warp == Gm::ACC_MMA_WARP) {
     // ---------------- dV += P^T dO, dK += dS^T Q and dP^T = V dO^T issuer ----------------
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       // dP^T(it+2) overwrites the buffer behind the MMAs that read P^T / dS^T
       if (it + 2 < n_iter) issue_dp(it + 2);
     }
-    // Every S^T MMA completed before the last P^T / dS^T was ready, so this
-    // commit covers all MMAs of the CTA.
+    // every MMA this warp issued is complete before tensor memory is
+    // released (the row threads also wait for it before reading dK, dV)
     mma_commit_w(smem_u32(&bar_accdone));
     mbar_wait_drain(smem_u32(&bar_accdone), 0);
     __syncwarp();

@@ -179,35 +179,47 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     auto wq = qw, wo = qw;
     int gq = 0, tq = wq.first(qt_start);  // query head in the group and query tile of the next Q load
     int go = 0, to = wo.first(qt_start);  // and of the next dO load
+    // Q and dO tiles issued; after an abort (a wait ran out) no further copy
+    // is issued, so the drains below cover every copy still in flight
+    int nqi = 0, noi = 0;
     auto load_q = [&](int i) {
       if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, kDevTimeoutBase + 111);
       __syncwarp();
+      if (abort_flag) return false;
+      ++nqi;
       const uint32_t bar = smem_u32(&bar_qfull[rq.slot]);
       mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
       load_tile256(sQ0 + rq.slot * Gm::Q_BYTES, &tmQ, bar, tq * BQ, b * p.Hq + hk * p.G + gq);
       rq.next();
       tq = wq.next(tq);
       if (tq >= p.n_qtiles) tq = wq.first(qt_start), ++gq;
+      return true;
     };
     auto load_o = [&](int i) {
       if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, kDevTimeoutBase + 119);
       __syncwarp();
+      if (abort_flag) return false;
+      ++noi;
       const uint32_t bar = smem_u32(&bar_ofull[ro.slot]);
       mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
       load_tile256(sdO0 + ro.slot * Gm::Q_BYTES, &tmdO, bar, to * BQ, b * p.Hq + hk * p.G + go);
       ro.next();
       to = wo.next(to);
       if (to >= p.n_qtiles) to = wo.first(qt_start), ++go;
+      return true;
     };
     // in the order the MMA warp needs them: dO runs two query tiles ahead of Q
-    for (int i = 0; i < 2 && i < n_iter; ++i) load_o(i);
-    for (int it = 0; it < n_iter; ++it) {
-      load_q(it);
-      if (it + 2 < n_iter) load_o(it + 2);
+    for (int i = 0; i < 2 && i < n_iter; ++i)
+      if (!load_o(i)) break;
+    for (int it = 0; it < n_iter && !abort_flag; ++it) {
+      if (!load_q(it)) break;
+      if (it + 2 < n_iter && !load_o(it + 2)) break;
     }
-    for (int i = (n_iter > NQ ? n_iter - NQ : 0); i < n_iter; ++i)
+    // the last Q and dO copies issued (a slot is refilled only after its
+    // release, so each slot has at most one copy in flight)
+    for (int i = (nqi > NQ ? nqi - NQ : 0); i < nqi; ++i)
       mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1);
-    for (int i = (n_iter > NO ? n_iter - NO : 0); i < n_iter; ++i)
+    for (int i = (noi > NO ? noi - NO : 0); i < noi; ++i)
       mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
@@ -363,6 +375,14 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
   }
+  // The last two hand-offs have landed before this CTA meets its partner
+  // at the final cluster barrier (after which either may exit): at once in
+  // a normal run, where every one of them was waited for; after an abort
+  // the partner may have sent part of a slot, and the bounded drain outlasts
+  // any copy still landing.
+  if (threadIdx.x == 0)
+    for (int it = (n_iter > PtXch::SLOTS ? n_iter - PtXch::SLOTS : 0); it < n_iter; ++it)
+      mbar_wait_drain(smem_u32(&xb.pfull[it & 1]), (it >> 1) & 1);
 }
 
 // D = 256, dV half (cluster rank 0): K in tensor memory as the A operand of
@@ -479,35 +499,47 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     auto wq = qw, wo = qw;
     int gq = 0, tq = wq.first(qt_start);  // query head in the group and query tile of the next Q load
     int go = 0, to = wo.first(qt_start);  // and of the next dO load
+    // Q and dO tiles issued; after an abort (a wait ran out) no further copy
+    // is issued, so the drains below cover every copy still in flight
+    int nqi = 0, noi = 0;
     auto load_q = [&](int i) {
       if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, kDevTimeoutBase + 131);
       __syncwarp();
+      if (abort_flag) return false;
+      ++nqi;
       const uint32_t bar = smem_u32(&bar_qfull[rq.slot]);
       mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
       load_tile256(sQ0 + rq.slot * Gm::Q_BYTES, &tmQ, bar, tq * BQ, b * p.Hq + hk * p.G + gq);
       rq.next();
       tq = wq.next(tq);
       if (tq >= p.n_qtiles) tq = wq.first(qt_start), ++gq;
+      return true;
     };
     auto load_o = [&](int i) {
       if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, kDevTimeoutBase + 139);
       __syncwarp();
+      if (abort_flag) return false;
+      ++noi;
       const uint32_t bar = smem_u32(&bar_ofull[ro.slot]);
       mbar_arrive_expect_tx_w(bar, Gm::Q_BYTES);
       load_tile256(sdO0 + ro.slot * Gm::Q_BYTES, &tmdO, bar, to * BQ, b * p.Hq + hk * p.G + go);
       ro.next();
       to = wo.next(to);
       if (to >= p.n_qtiles) to = wo.first(qt_start), ++go;
+      return true;
     };
     // in the order the MMA warp needs them: Q runs two query tiles ahead of dO
-    for (int i = 0; i < 2 && i < n_iter; ++i) load_q(i);
-    for (int it = 0; it < n_iter; ++it) {
-      load_o(it);
-      if (it + 2 < n_iter) load_q(it + 2);
+    for (int i = 0; i < 2 && i < n_iter; ++i)
+      if (!load_q(i)) break;
+    for (int it = 0; it < n_iter && !abort_flag; ++it) {
+      if (!load_o(it)) break;
+      if (it + 2 < n_iter && !load_q(it + 2)) break;
     }
-    for (int i = (n_iter > NQ ? n_iter - NQ : 0); i < n_iter; ++i)
+    // the last Q and dO copies issued (a slot is refilled only after its
+    // release, so each slot has at most one copy in flight)
+    for (int i = (nqi > NQ ? nqi - NQ : 0); i < nqi; ++i)
       mbar_wait_drain(smem_u32(&bar_qfull[i % NQ]), (i / NQ) & 1);
-    for (int i = (n_iter > NO ? n_iter - NO : 0); i < n_iter; ++i)
+    for (int i = (noi > NO ? noi - NO : 0); i < noi; ++i)
       mbar_wait_drain(smem_u32(&bar_ofull[i % NO]), (i / NO) & 1);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
@@ -635,13 +667,15 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       // completing on its pfull (the proxy fence makes the stores visible to
       // the copy)
       if (it >= 2) mbar_wait(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, kDevTimeoutBase + 138);
+      if (!abort_flag) {  // after an abort nothing more is sent
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
-        st_shared_v4(PtXch::addr(sStage, buf, warp, lane, v), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      bulk_s2cluster_w(PtXch::block(sX1, buf, warp), PtXch::block(sStage, buf, warp), PtXch::BLOCK_BYTES,
-                       cluster_map(smem_u32(&xb.pfull[buf]), 1));
+        for (int v = 0; v < 4; ++v)
+          st_shared_v4(PtXch::addr(sStage, buf, warp, lane, v), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        bulk_s2cluster_w(PtXch::block(sX1, buf, warp), PtXch::block(sStage, buf, warp), PtXch::BLOCK_BYTES,
+                         cluster_map(smem_u32(&xb.pfull[buf]), 1));
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready[buf]));

@@ -192,8 +192,10 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       tma_prefetch_desc(&tmV);
     }
     __syncwarp();
+    int nqb = 0;  // Q / dO prefetches issued
     auto load_q = [&](int w) {
       const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
+      ++nqb;
       mbar_arrive_expect_tx_w(smem_u32(&bar_qbfull), 2 * Gm::QB_BYTES);
       for (int c = 0; c < NCH; ++c) {
         tma_load_3d_w(sQb + c * BQ * 128, &tmQ, smem_u32(&bar_qbfull), c * 64, it.qt * BQ, it.bh);
@@ -231,6 +233,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         if (kv.slot == 0 && kv.phase == 1) wrapped = true;
         if (wrapped) mbar_wait(smem_u32(&bar_kvempty[s]), kv.phase ^ 1u, g, kDevTimeoutBase + 61);
         __syncwarp();
+        if (abort_flag) break;  // after an abort no further copy is issued
         const uint32_t bar = smem_u32(&bar_kvfull[s]);
         const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
         mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
@@ -248,9 +251,12 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       mbar_wait(smem_u32(&bar_qbfree), r & 1, g, kDevTimeoutBase + 72);
       __syncwarp();
       publish(r + 1, w);
-      if (w >= 0) load_q(w);
+      if (w >= 0 && !abort_flag) load_q(w);
     }
-    // the last ST issued stages (fewer if the ring never wrapped)
+    // the last Q / dO prefetch and the last ST issued stages (fewer if the
+    // ring never wrapped; a stage is refilled only after its release, so each
+    // holds at most one copy in flight)
+    if (nqb > 0) mbar_wait_drain(smem_u32(&bar_qbfull), (nqb - 1) & 1);
     for (int u = 0; u < ST; ++u) {
       kv.slot = kv.slot == 0 ? ST - 1 : kv.slot - 1;
       if (kv.slot == ST - 1) {

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
-      bar_dsready[2], bar_pfree[2], bar_dqdone;
+      bar_dsready[2], bar_pfree[2], bar_dqdone, bar_sdone;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       mbar_init(smem_u32(&bar_pfree[i]), 1);
     }
     mbar_init(smem_u32(&bar_dqdone), 1);
+    mbar_init(smem_u32(&bar_sdone), 1);
     fence_mbar_init();
   }
   if (warp == Gm::MMA_WARP) {
@@ -158,24 +159,34 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     }
     auto kw = kept_walk<MASKED>(keep, n_kv);
     int jt = kw.first(0);  // key tile of the j-th computed tile
+    int nki = 0, nvi = 0;  // K and V tiles issued
+    // After an abort (a wait ran out) no further copy is issued, so the
+    // drains below cover every copy still in flight.
     for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
       const int ks = j % KST, vs = j % VST;
       if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 11);
       __syncwarp();
+      if (abort_flag) break;
+      ++nki;
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64,
                       (j0 + jt) * BK, zkv);
       if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 18);
       __syncwarp();
+      if (abort_flag) break;
+      ++nvi;
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64,
                       (j0 + jt) * BK, zkv);
     }
-    for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
+    // Q / dO and the last K and V copies issued (a slot is refilled only
+    // after its release, so each slot has at most one copy in flight)
+    mbar_wait_drain(smem_u32(&bar_q), 0);
+    for (int j = (nki > KST ? nki - KST : 0); j < nki; ++j)
       mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1);
-    for (int j = (nk > VST ? nk - VST : 0); j < nk; ++j)
+    for (int j = (nvi > VST ? nvi - VST : 0); j < nvi; ++j)
       mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1);
     __syncwarp();
   } else if (warp == Gm::MMA_WARP) {
@@ -212,6 +223,9 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       mma_commit_w(smem_u32(&bar_vempty[vs]));
       mma_commit_w(smem_u32(&bar_sfull[buf]));
     }
+    // every MMA this warp issued is complete before tensor memory is released
+    mma_commit_w(smem_u32(&bar_sdone));
+    mbar_wait_drain(smem_u32(&bar_sdone), 0);
     __syncwarp();
   } else if (warp == Gm::ACC_MMA_WARP) {
     // ---------------- dQ += dS K issuer ----------------
@@ -234,8 +248,8 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       mma_commit_w(smem_u32(&bar_pfree[buf]));
       mma_commit_w(smem_u32(&bar_kempty[ks]));
     }
-    // Every S / dP MMA completed before the last dS was ready, so this commit
-    // covers all MMAs of the CTA.
+    // every MMA this warp issued is complete (the row threads also wait for
+    // it before reading dQ)
     mma_commit_w(smem_u32(&bar_dqdone));
     mbar_wait_drain(smem_u32(&bar_dqdone), 0);
     __syncwarp();

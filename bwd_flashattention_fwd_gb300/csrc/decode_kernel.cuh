@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
   constexpr int BK = Gm::BK, RQ = Gm::RQ, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_pready, bar_accfull, bar_accfree;
+  __shared__ uint64_t bar_q, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_pready, bar_accfull, bar_accfree,
+      bar_mfin;
   __shared__ __align__(16) float nlse_s[RQ];  // -lse per packed query column (-inf past R)
   __shared__ __align__(16) float dlt_s[RQ];
   __shared__ uint32_t tmem_slot;
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
     mbar_init(smem_u32(&bar_pready), NCT);
     mbar_init(smem_u32(&bar_accfull), 1);
     mbar_init(smem_u32(&bar_accfree), NCT);
+    mbar_init(smem_u32(&bar_mfin), 1);
     fence_mbar_init();
   }
   if (warp == Gm::MMA_WARP) {
@@ -185,10 +187,13 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
       dlt_s[c] = c < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 26) ? p.delta[row] : 0.f;
     }
     mbar_arrive(smem_u32(&bar_q));
+    int ni = 0;  // stages issued; after an abort (a wait ran out) no further copy is issued
     for (int i = 0; i < n_t; ++i) {
       const int s = i % ST;
       if (i >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (i / ST - 1) & 1, g, kDevTimeoutBase + 141);
       __syncwarp();
+      if (abort_flag) break;
+      ++ni;
       const uint32_t bar = smem_u32(&bar_kvfull[s]);
       const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
       mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
@@ -197,8 +202,10 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
         tma_load_3d_w(dK + Gm::KV_BYTES + c * BK * 128, &tmV, bar, c * 64, (t0 + i) * BK, bhk);
       }
     }
+    // Q / dO and the last ST stages issued (a stage is refilled only after
+    // its release, so each holds at most one copy in flight)
     mbar_wait_drain(smem_u32(&bar_q), 0);
-    for (int i = (n_t > ST ? n_t - ST : 0); i < n_t; ++i)
+    for (int i = (ni > ST ? ni - ST : 0); i < ni; ++i)
       mbar_wait_drain(smem_u32(&bar_kvfull[i % ST]), (i / ST) & 1);
   } else if (warp == Gm::MMA_WARP) {
     // ---------------- MMA issuer ----------------
@@ -244,6 +251,9 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
       }
       mma_commit_w(smem_u32(&bar_accfull));
     }
+    // every MMA this warp issued is complete before tensor memory is released
+    mma_commit_w(smem_u32(&bar_mfin));
+    mbar_wait_drain(smem_u32(&bar_mfin), 0);
     __syncwarp();
   } else {
     // ---------------- key-row threads ----------------

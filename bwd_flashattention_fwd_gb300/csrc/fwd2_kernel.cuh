@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(352, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qfree, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2][2], bar_pready[2][2],
-      bar_odone[2], bar_done;
+      bar_odone[2], bar_done, bar_mfin[2];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(smem_u32(&bar_odone[t]), 1);
     }
     mbar_init(smem_u32(&bar_done), 2);
+    for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&bar_mfin[t]), 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -162,7 +163,10 @@ __global__ void __launch_bounds__(352, 1)
     __syncwarp();
     RingPos<ST> st;  // stage of the next key tile
     int issued = 0;  // key tiles issued (all items)
-    for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
+    int nq = 0;      // items whose Q was loaded
+    // After an abort (a wait ran out) no further copy is issued, so the
+    // drains below cover every copy still in flight.
+    for (int r = 0, w = round_item(0); w >= 0 && !abort_flag; w = round_item(++r)) {
       const int pt = item_pt(w), bh = item_bh(w);
       const int b = bh / p.Hq, hq = bh - b * p.Hq;
       const int zkv = b * p.Hkv + hq / p.G;
@@ -171,6 +175,8 @@ __global__ void __launch_bounds__(352, 1)
       // the previous item's S MMAs, the only readers of Q, are complete
       if (r > 0) mbar_wait(smem_u32(&bar_qfree), (r - 1) & 1, g, kDevTimeoutBase + 30);
       __syncwarp();
+      if (abort_flag) break;
+      ++nq;
       mbar_arrive_expect_tx_w(smem_u32(&bar_q), 2 * Gm::Q_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < NCH; ++c)
@@ -180,6 +186,7 @@ __global__ void __launch_bounds__(352, 1)
         const int s = st.slot;
         if (issued >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 31);
         __syncwarp();
+        if (abort_flag) break;
         const uint32_t bar = smem_u32(&bar_kvfull[s]);
         const uint32_t dK = sK0 + 2 * s * Gm::KV_BYTES;
         mbar_arrive_expect_tx_w(bar, 2 * Gm::KV_BYTES);
@@ -191,12 +198,14 @@ __global__ void __launch_bounds__(352, 1)
         ++issued;
       }
     }
-    // the last ST issued stages
+    // the last ST issued stages (each slot holds at most one copy in
+    // flight: a stage is refilled only after its release), and the last Q
     for (int u = 0; u < ST && u < issued; ++u) {
       if (st.slot == 0) st.phase ^= 1u;
       st.slot = (st.slot == 0 ? ST : st.slot) - 1;
       mbar_wait_drain(smem_u32(&bar_kvfull[st.slot]), st.phase);
     }
+    if (nq > 0) mbar_wait_drain(smem_u32(&bar_q), (nq - 1) & 1);
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
     // ---------------- MMA issuers: warp 9 for tile 0, warp 10 for tile 1 ----------------
@@ -263,7 +272,9 @@ __global__ void __launch_bounds__(352, 1)
       if (n_kv == 0) mma_commit_w(smem_u32(&bar_qfree));  // nothing reads this item's Q
       mma_commit_w(smem_u32(&bar_done));
     }
-    if (r > 0) mbar_wait_drain(smem_u32(&bar_done), (r - 1) & 1);
+    // every MMA this warp issued is complete before tensor memory is released
+    mma_commit_w(smem_u32(&bar_mfin[t]));
+    mbar_wait_drain(smem_u32(&bar_mfin[t]), 0);
     __syncwarp();
   } else {
     // ---------------- softmax warpgroups ----------------

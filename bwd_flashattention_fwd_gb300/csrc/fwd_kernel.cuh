@@ -144,25 +144,35 @@ __global__ void __launch_bounds__(192, 1)
     RingPos<VST> vp;
     auto kw = kept_walk<MASKED>(keep, n_kv);
     int jt = kw.first(0);  // key tile of the j-th computed tile
+    int nki = 0, nvi = 0;  // K and V tiles issued
+    // After an abort (a wait ran out) no further copy is issued, so the
+    // drains below cover every copy still in flight.
     for (int j = 0; j < nk; ++j, jt = kw.next(jt), kp.next(), vp.next()) {
       const int ks = kp.slot, vs = vp.slot;
       if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), kp.phase ^ 1u, g, kDevTimeoutBase + 1);
       __syncwarp();
+      if (abort_flag) break;
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, (j0 + jt) * BK,
                       zkv);
+      ++nki;
       if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), vp.phase ^ 1u, g, kDevTimeoutBase + 9);
       __syncwarp();
+      if (abort_flag) break;
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sV0 + vs * Gm::KV_BYTES + c * BK * 128, &tmV, smem_u32(&bar_vfull[vs]), c * 64, (j0 + jt) * BK,
                       zkv);
+      ++nvi;
     }
-    // Do not leave the CTA while a copy may still be landing.
-    for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
+    // Do not leave the CTA while a copy may still be landing: Q and the last
+    // K and V copies issued (a slot is refilled only after its release, so
+    // each slot has at most one copy in flight).
+    mbar_wait_drain(smem_u32(&bar_q), 0);
+    for (int j = (nki > KST ? nki - KST : 0); j < nki; ++j)
       mbar_wait_drain(smem_u32(&bar_kfull[j % KST]), (j / KST) & 1);
-    for (int j = (nk > VST ? nk - VST : 0); j < nk; ++j)
+    for (int j = (nvi > VST ? nvi - VST : 0); j < nvi; ++j)
       mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1);
     __syncwarp();
   } else if (warp == 5) {

@@ -109,13 +109,14 @@ __global__ void __launch_bounds__(LceGemmGeom::NUM_THREADS, 1)
     __syncwarp();
     RingPos<ST> st;
     int issued = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x) {
       const int mt = t / p.n_nt, nt = t - mt * p.n_nt;
       const int m0 = mt * BM, n0 = nt * BN;
       for (int kt = 0; kt < p.n_kt; ++kt, st.next(), ++issued) {
         const int s = st.slot;
         if (issued >= ST) mbar_wait(smem_u32(&bar_empty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 51);
         __syncwarp();
+        if (abort_flag) break;  // after an abort no further copy is issued
         const uint32_t bar = smem_u32(&bar_full[s]);
         const uint32_t sA = sbase + s * Gm::STAGE_BYTES;
         const uint32_t sB = sA + Gm::A_BYTES;
@@ -131,7 +132,8 @@ __global__ void __launch_bounds__(LceGemmGeom::NUM_THREADS, 1)
         for (int j = 0; j < BN / 64; ++j) tma_load_3d_w(sB + j * Gm::MN_BOX_BYTES, &tmB, bar, n0 + 64 * j, p.b_k0 + k0, 0);
       }
     }
-    // the last ST issued stages have landed before shared memory is released
+    // the last ST issued stages (a stage is refilled only after its release,
+    // so each holds at most one copy in flight) have landed before shared memory is released
     for (int u = 0; u < ST && u < issued; ++u) {
       if (st.slot == 0) st.phase ^= 1u;
       st.slot = (st.slot == 0 ? ST : st.slot) - 1;

@@ -112,12 +112,13 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
     __syncwarp();
     RingPos<ST> st;
     int issued = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x) {
       const int vt = t / p.n_rt, rt = t - vt * p.n_rt;
       for (int k = 0; k < nk; ++k, st.next(), ++issued) {
         const int s = st.slot;
         if (issued >= ST) mbar_wait(smem_u32(&bar_empty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 41);
         __syncwarp();
+        if (abort_flag) break;  // after an abort no further copy is issued
         const uint32_t bar = smem_u32(&bar_full[s]);
         const uint32_t dA = sbase + s * Gm::STAGE_BYTES;
         mbar_arrive_expect_tx_w(bar, Gm::STAGE_BYTES);
@@ -125,7 +126,8 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
         tma_load_3d_w(dA + Gm::A_BYTES, &tmW, bar, k * BK, p.v0 + vt * BN, 0);
       }
     }
-    // the last ST issued stages
+    // the last ST issued stages (a stage is refilled only after its release,
+    // so each holds at most one copy in flight)
     for (int u = 0; u < ST && u < issued; ++u) {
       if (st.slot == 0) st.phase ^= 1u;
       st.slot = (st.slot == 0 ? ST : st.slot) - 1;
