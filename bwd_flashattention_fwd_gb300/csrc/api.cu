@@ -382,6 +382,7 @@ extern "C" attn_status_t attn_bwd_decode(const void* q, const void* k, const voi
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();
   const int r = dispatch_bwd_dkv_decode(a);
+  a.dq_behind_dkv = true;
   return finish(r == kLaunchOk ? dispatch_bwd_dq_decode(a) : r);
 }
 

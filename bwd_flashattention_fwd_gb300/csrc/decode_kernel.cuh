@@ -118,6 +118,10 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
   using Gm = DecodeDkvGeom<D>;
   using E = Elem<BF16>;
   constexpr int BK = Gm::BK, RQ = Gm::RQ, NCH = Gm::NCH, ST = Gm::STAGES, NCT = Gm::NCT;
+  // The split dQ kernel launched behind this one may start on the SMs this
+  // grid frees as soon as every CTA of it is running (it reads none of its
+  // outputs).
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_pready, bar_accfull, bar_accfree,

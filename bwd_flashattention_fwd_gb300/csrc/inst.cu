@@ -329,8 +329,21 @@ int dq_decode_impl(const AttnArgs& a) {
   p.split_tiles = sp.tiles_per_split;
   p.ws = a.workspace;
   const dim3 grid(static_cast<unsigned>(groups), sp.n_split);
-  const int r = launch(attn_bwd_dq_kernel<kD, BF16, CAUSAL, true>, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream,
-                       tq, tk, tv, tdo, p);
+  auto kern = attn_bwd_dq_kernel<kD, BF16, CAUSAL, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+    return kLaunchCudaError;
+  // behind the decode dK/dV kernel: its CTAs take the SMs that kernel frees
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(Gm::NUM_THREADS);
+  cfg.dynamicSmemBytes = Gm::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.dq_behind_dkv ? 1 : 0;
+  const int r = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, p) == cudaSuccess ? kLaunchOk : kLaunchCudaError;
   if (r != kLaunchOk) return r;
   const long long n4 = nrows * kD / 4;
   long long blocks = (n4 + kReduceThreads - 1) / kReduceThreads;

@@ -48,6 +48,9 @@ struct AttnArgs {
   // the persistent dQ kernel's work counter: two ints in device memory, zero
   // between launches (one slot of the library's per-device pool)
   int* sched = nullptr;
+  // the dQ launch follows the dK/dV launch on the same stream and may run
+  // beside its last wave (programmatic dependent launch)
+  bool dq_behind_dkv = false;
 };
 
 // Decode-shaped calls (G * Lq <= 128): each KV head's G query heads x Lq rows
