@@ -517,7 +517,7 @@ def run_ours(args):
     if gbattn.attn_last_device_status(stream) != gbattn.ATTN_OK:
         raise RuntimeError("device-side wait timed out during warm-up")
     clocks.wait_first()
-    canary_before = gemm_canary(dev)
+    canary_before = None if args.no_canary else gemm_canary(dev)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     replicas.barrier(dev)
@@ -590,7 +590,7 @@ def run_ours(args):
         long_run["pct_of_bf16_peak_sustained"] = 100.0 * long_run["value"] / peaks["bf16_tflops_sustained"]
     avg = {n: statistics.mean(v) for n, v in per_phase.items()}
     kavg = dict(avg, **split) if split else avg  # per-kernel times
-    canary_after = gemm_canary(dev)
+    canary_after = None if args.no_canary else gemm_canary(dev)
     clocks.stop()  # the tool exits and flushes its last lines
     clk = clocks.window()
     if long_run is not None:
@@ -719,7 +719,9 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
               for s_ in sets]
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = max(3, min(args.steps, 20))
+    # at least 50 steps: the pipeline's fill and drain (the first input copy
+    # and the last output copy, ~0.5 ms each) would weigh ~3% in 20
+    n = max(50, min(args.steps, 200))
     total = n + 3
     ev_in = [torch.cuda.Event() for _ in range(total)]
     ev_comp = [torch.cuda.Event() for _ in range(total)]
@@ -946,6 +948,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-long-run", action="store_true",
                     help=f"skip the extra {LONG_RUN_STEPS}-step run reported beside a shorter timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-canary", action="store_true",
+                    help="skip the library GEMM run before and after the timed steps (for kernel launch lists)")
     ap.add_argument("--oracle-table", action="store_true",
                     help="time the fp64 oracle on every full workload (host cores; no GPU)")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline sample")
