@@ -16,7 +16,11 @@
 // Tensor memory (512 columns): O (D columns, fp32), two S buffers (BK columns
 // each, fp32) and two P buffers (BK/2 columns, bf16/fp16 pairs).  S_j = Q K_j^T
 // runs on the tensor cores while the softmax warps turn S_{j-1} into P_{j-1};
-// O += P_j V_j reads P straight from tensor memory.
+// O += P_j V_j reads P straight from tensor memory.  A row keeps its
+// reference maximum until a tile raises the row maximum by more than 8 (log2
+// units), so the 256-column O accumulator is rescaled only on those rare
+// tiles; O / l and lse = m + log2 l use the same reference, so the result is
+// exact in exact arithmetic.
 //
 // DECODE (short query lengths): the G query heads x Lq rows of one KV head
 // (consecutive in the [B, Hq, Lq, D] layout) form one packed tile; packed row
@@ -58,6 +62,7 @@ struct FwdGeom {
   static constexpr int P_COL1 = P_COL0 + BK / 2;
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_THREADS = 192;
+  static constexpr float TAU = 8.0f;  // lazy-rescaling threshold (log2 units)
   static_assert(KSTAGES >= 2 && VSTAGES >= 2, "need double-buffered K and V rings");
   static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
 };
@@ -72,7 +77,7 @@ __global__ void __launch_bounds__(192, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
-      bar_pready[2], bar_odone, bar_drain;
+      bar_pready[2], bar_odone, bar_ofin, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -117,6 +122,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(smem_u32(&bar_pready[i]), 128);
     }
     mbar_init(smem_u32(&bar_odone), 1);
+    mbar_init(smem_u32(&bar_ofin), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     fence_mbar_init();
   }
@@ -213,7 +219,10 @@ __global__ void __launch_bounds__(192, 1)
           mma_ts_w(tmem + Gm::O_COL, pcol + kk * 8, sdesc_add(dVm, sp * Gm::KV_BYTES + kk * 2048), IDESC_PV,
                    (jp > 0 || kk > 0) ? 1u : 0u);
         mma_commit_w(smem_u32(&bar_vempty[sp]));
-        mma_commit_w(smem_u32(&bar_odone));
+        // O after the next-to-last and after the last key tile (earlier
+        // rescales wait for the next S commit, which follows P V in issue order)
+        if (jp == nk - 2) mma_commit_w(smem_u32(&bar_odone));
+        if (jp == nk - 1) mma_commit_w(smem_u32(&bar_ofin));
       }
     }
     // Wait for every MMA of this CTA before tensor memory is released.
@@ -236,50 +245,50 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t scol = tmem + lrow + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
-      float x[BK];
+      // raw S, 32 columns per load, all loads in flight before one wait
+      constexpr int NC = BK / 32;
+      uint32_t sr[NC][32];
 #pragma unroll
-      for (int c = 0; c < BK / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(scol + c * 32, rr);
-        tmem_ld_wait(rr);
+      for (int c = 0; c < NC; ++c) tmem_ld32(scol + c * 32, sr[c]);
+      tmem_ld_wait(sr[0]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]) * sl2;
-      }
+      for (int c = 1; c < NC; ++c) reg_fence(sr[c]);
       const int k0 = (j0 + jt) * BK;
       const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
       if (need_mask) {
 #pragma unroll
         for (int i = 0; i < BK; ++i)
-          if (k0 + i > lim) x[i] = -INFINITY;
+          if (k0 + i > lim) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
       }
-      float mt = x[0];
+      // row maximum of the raw scores (scale_log2 > 0 commutes with max):
+      // eight independent chains of three-input maxima
+      float mx[8];
 #pragma unroll
-      for (int i = 1; i < BK; ++i) mt = fmaxf(mt, x[i]);
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[0][i]);
+#pragma unroll
+      for (int e = 8; e < BK; e += 2)
+        mx[(e >> 1) & 7] = fmax3(mx[(e >> 1) & 7], __uint_as_float(sr[e >> 5][e & 31]),
+                                 __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]));
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
       const float m_new = fmaxf(m, mt);
-      // (decode: a row that has seen no key of its split keeps m = -inf, P = 0)
-      const float mu = ((DECODE || MASKED) && m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - mu);
-      float sum = 0.f;
-      const uint32_t pcol = tmem + lrow + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
-#pragma unroll
-      for (int c = 0; c < BK / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(x[c * 32 + 2 * i] - mu);
-          const float p1 = ex2_approx(x[c * 32 + 2 * i + 1] - mu);
-          sum += p0 + p1;
-          pk[i] = E::pack(p0, p1);
-        }
-        tmem_st16(pcol + c * 16, pk);
-      }
-      l = l * alpha + sum;
-      if (j > 0) {
-        // O holds P_{j-1} V_{j-1} only once that MMA is done; rescale after it.
-        mbar_wait(smem_u32(&bar_odone), (j - 1) & 1, g, kDevTimeoutBase + 7);
-        __syncwarp();
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // Lazy rescaling: the row keeps its reference maximum m until a tile
+      // raises the row maximum by more than TAU = 8 (log2 units), so P <= 2^8 and
+      // O and l are rescaled only on those (rare) tiles.  O holds P V up to
+      // the previous key tile once that MMA is done (none on the first tile:
+      // its P V overwrites O).  The MMA warp issues S of tile j+1 right after
+      // P V of tile j-1, so that S's barrier covers the P V; on the last tile
+      // a dedicated commit does.
+      if (__any_sync(0xffffffffu, m_new > m + Gm::TAU)) {
+        const float alpha = ex2_approx(m - m_new);  // 0 while m = -inf
+        m = m_new;
+        l *= alpha;
+        if (j > 0) {
+          if (j + 1 < nk)
+            mbar_wait(smem_u32(&bar_sfull[(j + 1) & 1]), ((j + 1) >> 1) & 1, g, kDevTimeoutBase + 7);
+          else
+            mbar_wait(smem_u32(&bar_odone), 0, g, kDevTimeoutBase + 7);
+          __syncwarp();
+          tc_fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t rr[32];
@@ -291,13 +300,38 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      // (decode, block mask: a row that has seen no key keeps m = -inf, P = 0)
+      const float mu = ((DECODE || MASKED) && m == -INFINITY) ? 0.f : m;
+      // P = exp2(S * scale_log2 - mu), two elements per packed instruction
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
+      uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      const uint32_t pcol = tmem + lrow + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, nm2), x0,
+                    x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
+          pk[i] = E::pack(p0, p1);
+        }
+        tmem_st16(pcol + c * 16, pk);
+      }
+      {
+        float s0, s1, s2, s3;
+        f2_unpack(sum2[0], s0, s1);
+        f2_unpack(sum2[1], s2, s3);
+        l += (s0 + s1) + (s2 + s3);
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready[j & 1]));
-      m = m_new;
     }
     // ---------------- epilogue ----------------
-    if (nk > 0) mbar_wait(smem_u32(&bar_odone), (nk - 1) & 1, g, kDevTimeoutBase + 8);
+    if (nk > 0) mbar_wait(smem_u32(&bar_ofin), 0, g, kDevTimeoutBase + 8);
     __syncwarp();
     tc_fence_after_sync();
     if constexpr (DECODE) {
