@@ -546,7 +546,7 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
 namespace gbattn {
 namespace probe {
 
-constexpr int kProbeCode = kDevTimeoutBase + 99;
+constexpr int kProbeCode = wait_code<99>();
 
 __global__ void attn_wait_probe_kernel(int* status, uint64_t limit_ns) {
   __shared__ uint64_t bar;

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     int ni = 0;  // stages issued; after an abort (a wait ran out) no further copy is issued
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
-      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 81);
+      if (it >= ST) mbar_wait(smem_u32(&bar_stempty[s]), st.phase ^ 1u, g, wait_code<81>());
       __syncwarp();
       if (abort_flag) break;
       ++ni;
@@ -202,15 +202,15 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     // ---------------- S^T = K Q^T issuer (A operand K from tensor memory) ----------------
     constexpr uint32_t IDESC_S = make_idesc_f16(128, BQ, BF16, false, false);
     const uint64_t dQk = make_sdesc_sw128(sQ0, 16, 1024);  // Q stage 0, K-major
-    mbar_wait(smem_u32(&bar_kready), 0, g, kDevTimeoutBase + 82);
+    mbar_wait(smem_u32(&bar_kready), 0, g, wait_code<82>());
     __syncwarp();
     tc_fence_after_sync();
     RingPos<ST> st;  // stage of iteration it
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot;
       // every row thread has loaded S^T(it-1) from the buffer
-      if (it >= 1) mbar_wait(smem_u32(&bar_sfree), (it - 1) & 1, g, kDevTimeoutBase + 83);
-      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 84);
+      if (it >= 1) mbar_wait(smem_u32(&bar_sfree), (it - 1) & 1, g, wait_code<83>());
+      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, wait_code<84>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -233,12 +233,12 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     const uint64_t dOk = make_sdesc_sw128(sdO0, 16, 1024);          // dO stage 0, K-major
     const uint64_t dQm = make_sdesc_sw128(sQ0, BQ * 128, 1024);     // Q stage 0, MN-major
     const uint64_t dOm = make_sdesc_sw128(sdO0, BQ * 128, 1024);    // dO stage 0, MN-major
-    mbar_wait(smem_u32(&bar_v), 0, g, kDevTimeoutBase + 85);
+    mbar_wait(smem_u32(&bar_v), 0, g, wait_code<85>());
     __syncwarp();
     RingPos<ST> st, st_dp;  // stages of the next dV / dK and of the next dP^T iteration
     auto issue_dp = [&](int it) {
       const int s = st_dp.slot, buf = it & 1;
-      mbar_wait(smem_u32(&bar_stfull[s]), st_dp.phase, g, kDevTimeoutBase + 86);
+      mbar_wait(smem_u32(&bar_stfull[s]), st_dp.phase, g, wait_code<86>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
     for (int it = 0; it < 2 && it < n_iter; ++it) issue_dp(it);
     for (int it = 0; it < n_iter; ++it, st.next()) {
       const int s = st.slot, buf = it & 1;
-      mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 87);
+      mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, wait_code<87>());
       __syncwarp();
       tc_fence_after_sync();
       // A operands: 16 queries per K step; the warps of query half h hold P^T
@@ -329,9 +329,9 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       const int q0 = qtile * BQ;
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start);
-      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, kDevTimeoutBase + 88);
-      mbar_wait(smem_u32(&bar_sfull), it & 1, g, kDevTimeoutBase + 89);
-      mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 90);
+      mbar_wait(smem_u32(&bar_stfull[s]), st.phase, g, wait_code<88>());
+      mbar_wait(smem_u32(&bar_sfull), it & 1, g, wait_code<89>());
+      mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, wait_code<90>());
       __syncwarp();
       tc_fence_after_sync();
       const bool need_mask = CAUSAL && (q0 < k0 + BK - 1 - p.off);
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready[buf]));
     }
-    mbar_wait(smem_u32(&bar_accdone), 0, g, kDevTimeoutBase + 91);
+    mbar_wait(smem_u32(&bar_accdone), 0, g, wait_code<91>());
     __syncwarp();
     tc_fence_after_sync();
     // epilogue: warpgroup `half` writes output columns [half*D/2, (half+1)*D/2)

@@ -183,7 +183,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     // is issued, so the drains below cover every copy still in flight
     int nqi = 0, noi = 0;
     auto load_q = [&](int i) {
-      if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, kDevTimeoutBase + 111);
+      if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, wait_code<20>());
       __syncwarp();
       if (abort_flag) return false;
       ++nqi;
@@ -196,7 +196,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       return true;
     };
     auto load_o = [&](int i) {
-      if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, kDevTimeoutBase + 119);
+      if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, wait_code<28>());
       __syncwarp();
       if (abort_flag) return false;
       ++noi;
@@ -231,7 +231,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
     RingPos<NO> ro;
     // dP^T(it) = V dO^T into buffer it & 1 (V from tensor memory)
     auto issue_dp = [&](int it) {
-      mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, kDevTimeoutBase + 113);
+      mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, wait_code<22>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -244,13 +244,13 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       mma_commit_w(smem_u32(&bar_oempty[ro.slot]));
       ro.next();
     };
-    mbar_wait(smem_u32(&bar_vready), 0, g, kDevTimeoutBase + 112);
+    mbar_wait(smem_u32(&bar_vready), 0, g, wait_code<21>());
     for (int it = 0; it < 2 && it < n_iter; ++it) issue_dp(it);
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
       // dS^T(it) is in dP^T buffer buf
-      mbar_wait(smem_u32(&bar_dsready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 114);
-      mbar_wait(smem_u32(&bar_qfull[rq.slot]), rq.phase, g, kDevTimeoutBase + 115);
+      mbar_wait(smem_u32(&bar_dsready[buf]), (it >> 1) & 1, g, wait_code<23>());
+      mbar_wait(smem_u32(&bar_qfull[rq.slot]), rq.phase, g, wait_code<24>());
       __syncwarp();
       tc_fence_after_sync();
       // A operand: queries 32h..32h+31 of warpgroup h as pairs in columns
@@ -312,14 +312,14 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
       if (it + 1 < n_iter) dl = delta_of(qtile, gi);  // next query tile's, in flight during this one
-      mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 116);
+      mbar_wait(smem_u32(&bar_dpfull[buf]), (it >> 1) & 1, g, wait_code<25>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t dcol = tmem + lrow + Gm::DPT_COL + buf * BQ + half * 32;
       uint32_t dr[32];
       tmem_ld32(dcol, dr);
       // P^T(it) from the dV CTA: 32 queries (four chunks) of this thread's key row
-      mbar_wait(smem_u32(&xb.pfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 117);
+      mbar_wait(smem_u32(&xb.pfull[buf]), (it >> 1) & 1, g, wait_code<26>());
       // the slot's next use (query tile it + 2) expects its bytes: the dV CTA
       // cannot write them before every warp here has released this use
       if (threadIdx.x == 0 && it + 2 < n_iter && !abort_flag)
@@ -349,7 +349,7 @@ __device__ __forceinline__ void dk256_tile(const CUtensorMap& tmQ, const CUtenso
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_dsready[buf]));
     }
-    mbar_wait(smem_u32(&bar_accdone), 0, g, kDevTimeoutBase + 118);
+    mbar_wait(smem_u32(&bar_accdone), 0, g, wait_code<27>());
     __syncwarp();
     tc_fence_after_sync();
     // epilogue: warpgroup `half` writes dK columns [half*128, half*128+128)
@@ -503,7 +503,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     // is issued, so the drains below cover every copy still in flight
     int nqi = 0, noi = 0;
     auto load_q = [&](int i) {
-      if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, kDevTimeoutBase + 131);
+      if (i >= NQ) mbar_wait(smem_u32(&bar_qempty[rq.slot]), rq.phase ^ 1u, g, wait_code<45>());
       __syncwarp();
       if (abort_flag) return false;
       ++nqi;
@@ -516,7 +516,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       return true;
     };
     auto load_o = [&](int i) {
-      if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, kDevTimeoutBase + 139);
+      if (i >= NO) mbar_wait(smem_u32(&bar_oempty[ro.slot]), ro.phase ^ 1u, g, wait_code<57>());
       __syncwarp();
       if (abort_flag) return false;
       ++noi;
@@ -551,7 +551,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
     RingPos<NO> ro;
     // S^T(it) = K Q^T into buffer it & 1 (K from tensor memory)
     auto issue_s = [&](int it) {
-      mbar_wait(smem_u32(&bar_qfull[rq.slot]), rq.phase, g, kDevTimeoutBase + 132);
+      mbar_wait(smem_u32(&bar_qfull[rq.slot]), rq.phase, g, wait_code<46>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -564,12 +564,12 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       mma_commit_w(smem_u32(&bar_qempty[rq.slot]));
       rq.next();
     };
-    mbar_wait(smem_u32(&bar_kready), 0, g, kDevTimeoutBase + 133);
+    mbar_wait(smem_u32(&bar_kready), 0, g, wait_code<47>());
     for (int it = 0; it < 2 && it < n_iter; ++it) issue_s(it);
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
-      mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 134);
-      mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, kDevTimeoutBase + 135);
+      mbar_wait(smem_u32(&bar_pready[buf]), (it >> 1) & 1, g, wait_code<48>());
+      mbar_wait(smem_u32(&bar_ofull[ro.slot]), ro.phase, g, wait_code<49>());
       __syncwarp();
       tc_fence_after_sync();
       // A operand: queries 32h..32h+31 of warpgroup h as pairs in columns
@@ -632,7 +632,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       qtile = qw.next(qtile);
       if (qtile >= p.n_qtiles) qtile = qw.first(qt_start), ++gi;
       if (it + 1 < n_iter) nl = nlse_of(qtile, gi);  // next query tile's, in flight during this one
-      mbar_wait(smem_u32(&bar_sfull[buf]), (it >> 1) & 1, g, kDevTimeoutBase + 136);
+      mbar_wait(smem_u32(&bar_sfull[buf]), (it >> 1) & 1, g, wait_code<50>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t scol = tmem + lrow + Gm::ST_COL + buf * BQ + half * 32;
@@ -666,7 +666,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       // too), then to the dK CTA's slot with one bulk copy per warp,
       // completing on its pfull (the proxy fence makes the stores visible to
       // the copy)
-      if (it >= 2) mbar_wait(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, kDevTimeoutBase + 138);
+      if (it >= 2) mbar_wait(smem_u32(&xb.pfree[buf]), ((it >> 1) & 1) ^ 1, g, wait_code<56>());
       if (!abort_flag) {  // after an abort nothing more is sent
 #pragma unroll
         for (int v = 0; v < 4; ++v)
@@ -680,7 +680,7 @@ __device__ __forceinline__ void dv256_tile(const CUtensorMap& tmQ, const CUtenso
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready[buf]));
     }
-    mbar_wait(smem_u32(&bar_accdone), 0, g, kDevTimeoutBase + 137);
+    mbar_wait(smem_u32(&bar_accdone), 0, g, wait_code<55>());
     __syncwarp();
     tc_fence_after_sync();
     typename E::T* dst = reinterpret_cast<typename E::T*>(p.dv) + (static_cast<size_t>(bhk) * p.Lk + kj) * D;

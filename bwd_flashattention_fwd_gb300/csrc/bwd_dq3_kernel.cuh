@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
   // the work item of round r, as the producer published it; -1 ends the
   // CTA's loop (also once a wait has run out, so no loop outlives an abort)
   auto round_item = [&](int r) {
-    mbar_wait(smem_u32(&bar_item[r % kDq3ItemRing]), (r / kDq3ItemRing) & 1, g, kDevTimeoutBase + 76);
+    mbar_wait(smem_u32(&bar_item[r % kDq3ItemRing]), (r / kDq3ItemRing) & 1, g, wait_code<76>());
     return abort_flag ? -1 : item_ring[r % kDq3ItemRing];
   };
   // extents for the debug build's index checks: rows of q / dq / lse /
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       for (int j = kw.first(0); j < n_kv; j = kw.next(j)) {
         const int s = kv.slot;
         if (kv.slot == 0 && kv.phase == 1) wrapped = true;
-        if (wrapped) mbar_wait(smem_u32(&bar_kvempty[s]), kv.phase ^ 1u, g, kDevTimeoutBase + 61);
+        if (wrapped) mbar_wait(smem_u32(&bar_kvempty[s]), kv.phase ^ 1u, g, wait_code<61>());
         __syncwarp();
         if (abort_flag) break;  // after an abort no further copy is issued
         const uint32_t bar = smem_u32(&bar_kvfull[s]);
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       // warp has read round r - 1's slot): round r + 1 may take the slot of
       // round r - 3, and the buffer the next item's Q / dO.
       w = take_item();
-      mbar_wait(smem_u32(&bar_qbfree), r & 1, g, kDevTimeoutBase + 72);
+      mbar_wait(smem_u32(&bar_qbfree), r & 1, g, wait_code<72>());
       __syncwarp();
       publish(r + 1, w);
       if (w >= 0 && !abort_flag) load_q(w);
@@ -276,14 +276,14 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
       const int nk = n_kept(dq3_item(w, BH, p.n_qtiles).qt);
       // this item's Q is in tensor memory
-      mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 63);
+      mbar_wait(smem_u32(&bar_qready), r & 1, g, wait_code<63>());
       for (int j = 0; j < nk; ++j, kv.next()) {
         const int s = kv.slot;
         // every row thread has loaded the previous S from the buffer
-        if (!first) mbar_wait(smem_u32(&bar_sfree), sphase ^ 1u, g, kDevTimeoutBase + 64);
+        if (!first) mbar_wait(smem_u32(&bar_sfree), sphase ^ 1u, g, wait_code<64>());
         first = false;
         sphase ^= 1u;
-        mbar_wait(smem_u32(&bar_kvfull[s]), kv.phase, g, kDevTimeoutBase + 65);
+        mbar_wait(smem_u32(&bar_kvfull[s]), kv.phase, g, wait_code<65>());
         __syncwarp();
         tc_fence_after_sync();
 #pragma unroll
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     // dP of the next key tile to load into its dP buffer
     auto issue_dp = [&]() {
       const int s = kv_dp.slot, buf = db_dp.slot;
-      mbar_wait(smem_u32(&bar_kvfull[s]), kv_dp.phase, g, kDevTimeoutBase + 67);
+      mbar_wait(smem_u32(&bar_kvfull[s]), kv_dp.phase, g, wait_code<67>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -326,11 +326,11 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
       const int nk = n_kept(dq3_item(w, BH, p.n_qtiles).qt);
       // this item's dO is in tensor memory
-      mbar_wait(smem_u32(&bar_qready), r & 1, g, kDevTimeoutBase + 66);
+      mbar_wait(smem_u32(&bar_qready), r & 1, g, wait_code<66>());
       for (int j = 0; j < NDP && j < nk; ++j) issue_dp();
       for (int j = 0; j < nk; ++j, kv.next(), db.next()) {
         const int s = kv.slot, buf = db.slot;
-        mbar_wait(smem_u32(&bar_dsready[buf]), db.phase, g, kDevTimeoutBase + 68);
+        mbar_wait(smem_u32(&bar_dsready[buf]), db.phase, g, wait_code<68>());
         __syncwarp();
         tc_fence_after_sync();
         // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     // MMA of the previous item reads them any more (its final commit has
     // completed).
     auto copy_q = [&](int rn) {
-      mbar_wait(smem_u32(&bar_qbfull), rn & 1, g, kDevTimeoutBase + 73);
+      mbar_wait(smem_u32(&bar_qbfull), rn & 1, g, wait_code<73>());
       uint32_t qa[HALF / 2], oa[HALF / 2];
 #pragma unroll
       for (int v = 0; v < HALF / 8; ++v) {
@@ -426,9 +426,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         const int buf = db.slot;
         const uint32_t dph = db.phase;
         db.next();
-        mbar_wait(smem_u32(&bar_sfull), sphase, g, kDevTimeoutBase + 69);
+        mbar_wait(smem_u32(&bar_sfull), sphase, g, wait_code<69>());
         sphase ^= 1u;
-        mbar_wait(smem_u32(&bar_dpfull[buf]), dph, g, kDevTimeoutBase + 71);
+        mbar_wait(smem_u32(&bar_dpfull[buf]), dph, g, wait_code<71>());
         __syncwarp();
         tc_fence_after_sync();
         const int kc0 = j * BK + half * 32;  // first key of this thread's columns
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         mbar_arrive(smem_u32(&bar_dsready[buf]));
       }
       // epilogue of the item: every MMA of the item is complete
-      mbar_wait(smem_u32(&bar_dqdone), r & 1, g, kDevTimeoutBase + 70);
+      mbar_wait(smem_u32(&bar_dqdone), r & 1, g, wait_code<70>());
       __syncwarp();
       tc_fence_after_sync();
       // the next item's Q and dO first, so that its first S and dP products

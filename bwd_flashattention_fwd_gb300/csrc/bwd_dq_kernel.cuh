@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     // drains below cover every copy still in flight.
     for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
       const int ks = j % KST, vs = j % VST;
-      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, kDevTimeoutBase + 11);
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), (j / KST - 1) & 1, g, wait_code<11>());
       __syncwarp();
       if (abort_flag) break;
       ++nki;
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       for (int c = 0; c < NCH; ++c)
         tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64,
                       (j0 + jt) * BK, zkv);
-      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, kDevTimeoutBase + 18);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), (j / VST - 1) & 1, g, wait_code<18>());
       __syncwarp();
       if (abort_flag) break;
       ++nvi;
@@ -196,13 +196,13 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const uint64_t dOd = make_sdesc_sw128(sdO, 16, 1024);  // dO, K-major
     const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
     const uint64_t dVk = make_sdesc_sw128(sV0, 16, 1024);  // V stage 0, K-major
-    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 12);
+    mbar_wait(smem_u32(&bar_q), 0, g, wait_code<12>());
     __syncwarp();
     for (int j = 0; j < nk; ++j) {
       const int ks = j % KST, vs = j % VST, buf = j & 1;
       // the dQ MMA of key tile j-2 has read this buffer's dS
-      if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, kDevTimeoutBase + 19);
-      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 13);
+      if (j >= 2) mbar_wait(smem_u32(&bar_pfree[buf]), ((j - 2) >> 1) & 1, g, wait_code<19>());
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, wait_code<13>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
         mma_ss_w(tmem + Gm::S_COL + buf * BK, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_S, kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_kempty[ks]));
-      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, kDevTimeoutBase + 14);
+      mbar_wait(smem_u32(&bar_vfull[vs]), (j / VST) & 1, g, wait_code<14>());
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -233,8 +233,8 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const uint64_t dKm = make_sdesc_sw128(sK0, BK * 128, 1024);  // K stage 0, MN-major
     for (int j = 0; j < nk; ++j) {
       const int ks = j % KST, buf = j & 1;
-      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, kDevTimeoutBase + 10);
-      mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 15);
+      mbar_wait(smem_u32(&bar_kfull[ks]), (j / KST) & 1, g, wait_code<10>());
+      mbar_wait(smem_u32(&bar_dsready[buf]), (j >> 1) & 1, g, wait_code<15>());
       __syncwarp();
       tc_fence_after_sync();
       // A operand: 16 keys per K step; keys 32h..32h+31 of warpgroup h sit as
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     int jt = kw.first(0);  // key tile of the j-th computed tile
     for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
       const int buf = j & 1;
-      mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, kDevTimeoutBase + 16);
+      mbar_wait(smem_u32(&bar_sfull[buf]), (j >> 1) & 1, g, wait_code<16>());
       __syncwarp();
       tc_fence_after_sync();
       const int k0 = (j0 + jt) * BK;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_dsready[buf]));
     }
-    mbar_wait(smem_u32(&bar_dqdone), 0, g, kDevTimeoutBase + 17);
+    mbar_wait(smem_u32(&bar_dqdone), 0, g, wait_code<17>());
     __syncwarp();
     tc_fence_after_sync();
     if constexpr (DECODE) {

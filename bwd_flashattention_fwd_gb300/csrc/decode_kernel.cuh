@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
     int ni = 0;  // stages issued; after an abort (a wait ran out) no further copy is issued
     for (int i = 0; i < n_t; ++i) {
       const int s = i % ST;
-      if (i >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (i / ST - 1) & 1, g, kDevTimeoutBase + 141);
+      if (i >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), (i / ST - 1) & 1, g, wait_code<58>());
       __syncwarp();
       if (abort_flag) break;
       ++ni;
@@ -221,10 +221,10 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
     const uint64_t dOk = make_sdesc_sw128(sdO, 16, 1024);                 // dO, K-major
     const uint64_t dQm = make_sdesc_sw128(sQ, RQ * 128, 1024);            // Q, MN-major
     const uint64_t dOm = make_sdesc_sw128(sdO, RQ * 128, 1024);           // dO, MN-major
-    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 142);
+    mbar_wait(smem_u32(&bar_q), 0, g, wait_code<59>());
     for (int i = 0; i < n_t; ++i) {
       const int s = i % ST;
-      mbar_wait(smem_u32(&bar_kvfull[s]), (i / ST) & 1, g, kDevTimeoutBase + 143);
+      mbar_wait(smem_u32(&bar_kvfull[s]), (i / ST) & 1, g, wait_code<60>());
       __syncwarp();
       tc_fence_after_sync();
       // S^T and dP^T of key tile i; they overwrite P^T / dS^T of tile i-1
@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
       }
       mma_commit_w(smem_u32(&bar_sfull));
       mma_commit_w(smem_u32(&bar_kvempty[s]));  // K and V of the stage are read
-      mbar_wait(smem_u32(&bar_pready), i & 1, g, kDevTimeoutBase + 144);
+      mbar_wait(smem_u32(&bar_pready), i & 1, g, wait_code<62>());
       // the row threads have read dK / dV of tile i-1 out
-      if (i > 0) mbar_wait(smem_u32(&bar_accfree), (i - 1) & 1, g, kDevTimeoutBase + 145);
+      if (i > 0) mbar_wait(smem_u32(&bar_accfree), (i - 1) & 1, g, wait_code<77>());
       __syncwarp();
       tc_fence_after_sync();
       // A operands: packed query columns 64h..64h+63 of warpgroup h sit as
@@ -266,12 +266,12 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
     const int r = quad * 32 + lane;
     const uint32_t lrow = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
-    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 146);  // the lse / delta tables
+    mbar_wait(smem_u32(&bar_q), 0, g, wait_code<78>());  // the lse / delta tables
     for (int i = 0; i < n_t; ++i) {
       const int k0 = (t0 + i) * BK, kj = k0 + r;
       const int qmin = kj - p.off;  // causal: query indices below this cannot see key kj
       const bool need_mask = CAUSAL && (k0 + BK - 1 - p.off > 0);
-      mbar_wait(smem_u32(&bar_sfull), i & 1, g, kDevTimeoutBase + 147);
+      mbar_wait(smem_u32(&bar_sfull), i & 1, g, wait_code<79>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll 1
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(DecodeDkvGeom<D>::NUM_THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_pready));
       // dK and dV of this key tile
-      mbar_wait(smem_u32(&bar_accfull), i & 1, g, kDevTimeoutBase + 148);
+      mbar_wait(smem_u32(&bar_accfull), i & 1, g, wait_code<80>());
       __syncwarp();
       tc_fence_after_sync();
       const size_t krow = static_cast<size_t>(bhk) * p.Lk + kj;

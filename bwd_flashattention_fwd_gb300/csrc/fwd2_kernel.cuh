@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(352, 1)
       const int q0 = pt * 2 * BQ;
       const int n_kv = n_kv_of(pt);
       // the previous item's S MMAs, the only readers of Q, are complete
-      if (r > 0) mbar_wait(smem_u32(&bar_qfree), (r - 1) & 1, g, kDevTimeoutBase + 30);
+      if (r > 0) mbar_wait(smem_u32(&bar_qfree), (r - 1) & 1, g, wait_code<30>());
       __syncwarp();
       if (abort_flag) break;
       ++nq;
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(352, 1)
       auto kw = kept_walk<MASKED>([&](int j) { return keep(pt, j); }, n_kv);
       for (int j = kw.first(0); j < n_kv; j = kw.next(j)) {
         const int s = st.slot;
-        if (issued >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 31);
+        if (issued >= ST) mbar_wait(smem_u32(&bar_kvempty[s]), st.phase ^ 1u, g, wait_code<31>());
         __syncwarp();
         if (abort_flag) break;
         const uint32_t bar = smem_u32(&bar_kvfull[s]);
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(352, 1)
     // S_t of the next key tile; the wait on the stage also covers V_j for P_t V_j
     auto issue_s = [&]() {
       const int s = st_s.slot, bb = ts & 1;
-      mbar_wait(smem_u32(&bar_kvfull[s]), st_s.phase, g, kDevTimeoutBase + 34);
+      mbar_wait(smem_u32(&bar_kvfull[s]), st_s.phase, g, wait_code<34>());
       st_s.next();
       ++ts;
       __syncwarp();
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t ph = (tp >> 1) & 1;
       st_pv.next();
       ++tp;
-      mbar_wait(smem_u32(&bar_pready[t][bb]), ph, g, kDevTimeoutBase + 35);
+      mbar_wait(smem_u32(&bar_pready[t][bb]), ph, g, wait_code<35>());
       __syncwarp();
       tc_fence_after_sync();
 #pragma unroll
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int w = round_item(0); w >= 0; w = round_item(++r)) {
       const int n_kv = n_kept(item_pt(w));  // computed key tiles of the item
       // this item's Q is in shared memory
-      mbar_wait(smem_u32(&bar_q), r & 1, g, kDevTimeoutBase + 33);
+      mbar_wait(smem_u32(&bar_q), r & 1, g, wait_code<33>());
       __syncwarp();
       tc_fence_after_sync();
       for (int j = 0; j < 2 && j < n_kv; ++j) {
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(352, 1)
         const int T = ts + k;
         const int bb = T & 1;
         const uint32_t s_col = tmem + lrow + Gm::s_col(t, bb);
-        mbar_wait(smem_u32(&bar_sfull[t][bb]), (T >> 1) & 1, g, kDevTimeoutBase + 37);
+        mbar_wait(smem_u32(&bar_sfull[t][bb]), (T >> 1) & 1, g, wait_code<37>());
         __syncwarp();
         tc_fence_after_sync();
         uint32_t ra[32], rb[32];
@@ -338,9 +338,9 @@ __global__ void __launch_bounds__(352, 1)
             // S_t of the next key tile was issued right after it, so its
             // barrier covers it; on the last key tile a dedicated commit does.
             if (k + 1 < nk)
-              mbar_wait(smem_u32(&bar_sfull[t][(T + 1) & 1]), ((T + 1) >> 1) & 1, g, kDevTimeoutBase + 39);
+              mbar_wait(smem_u32(&bar_sfull[t][(T + 1) & 1]), ((T + 1) >> 1) & 1, g, wait_code<39>());
             else
-              mbar_wait(smem_u32(&bar_odone[t]), odone_ph, g, kDevTimeoutBase + 40);
+              mbar_wait(smem_u32(&bar_odone[t]), odone_ph, g, wait_code<40>());
             __syncwarp();
             tc_fence_after_sync();
 #pragma unroll 1
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(352, 1)
       ts += nk;
       if (nk >= 2) odone_ph ^= 1u;
       // ---------------- epilogue ----------------
-      mbar_wait(smem_u32(&bar_done), r & 1, g, kDevTimeoutBase + 38);
+      mbar_wait(smem_u32(&bar_done), r & 1, g, wait_code<38>());
       __syncwarp();
       tc_fence_after_sync();
       const bool empty = MASKED && !(l > 0.f);  // the row saw no key: O = 0, lse = +inf

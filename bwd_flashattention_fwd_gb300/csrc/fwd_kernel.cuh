@@ -8,11 +8,15 @@
 // complete Flash Attention VJP implementation", section "Background":
 // P = exp2(S * scale_log2 - LSE)).
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3  softmax: thread t of warp w owns query row 32w+t, which is TMEM
 //              lane 32w+t of every accumulator;
 //   warp 4     TMA producer: Q once, then K and V tiles into their rings;
-//   warp 5     MMA issuer (one thread) and TMEM owner.
+//   warp 5     issues S = Q K^T (one thread) and owns the TMEM allocation;
+//   warp 6     issues O += P V.
+// Two issuing warps halve the serial barrier waits and commits per key tile
+// of each; S of tile j+2 is issued as soon as the softmax warps have loaded
+// S of tile j, so the score products run two tiles ahead of P V.
 // Tensor memory (512 columns): O (D columns, fp32), two S buffers (BK columns
 // each, fp32) and two P buffers (BK/2 columns, bf16/fp16 pairs).  S_j = Q K_j^T
 // runs on the tensor cores while the softmax warps turn S_{j-1} into P_{j-1};
@@ -61,14 +65,14 @@ struct FwdGeom {
   static constexpr int P_COL0 = S_COL1 + BK;
   static constexpr int P_COL1 = P_COL0 + BK / 2;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int NUM_THREADS = 192;
+  static constexpr int NUM_THREADS = 224;
   static constexpr float TAU = 8.0f;  // lazy-rescaling threshold (log2 units)
   static_assert(KSTAGES >= 2 && VSTAGES >= 2, "need double-buffered K and V rings");
   static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
 };
 
 template <int D, bool BF16, bool CAUSAL, bool DECODE = false, bool MASKED = false>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdGeom<D>::NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using Gm = FwdGeom<D>;
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(192, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
-      bar_pready[2], bar_odone, bar_ofin, bar_drain;
+      bar_sfree[2], bar_pready[2], bar_pvdone[2], bar_drain[2];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -119,11 +123,11 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_sfull[i]), 1);
+      mbar_init(smem_u32(&bar_sfree[i]), 128);
       mbar_init(smem_u32(&bar_pready[i]), 128);
+      mbar_init(smem_u32(&bar_pvdone[i]), 1);
+      mbar_init(smem_u32(&bar_drain[i]), 1);
     }
-    mbar_init(smem_u32(&bar_odone), 1);
-    mbar_init(smem_u32(&bar_ofin), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(192, 1)
     // drains below cover every copy still in flight.
     for (int j = 0; j < nk; ++j, jt = kw.next(jt), kp.next(), vp.next()) {
       const int ks = kp.slot, vs = vp.slot;
-      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), kp.phase ^ 1u, g, kDevTimeoutBase + 1);
+      if (j >= KST) mbar_wait(smem_u32(&bar_kempty[ks]), kp.phase ^ 1u, g, wait_code<1>());
       __syncwarp();
       if (abort_flag) break;
       mbar_arrive_expect_tx_w(smem_u32(&bar_kfull[ks]), Gm::KV_BYTES);
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d_w(sK0 + ks * Gm::KV_BYTES + c * BK * 128, &tmK, smem_u32(&bar_kfull[ks]), c * 64, (j0 + jt) * BK,
                       zkv);
       ++nki;
-      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), vp.phase ^ 1u, g, kDevTimeoutBase + 9);
+      if (j >= VST) mbar_wait(smem_u32(&bar_vempty[vs]), vp.phase ^ 1u, g, wait_code<9>());
       __syncwarp();
       if (abort_flag) break;
       mbar_arrive_expect_tx_w(smem_u32(&bar_vfull[vs]), Gm::KV_BYTES);
@@ -182,52 +186,52 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait_drain(smem_u32(&bar_vfull[j % VST]), (j / VST) & 1);
     __syncwarp();
   } else if (warp == 5) {
-    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    // ---------------- S = Q K^T issuer (whole warp, one elected lane issues) ----------------
     constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
-    constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
-    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);         // Q, K-major
-    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);        // K stage 0, K-major
-    const uint64_t dVm = make_sdesc_sw128(sV0, BK * 128, 1024);  // V stage 0, MN-major
-    mbar_wait(smem_u32(&bar_q), 0, g, kDevTimeoutBase + 2);
-    __syncwarp();
-    tc_fence_after_sync();
-    for (int j = 0; j <= nk; ++j) {  // j: computed tiles so far
-      if (j < nk) {
-        const int s = j % KST;
-        mbar_wait(smem_u32(&bar_kfull[s]), (j / KST) & 1, g, kDevTimeoutBase + 3);
-        __syncwarp();
-        tc_fence_after_sync();
-        const uint32_t d = tmem + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
+    const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);   // Q, K-major
+    const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
+    mbar_wait(smem_u32(&bar_q), 0, g, wait_code<2>());
+    for (int j = 0; j < nk; ++j) {  // j: computed tiles so far
+      const int s = j % KST;
+      // the softmax warps have loaded S of tile j-2 from this buffer
+      if (j >= 2) mbar_wait(smem_u32(&bar_sfree[j & 1]), ((j - 2) >> 1) & 1, g, wait_code<4>());
+      mbar_wait(smem_u32(&bar_kfull[s]), (j / KST) & 1, g, wait_code<3>());
+      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t d = tmem + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          const uint32_t ko = s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-          mma_ss_w(d, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(smem_u32(&bar_sfull[j & 1]));
-        mma_commit_w(smem_u32(&bar_kempty[s]));  // S_j was K_j's only reader
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        const uint32_t ko = s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+        mma_ss_w(d, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
       }
-      if (j >= 1) {
-        const int jp = j - 1, sp = jp % VST;
-        mbar_wait(smem_u32(&bar_pready[jp & 1]), (jp >> 1) & 1, g, kDevTimeoutBase + 4);
-        mbar_wait(smem_u32(&bar_vfull[sp]), (jp / VST) & 1, g, kDevTimeoutBase + 5);
-        __syncwarp();
-        tc_fence_after_sync();
-        const uint32_t pcol = tmem + ((jp & 1) ? Gm::P_COL1 : Gm::P_COL0);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_ts_w(tmem + Gm::O_COL, pcol + kk * 8, sdesc_add(dVm, sp * Gm::KV_BYTES + kk * 2048), IDESC_PV,
-                   (jp > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(smem_u32(&bar_vempty[sp]));
-        // O after the next-to-last and after the last key tile (earlier
-        // rescales wait for the next S commit, which follows P V in issue order)
-        if (jp == nk - 2) mma_commit_w(smem_u32(&bar_odone));
-        if (jp == nk - 1) mma_commit_w(smem_u32(&bar_ofin));
-      }
+      mma_commit_w(smem_u32(&bar_sfull[j & 1]));
+      mma_commit_w(smem_u32(&bar_kempty[s]));  // S_j was K_j's only reader
     }
-    // Wait for every MMA of this CTA before tensor memory is released.
-    mma_commit_w(smem_u32(&bar_drain));
-    mbar_wait_drain(smem_u32(&bar_drain), 0);
+    // every MMA this warp issued is complete before tensor memory is released
+    mma_commit_w(smem_u32(&bar_drain[0]));
+    mbar_wait_drain(smem_u32(&bar_drain[0]), 0);
+    __syncwarp();
+  } else if (warp == 6) {
+    // ---------------- O += P V issuer ----------------
+    constexpr uint32_t IDESC_PV = make_idesc_f16(128, D, BF16, false, true);
+    const uint64_t dVm = make_sdesc_sw128(sV0, BK * 128, 1024);  // V stage 0, MN-major
+    for (int j = 0; j < nk; ++j) {
+      const int sp = j % VST;
+      mbar_wait(smem_u32(&bar_pready[j & 1]), (j >> 1) & 1, g, wait_code<5>());
+      mbar_wait(smem_u32(&bar_vfull[sp]), (j / VST) & 1, g, wait_code<32>());
+      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t pcol = tmem + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_ts_w(tmem + Gm::O_COL, pcol + kk * 8, sdesc_add(dVm, sp * Gm::KV_BYTES + kk * 2048), IDESC_PV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(smem_u32(&bar_vempty[sp]));
+      mma_commit_w(smem_u32(&bar_pvdone[j & 1]));  // P buffer j&1 free; O includes tile j
+    }
+    mma_commit_w(smem_u32(&bar_drain[1]));
+    mbar_wait_drain(smem_u32(&bar_drain[1]), 0);
     __syncwarp();
   } else {
     // ---------------- softmax warps ----------------
@@ -241,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
     auto kw = kept_walk<MASKED>(keep, n_kv);
     int jt = kw.first(0);  // key tile of the j-th computed tile
     for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
-      mbar_wait(smem_u32(&bar_sfull[j & 1]), (j >> 1) & 1, g, kDevTimeoutBase + 6);
+      mbar_wait(smem_u32(&bar_sfull[j & 1]), (j >> 1) & 1, g, wait_code<6>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t scol = tmem + lrow + ((j & 1) ? Gm::S_COL1 : Gm::S_COL0);
@@ -253,6 +257,9 @@ __global__ void __launch_bounds__(192, 1)
       tmem_ld_wait(sr[0]);
 #pragma unroll
       for (int c = 1; c < NC; ++c) reg_fence(sr[c]);
+      // S is in registers: the S warp may compute tile j+2 into this buffer
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_sfree[j & 1]));
       const int k0 = (j0 + jt) * BK;
       const bool need_mask = (CAUSAL && (k0 + BK - 1 > q0 + p.off)) || (k0 + BK > p.Lk);
       if (need_mask) {
@@ -275,18 +282,15 @@ __global__ void __launch_bounds__(192, 1)
       // raises the row maximum by more than TAU = 8 (log2 units), so P <= 2^8 and
       // O and l are rescaled only on those (rare) tiles.  O holds P V up to
       // the previous key tile once that MMA is done (none on the first tile:
-      // its P V overwrites O).  The MMA warp issues S of tile j+1 right after
-      // P V of tile j-1, so that S's barrier covers the P V; on the last tile
-      // a dedicated commit does.
+      // its P V overwrites O).  (Each P V barrier completes once per two
+      // tiles and is waited for in order below, so a parity wait cannot
+      // mistake an older phase for this one.)
       if (__any_sync(0xffffffffu, m_new > m + Gm::TAU)) {
         const float alpha = ex2_approx(m - m_new);  // 0 while m = -inf
         m = m_new;
         l *= alpha;
         if (j > 0) {
-          if (j + 1 < nk)
-            mbar_wait(smem_u32(&bar_sfull[(j + 1) & 1]), ((j + 1) >> 1) & 1, g, kDevTimeoutBase + 7);
-          else
-            mbar_wait(smem_u32(&bar_odone), 0, g, kDevTimeoutBase + 7);
+          mbar_wait(smem_u32(&bar_pvdone[(j - 1) & 1]), ((j - 1) >> 1) & 1, g, wait_code<7>());
           __syncwarp();
           tc_fence_after_sync();
 #pragma unroll 1
@@ -306,6 +310,12 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mu, -mu);
       uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
       const uint32_t pcol = tmem + lrow + ((j & 1) ? Gm::P_COL1 : Gm::P_COL0);
+      // P V of tile j-2 has read this P buffer
+      if (j >= 2) {
+        mbar_wait(smem_u32(&bar_pvdone[j & 1]), ((j - 2) >> 1) & 1, g, wait_code<29>());
+        __syncwarp();
+        tc_fence_after_sync();
+      }
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         uint32_t pk[16];
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(smem_u32(&bar_pready[j & 1]));
     }
     // ---------------- epilogue ----------------
-    if (nk > 0) mbar_wait(smem_u32(&bar_ofin), 0, g, kDevTimeoutBase + 8);
+    if (nk > 0) mbar_wait(smem_u32(&bar_pvdone[(nk - 1) & 1]), ((nk - 1) >> 1) & 1, g, wait_code<8>());
     __syncwarp();
     tc_fence_after_sync();
     if constexpr (DECODE) {

@@ -19,6 +19,15 @@ enum : int {
   kDevBoundsBase = 200,
 };
 
+// Status code of bounded wait number C of a kernel.  A template, so that a
+// number that would leave the range of wait codes (and be read as a failed
+// index check) does not compile.
+template <int C>
+__host__ __device__ constexpr int wait_code() {
+  static_assert(C >= 1 && C < kDevBoundsBase - kDevTimeoutBase, "wait codes are 101..199");
+  return kDevTimeoutBase + C;
+}
+
 // Debug build (compiled with -DGBATTN_DEBUG_CHECKS): every plain global load
 // and store of the kernels first checks that the elements it touches,
 // [first, first + count), lie inside the tensor's extent [0, extent).  A

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(LceGemmGeom::NUM_THREADS, 1)
       const int m0 = mt * BM, n0 = nt * BN;
       for (int kt = 0; kt < p.n_kt; ++kt, st.next(), ++issued) {
         const int s = st.slot;
-        if (issued >= ST) mbar_wait(smem_u32(&bar_empty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 51);
+        if (issued >= ST) mbar_wait(smem_u32(&bar_empty[s]), st.phase ^ 1u, g, wait_code<51>());
         __syncwarp();
         if (abort_flag) break;  // after an abort no further copy is issued
         const uint32_t bar = smem_u32(&bar_full[s]);
@@ -152,13 +152,13 @@ __global__ void __launch_bounds__(LceGemmGeom::NUM_THREADS, 1)
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++u) {
       const int b = u & 1;
       // the epilogue has read this accumulator's previous tile
-      if (u >= 2) mbar_wait(smem_u32(&bar_accempty[b]), ((u >> 1) - 1) & 1, g, kDevTimeoutBase + 52);
+      if (u >= 2) mbar_wait(smem_u32(&bar_accempty[b]), ((u >> 1) - 1) & 1, g, wait_code<52>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t acc = tmem + b * BN;
       for (int kt = 0; kt < p.n_kt; ++kt, st.next()) {
         const int s = st.slot;
-        mbar_wait(smem_u32(&bar_full[s]), st.phase, g, kDevTimeoutBase + 53);
+        mbar_wait(smem_u32(&bar_full[s]), st.phase, g, wait_code<53>());
         __syncwarp();
         tc_fence_after_sync();
 #pragma unroll
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(LceGemmGeom::NUM_THREADS, 1)
       const int mt = t / p.n_nt, nt = t - mt * p.n_nt;
       const int b = u & 1;
       const int row = mt * BM + r;
-      mbar_wait(smem_u32(&bar_accfull[b]), (u >> 1) & 1, g, kDevTimeoutBase + 54);
+      mbar_wait(smem_u32(&bar_accfull[b]), (u >> 1) & 1, g, wait_code<54>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t acc = tmem + lrow + b * BN;

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
       const int vt = t / p.n_rt, rt = t - vt * p.n_rt;
       for (int k = 0; k < nk; ++k, st.next(), ++issued) {
         const int s = st.slot;
-        if (issued >= ST) mbar_wait(smem_u32(&bar_empty[s]), st.phase ^ 1u, g, kDevTimeoutBase + 41);
+        if (issued >= ST) mbar_wait(smem_u32(&bar_empty[s]), st.phase ^ 1u, g, wait_code<41>());
         __syncwarp();
         if (abort_flag) break;  // after an abort no further copy is issued
         const uint32_t bar = smem_u32(&bar_full[s]);
@@ -144,13 +144,13 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++u) {
       const int b = u & 1;
       // the epilogue has read this accumulator's previous tile
-      if (u >= 2) mbar_wait(smem_u32(&bar_accempty[b]), ((u >> 1) - 1) & 1, g, kDevTimeoutBase + 42);
+      if (u >= 2) mbar_wait(smem_u32(&bar_accempty[b]), ((u >> 1) - 1) & 1, g, wait_code<42>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t acc = tmem + b * BN;
       for (int k = 0; k < nk; ++k, st.next()) {
         const int s = st.slot;
-        mbar_wait(smem_u32(&bar_full[s]), st.phase, g, kDevTimeoutBase + 43);
+        mbar_wait(smem_u32(&bar_full[s]), st.phase, g, wait_code<43>());
         __syncwarp();
         tc_fence_after_sync();
 #pragma unroll
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(LceGeom::NUM_THREADS, 1)
       const int tv0 = p.v0 + vt * BN;  // vocabulary entry of column 0
       const int n_valid = min(BN, p.v_end - tv0);
       const int tgt = row < p.N && dbg_in_range(row, 1, p.N, p.status, 41) ? p.targets[row] : -1;
-      mbar_wait(smem_u32(&bar_accfull[b]), (u >> 1) & 1, g, kDevTimeoutBase + 44);
+      mbar_wait(smem_u32(&bar_accfull[b]), (u >> 1) & 1, g, wait_code<44>());
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t acc = tmem + lrow + b * BN;
