@@ -69,6 +69,12 @@ struct FwdGeom {
   static constexpr float TAU = 8.0f;  // lazy-rescaling threshold (log2 units)
   static_assert(KSTAGES >= 2 && VSTAGES >= 2, "need double-buffered K and V rings");
   static_assert(P_COL1 + BK / 2 <= TMEM_COLS, "tensor memory budget");
+  // Tensor memory left over (64 columns at D = 256) holds the first K steps
+  // of Q as 16-bit pairs: those S = Q K^T steps read A from tensor memory,
+  // the rest from shared memory (an MMA with both operands in shared memory
+  // at N = 64 is bound by shared-memory bandwidth).
+  static constexpr int QT_COL = P_COL1 + BK / 2;
+  static constexpr int QT_STEPS = (TMEM_COLS - QT_COL) / 8 < D / 16 ? (TMEM_COLS - QT_COL) / 8 : D / 16;
 };
 
 template <int D, bool BF16, bool CAUSAL, bool DECODE = false, bool MASKED = false>
@@ -81,7 +87,7 @@ __global__ void __launch_bounds__(FwdGeom<D>::NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST], bar_vempty[VST], bar_sfull[2],
-      bar_sfree[2], bar_pready[2], bar_pvdone[2], bar_drain[2];
+      bar_sfree[2], bar_pready[2], bar_pvdone[2], bar_drain[2], bar_qready;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -113,6 +119,7 @@ __global__ void __launch_bounds__(FwdGeom<D>::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
+    mbar_init(smem_u32(&bar_qready), 128);
     for (int s = 0; s < KST; ++s) {
       mbar_init(smem_u32(&bar_kfull[s]), 1);
       mbar_init(smem_u32(&bar_kempty[s]), 1);
@@ -190,7 +197,11 @@ __global__ void __launch_bounds__(FwdGeom<D>::NUM_THREADS, 1)
     constexpr uint32_t IDESC_QK = make_idesc_f16(128, BK, BF16, false, false);
     const uint64_t dQd = make_sdesc_sw128(sQ, 16, 1024);   // Q, K-major
     const uint64_t dKk = make_sdesc_sw128(sK0, 16, 1024);  // K stage 0, K-major
-    mbar_wait(smem_u32(&bar_q), 0, g, wait_code<2>());
+    // Q in shared memory, and its first QT_STEPS K steps in tensor memory
+    if constexpr (Gm::QT_STEPS > 0)
+      mbar_wait(smem_u32(&bar_qready), 0, g, wait_code<93>());
+    else
+      mbar_wait(smem_u32(&bar_q), 0, g, wait_code<2>());
     for (int j = 0; j < nk; ++j) {  // j: computed tiles so far
       const int s = j % KST;
       // the softmax warps have loaded S of tile j-2 from this buffer
@@ -203,7 +214,10 @@ __global__ void __launch_bounds__(FwdGeom<D>::NUM_THREADS, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
         const uint32_t ko = s * Gm::KV_BYTES + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-        mma_ss_w(d, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
+        if (kk < Gm::QT_STEPS)
+          mma_ts_w(d, tmem + Gm::QT_COL + kk * 8, sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
+        else
+          mma_ss_w(d, sdesc_add(dQd, qo), sdesc_add(dKk, ko), IDESC_QK, kk > 0 ? 1u : 0u);
       }
       mma_commit_w(smem_u32(&bar_sfull[j & 1]));
       mma_commit_w(smem_u32(&bar_kempty[s]));  // S_j was K_j's only reader
@@ -241,6 +255,30 @@ __global__ void __launch_bounds__(FwdGeom<D>::NUM_THREADS, 1)
     const float sl2 = p.scale_log2;
     // last visible key of this row (inclusive)
     const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
+    if constexpr (Gm::QT_STEPS > 0) {
+      // this row's first 16 * QT_STEPS elements of Q from shared memory (TMA
+      // layout: 64-column chunks of 128-byte rows, 16-byte units swizzled by
+      // row % 8) into tensor memory as 16-bit pairs
+      constexpr int NQ = 16 * Gm::QT_STEPS;  // elements
+      mbar_wait(smem_u32(&bar_q), 0, g, wait_code<92>());
+      uint32_t qa[NQ / 2];
+#pragma unroll
+      for (int v = 0; v < NQ / 8; ++v) {
+        const int e = 8 * v;
+        const uint4 x = ld_shared_v4(sQ + (e / 64) * (BQ * 128) + r * 128 + ((((e % 64) / 8) ^ (r & 7)) * 16));
+        qa[4 * v + 0] = x.x, qa[4 * v + 1] = x.y, qa[4 * v + 2] = x.z, qa[4 * v + 3] = x.w;
+      }
+#pragma unroll
+      for (int c = 0; c < NQ / 2; c += 16) {
+        uint32_t t16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t16[i] = qa[c + i];
+        tmem_st16(tmem + lrow + Gm::QT_COL + c, t16);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bar_qready));
+    }
     float m = -INFINITY, l = 0.f;
     auto kw = kept_walk<MASKED>(keep, n_kv);
     int jt = kw.first(0);  // key tile of the j-th computed tile
