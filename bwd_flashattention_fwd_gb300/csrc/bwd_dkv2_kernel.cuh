@@ -27,10 +27,11 @@
 // copies D/2 columns of its key rows into tensor memory; warp 8 producer (TMA
 // for the V tile and the Q/dO tiles, plain loads for the per-query lse/delta
 // values); warp 9 issues S^T and owns the TMEM allocation; warp 10 issues
-// dV, dK and dP^T.  MMA issue competes with MUFU instructions issued on the
-// same SM sub-partition, so the row warps on the sub-partitions of warps 9
-// and 10 evaluate part of their exponentials with a polynomial on the FMA
-// pipe (ex2_poly2).
+// dV, dK and dP^T.  A share of the exponentials of the row warps on the
+// sub-partitions of warps 9 and 10 can be evaluated with a polynomial on the
+// FMA pipe (ex2_poly2; GBATTN_DKV_POLY_Q1 / _Q2); none measured fastest.
+// (With equal shares, this three-way dispatch measured ~3% faster than a
+// single call.)
 //
 // MASKED: block-sparse variant ("feat(attention): complete Flash Attention
 // VJP implementation", section "Sparse Block Masks": the dK/dV kernel skips

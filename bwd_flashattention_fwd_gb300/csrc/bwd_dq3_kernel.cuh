@@ -38,10 +38,9 @@
 // tile, and copies D/2 columns of its rows of Q and dO into tensor memory;
 // warp 8 TMA producer (Q/dO tiles, and K_j and V_j together into one ring
 // stage); warp 9 issues S = Q K^T and owns the TMEM allocation; warp 10
-// issues dQ += dS K and dP = dO V^T.  MMA issue competes with MUFU
-// instructions issued on the same SM sub-partition, so the row warps on the
-// dQ warp's sub-partition evaluate part of their exponentials with a
-// polynomial on the FMA pipe (ex2_poly2).
+// issues dQ += dS K and dP = dO V^T.  All row warps run one code path (a
+// share of exponentials on the FMA pipe, ex2_poly2, can be compiled in with
+// GBATTN_DQ_POLY; none is fastest).
 //
 // MASKED: block-sparse variant ("feat(attention): complete Flash Attention
 // VJP implementation", section "Sparse Block Masks": the dQ kernel skips the
@@ -77,19 +76,16 @@ struct Dq3Geom {
   static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
   // element pairs (of 16 per thread and key tile) whose exponentials use the
-  // polynomial, on the sub-partition of the S warp (1) and of the dQ / dP
-  // warp (2)
-#ifndef GBATTN_DQ_POLY_Q1
-  static constexpr int POLY_Q1 = 0;
+  // polynomial, the same in every row warp: one code path for all of them
+  // measured faster than shares that differ per sub-partition, and no share
+  // fastest (L = 8192: 0.49 ms against 0.51-0.52 for uniform 2 or 4 and
+  // 0.57-0.60 for 2-8 on the dQ / dP warp's sub-partition only)
+#ifndef GBATTN_DQ_POLY
+  static constexpr int POLY = 0;
 #else
-  static constexpr int POLY_Q1 = GBATTN_DQ_POLY_Q1;
+  static constexpr int POLY = GBATTN_DQ_POLY;
 #endif
-#ifndef GBATTN_DQ_POLY_Q2
-  static constexpr int POLY_Q2 = 8;
-#else
-  static constexpr int POLY_Q2 = GBATTN_DQ_POLY_Q2;
-#endif
-  static_assert(POLY_Q1 >= 0 && POLY_Q1 <= 16 && POLY_Q2 >= 0 && POLY_Q2 <= 16, "polynomial share");
+  static_assert(POLY >= 0 && POLY <= 16, "polynomial share");
   static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
   static_assert(STAGES >= NDP + 1, "dP of tile j+3 is issued while K_j is still in use");
 };
@@ -467,12 +463,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
             pk[i] = E::pack(ds0, ds1);
           }
         };
-        if (quad == 1)  // sub-partition of the S warp
-          ds_tile(std::integral_constant<int, Gm::POLY_Q1>{});
-        else if (quad == 2)  // sub-partition of the dQ / dP warp
-          ds_tile(std::integral_constant<int, Gm::POLY_Q2>{});
-        else
-          ds_tile(std::integral_constant<int, 0>{});
+        ds_tile(std::integral_constant<int, Gm::POLY>{});
         tmem_st16(dcol, pk);
         tmem_st_wait();
         tc_fence_before_sync();
