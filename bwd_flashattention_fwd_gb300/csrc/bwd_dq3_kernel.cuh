@@ -76,16 +76,24 @@ struct Dq3Geom {
   static constexpr int DQ_MMA_WARP = NUM_COMPUTE_WARPS + 2;
   static constexpr int NUM_THREADS = 32 * (NUM_COMPUTE_WARPS + 3);
   // element pairs (of 16 per thread and key tile) whose exponentials use the
-  // polynomial, the same in every row warp: one code path for all of them
-  // measured faster than shares that differ per sub-partition, and no share
-  // fastest (L = 8192: 0.49 ms against 0.51-0.52 for uniform 2 or 4 and
-  // 0.57-0.60 for 2-8 on the dQ / dP warp's sub-partition only)
+  // polynomial.  Without a block mask: the same in every row warp, one code
+  // path for all of them, which measured faster than shares that differ per
+  // sub-partition, and no share fastest (L = 8192: 0.49 ms against 0.51-0.52
+  // for uniform 2 or 4 and 0.57-0.60 for 2-8 on the dQ / dP warp's
+  // sub-partition only).  With a block mask the opposite held: POLY_MASKED
+  // pairs on the dQ / dP warp's sub-partition only (random half of the
+  // blocks: backward 0.68 against 0.73 ms uniform).
 #ifndef GBATTN_DQ_POLY
   static constexpr int POLY = 0;
 #else
   static constexpr int POLY = GBATTN_DQ_POLY;
 #endif
-  static_assert(POLY >= 0 && POLY <= 16, "polynomial share");
+#ifndef GBATTN_DQ_POLY_MASKED
+  static constexpr int POLY_MASKED = 8;
+#else
+  static constexpr int POLY_MASKED = GBATTN_DQ_POLY_MASKED;
+#endif
+  static_assert(POLY >= 0 && POLY <= 16 && POLY_MASKED >= 0 && POLY_MASKED <= 16, "polynomial share");
   static_assert(D <= 128, "dQ, Q, dO and the S / dP buffers fill TMEM at D = 128");
   static_assert(STAGES >= NDP + 1, "dP of tile j+3 is issued while K_j is still in use");
 };
@@ -463,7 +471,16 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
             pk[i] = E::pack(ds0, ds1);
           }
         };
-        ds_tile(std::integral_constant<int, Gm::POLY>{});
+        if constexpr (MASKED) {
+          if (quad == 1)  // sub-partition of the S warp
+            ds_tile(std::integral_constant<int, 0>{});
+          else if (quad == 2)  // sub-partition of the dQ / dP warp
+            ds_tile(std::integral_constant<int, Gm::POLY_MASKED>{});
+          else
+            ds_tile(std::integral_constant<int, 0>{});
+        } else {
+          ds_tile(std::integral_constant<int, Gm::POLY>{});
+        }
         tmem_st16(dcol, pk);
         tmem_st_wait();
         tc_fence_before_sync();
