@@ -80,16 +80,19 @@ struct Dq3Geom {
   // path for all of them, which measured faster than shares that differ per
   // sub-partition, and no share fastest (L = 8192: 0.49 ms against 0.51-0.52
   // for uniform 2 or 4 and 0.57-0.60 for 2-8 on the dQ / dP warp's
-  // sub-partition only).  With a block mask the opposite held: POLY_MASKED
-  // pairs on the dQ / dP warp's sub-partition only (random half of the
-  // blocks: backward 0.68 against 0.73 ms uniform).
+  // sub-partition only).  The block-mask instantiation keeps a dispatch per
+  // sub-partition (POLY_MASKED on the dQ / dP warp's), which with no share
+  // measured fastest there (random half of the blocks: backward 0.66 ms,
+  // against 0.69 with 8 pairs and 0.73 with the single call), and gives the
+  // same arithmetic as the unmasked kernel: an all-ones mask reproduces the
+  // unmasked results bit for bit.
 #ifndef GBATTN_DQ_POLY
   static constexpr int POLY = 0;
 #else
   static constexpr int POLY = GBATTN_DQ_POLY;
 #endif
 #ifndef GBATTN_DQ_POLY_MASKED
-  static constexpr int POLY_MASKED = 8;
+  static constexpr int POLY_MASKED = 0;
 #else
   static constexpr int POLY_MASKED = GBATTN_DQ_POLY_MASKED;
 #endif
