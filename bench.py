@@ -699,10 +699,11 @@ def run_ours(args):
 def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
     """Same metric through attn_fwd / attn_bwd_delta / attn_bwd with pinned
     host buffers: every step copies q, k, v, dO in and o, lse, dq, dk, dv out.
-    Steps are pipelined over two sets of device buffers and three streams
+    Steps are pipelined over three sets of device buffers and three streams
     (copies in, compute, copies out), so step i's results travel to the host
-    while step i+1 computes; the timed region spans the first input copy to
-    the last output copy."""
+    while step i+1 computes and step i+2's inputs arrive (a third set keeps
+    one slow copy from stalling the compute stream); the timed region spans
+    the first input copy to the last output copy."""
     qh, kh, vh, doh = (t.pin_memory() for t in make_inputs(w, "cpu"))
     ins_h = (qh, kh, vh, doh)
     h2d = sum(t.numel() * t.element_size() for t in ins_h)
@@ -714,7 +715,8 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
         lse = torch.empty((w.B, w.Hq, w.Lq), dtype=torch.float32, device=dev)
         return {"in": (q, k, v, do), "o": o, "lse": lse, "dlt": torch.empty_like(lse), "dq": dq, "dk": dk, "dv": dv}
 
-    sets = [device_set(), device_set()]
+    NSET = 3
+    sets = [device_set() for _ in range(NSET)]
     outs_h = [[torch.empty_like(t, device="cpu").pin_memory() for t in (s_["o"], s_["lse"], s_["dq"], s_["dk"], s_["dv"])]
               for s_ in sets]
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
@@ -722,23 +724,23 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
     # at least 50 steps: the pipeline's fill and drain (the first input copy
     # and the last output copy, ~0.5 ms each) would weigh ~3% in 20
     n = max(50, min(args.steps, 200))
-    total = n + 3
+    total = n + NSET
     ev_in = [torch.cuda.Event() for _ in range(total)]
     ev_comp = [torch.cuda.Event() for _ in range(total)]
     ev_out = [torch.cuda.Event() for _ in range(total)]
 
     def e2e_step(i):
-        b = i % 2
+        b = i % NSET
         s_ = sets[b]
         with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev_comp[i - 2])  # buffer set b's inputs are free again
+            if i >= NSET:
+                s_in.wait_event(ev_comp[i - NSET])  # buffer set b's inputs are free again
             for dst, src in zip(s_["in"], ins_h):
                 dst.copy_(src, non_blocking=True)
             ev_in[i].record(s_in)
         stream.wait_event(ev_in[i])
-        if i >= 2:
-            stream.wait_event(ev_out[i - 2])  # buffer set b's outputs reached the host
+        if i >= NSET:
+            stream.wait_event(ev_out[i - NSET])  # buffer set b's outputs reached the host
         q, k, v, do = s_["in"]
         if bm is None:
             gbattn.attn_fwd(q, k, v, s_["o"], s_["lse"], w.scale, w.causal, stream)
@@ -757,14 +759,14 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
                 dst.copy_(src, non_blocking=True)
             ev_out[i].record(s_out)
 
-    for i in range(3):
+    for i in range(NSET):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     replicas.barrier(dev)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
-    for i in range(3, total):
+    for i in range(NSET, total):
         e2e_step(i)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
@@ -774,7 +776,7 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
     value, _, _ = replicas.aggregate_throughput(credited * n, local_s, dev)
     return {"value": value / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "ms_per_step": local_s * 1e3 / n,
-            "pipelining": "two device buffer sets; input copies, compute and output copies on separate streams"}
+            "pipelining": "three device buffer sets; input copies, compute and output copies on separate streams"}
 
 
 # ---------------------------------------------------------------------------
