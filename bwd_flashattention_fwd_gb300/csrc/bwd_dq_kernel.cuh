@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
     const float lse_r = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 10) ? p.lse[row] : 0.f;
     const float dlt_r = qi < p.Lq && dbg_in_range(row, 1, n_qrows, p.status, 11) ? p.delta[row] : 0.f;
     const int lim = CAUSAL ? min((DECODE ? qi % p.qmod : qi) + p.off, p.Lk - 1) : p.Lk - 1;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse_r, -lse_r), dlt2 = f2_pack(dlt_r, dlt_r);
     auto kw = kept_walk<MASKED>(keep, n_kv);
     int jt = kw.first(0);  // key tile of the j-th computed tile
     for (int j = 0; j < nk; ++j, jt = kw.next(jt)) {
@@ -281,16 +282,19 @@ __global__ void __launch_bounds__(DqGeom<D>::NUM_THREADS, 1)
       tmem_ld_wait(sr);
       reg_fence(dr);
       uint32_t pk[16];
+      // two elements per packed instruction
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, -lse_r));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -lse_r));
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sl2x2, nlse2), x0, x1);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         if (need_mask) {
           if (kc0 + 2 * i > lim) p0 = 0.f;
           if (kc0 + 2 * i + 1 > lim) p1 = 0.f;
         }
-        const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - dlt_r);
-        const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - dlt_r);
+        const uint64_t d2 = f2_sub(f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])), dlt2);
+        float ds0, ds1;
+        f2_unpack(f2_mul(f2_pack(p0, p1), d2), ds0, ds1);
         pk[i] = E::pack(ds0, ds1);
       }
       tmem_st16(scol, pk);
