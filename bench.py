@@ -451,6 +451,12 @@ def run_ours(args):
     bm_np = block_mask(args.block_mask, w.Lq, w.Lk, seed=w.seed)
     bm = None if bm_np is None else torch.from_numpy(bm_np).to(dev)
     kv_cap = args.kv_capacity
+    # the end-to-end run's pinned host buffers, allocated and copied through
+    # once now: in a fresh process, fresh pinned memory showed one-off copy
+    # stalls of ~15 ms for a while after its allocation
+    e2e_host = None
+    if not args.no_e2e and not kv_cap and not args.decode:
+        e2e_host = e2e_host_buffers(w, dev)
     if kv_cap:
         if kv_cap < w.Lk:
             raise SystemExit(f"--kv-capacity {kv_cap} is below Lk = {w.Lk}")
@@ -643,7 +649,7 @@ def run_ours(args):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and not kv_cap and not args.decode:
-        e2e = run_e2e(args, w, dev, stream, gbattn, credited, bm)
+        e2e = run_e2e(args, w, dev, stream, gbattn, credited, e2e_host, bm)
 
     n_dkv = 1  # one dK/dV launch (at D = 256 it holds both halves)
     extra = {}
@@ -696,7 +702,21 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
+def e2e_host_buffers(w, dev):
+    """Pinned host inputs (q, k, v, dO) and one set of pinned host outputs (o,
+    lse, dq, dk, dv) for run_e2e, each copied to and from the device once."""
+    ins_h = tuple(t.pin_memory() for t in make_inputs(w, "cpu"))
+    shapes = [(ins_h[0].shape, ins_h[0].dtype), ((w.B, w.Hq, w.Lq), torch.float32), (ins_h[0].shape, ins_h[0].dtype),
+              (ins_h[1].shape, ins_h[1].dtype), (ins_h[2].shape, ins_h[2].dtype)]
+    outs_h = [torch.empty(sh, dtype=dt).pin_memory() for sh, dt in shapes]
+    for t in (*ins_h, *outs_h):
+        d = t.to(dev, non_blocking=True)
+        t.copy_(d, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    return ins_h, outs_h
+
+
+def run_e2e(args, w, dev, stream, gbattn, credited, host, bm=None):
     """Same metric through attn_fwd / attn_bwd_delta / attn_bwd with pinned
     host buffers: every step copies q, k, v, dO in and o, lse, dq, dk, dv out.
     Steps are pipelined over three sets of device buffers and three streams
@@ -704,8 +724,7 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
     while step i+1 computes and step i+2's inputs arrive (a third set keeps
     one slow copy from stalling the compute stream); the timed region spans
     the first input copy to the last output copy."""
-    qh, kh, vh, doh = (t.pin_memory() for t in make_inputs(w, "cpu"))
-    ins_h = (qh, kh, vh, doh)
+    ins_h, outs_h = host
     h2d = sum(t.numel() * t.element_size() for t in ins_h)
 
     def device_set():
@@ -717,14 +736,19 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
 
     NSET = 3
     sets = [device_set() for _ in range(NSET)]
-    outs_h = [[torch.empty_like(t, device="cpu").pin_memory() for t in (s_["o"], s_["lse"], s_["dq"], s_["dk"], s_["dv"])]
-              for s_ in sets]
-    d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
+    # one host output set: the output copies run in order on one stream
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    # at least 50 steps: the pipeline's fill and drain (the first input copy
-    # and the last output copy, ~0.5 ms each) would weigh ~3% in 20
-    n = max(50, min(args.steps, 200))
-    total = n + NSET
+    # at least 200 steps (~0.3 s): the pipeline's fill and drain (the first
+    # input copy and the last output copy, ~1 ms each) would weigh ~6% in 20,
+    # and host copies on this shared machine stall now and then for ~15 ms at
+    # a time, which a 50-step window (~80 ms) cannot absorb
+    n = max(200, min(args.steps, 400))
+    # an untimed pass of the same length first: in a fresh process the first
+    # few dozen pipelined steps showed one-off stalls of ~15 ms in the host
+    # copies (later passes ran clean at the compute rate)
+    warm = NSET + n
+    total = warm + n
     ev_in = [torch.cuda.Event() for _ in range(total)]
     ev_comp = [torch.cuda.Event() for _ in range(total)]
     ev_out = [torch.cuda.Event() for _ in range(total)]
@@ -755,18 +779,18 @@ def run_e2e(args, w, dev, stream, gbattn, credited, bm=None):
         ev_comp[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[i])
-            for dst, src in zip(outs_h[b], (s_["o"], s_["lse"], s_["dq"], s_["dk"], s_["dv"])):
+            for dst, src in zip(outs_h, (s_["o"], s_["lse"], s_["dq"], s_["dk"], s_["dv"])):
                 dst.copy_(src, non_blocking=True)
             ev_out[i].record(s_out)
 
-    for i in range(NSET):
+    for i in range(warm):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     replicas.barrier(dev)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
-    for i in range(NSET, total):
+    for i in range(warm, total):
         e2e_step(i)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
