@@ -21,11 +21,11 @@ EncodeTiledFn g_encode = nullptr;
 int* g_status[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 
-// Work counters of the persistent dQ kernel: kSchedSlots pairs of ints per
-// device, zero between launches (each launch's last CTA resets its pair).
-// Calls take the slots in turn, so backward calls in flight at the same
-// time on one device use different counters unless more than kSchedSlots
-// of them overlap.
+// Work counters of the persistent forward (D <= 128) and dQ kernels:
+// kSchedSlots pairs of ints per device, zero between launches (each launch's
+// last CTA resets its pair).  Calls take the slots in turn, so calls in
+// flight at the same time on one device use different counters unless more
+// than kSchedSlots of them overlap.
 constexpr int kSchedSlots = 64;
 int* g_sched[kMaxDevices] = {};
 std::atomic<unsigned> g_sched_next[kMaxDevices];
@@ -206,6 +206,7 @@ attn_status_t fwd_call(const void* q, const void* k, const void* v, void* o, flo
   const attn_status_t ds = device_state(&dev, &a.encode, &a.status, &a.num_sms);
   if (ds != ATTN_OK) return ds;
   a.q = q, a.k = k, a.v = v, a.o_out = o, a.lse_out = lse, a.block_mask = block_mask, a.kv_pitch = kv_pitch;
+  a.sched = sched_slot(g_sched[dev], g_sched_next[dev]);
   a.B = B, a.Hq = Hq, a.Hkv = Hkv, a.Lq = Lq, a.Lk = Lk, a.D = D;
   a.scale = scale, a.causal = causal != 0, a.bf16 = dtype == ATTN_DTYPE_BF16;
   a.stream = stream, a.limit_ns = wait_limit_ns();

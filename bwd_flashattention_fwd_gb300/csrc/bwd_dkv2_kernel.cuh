@@ -108,9 +108,6 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   const uint32_t sQ0 = sbase + Gm::V_BYTES;
   const uint32_t sdO0 = sQ0 + ST * Gm::Q_BYTES;
 
-  // A dQ kernel launched behind this one may start filling the SMs this grid
-  // frees as soon as every CTA of it is running (it reads none of its outputs).
-  if (threadIdx.x == 0) grid_launch_dependents();
   const int bhk = blockIdx.x;  // b * Hkv + hk
   const int b = bhk / p.Hkv, hk = bhk - b * p.Hkv;
   const int kt = blockIdx.y;
@@ -119,8 +116,6 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   static_assert(BK == kMaskBlock && 2 * BQ == kMaskBlock, "key tile = mask block, query tile = half a block");
   // query tile qt is computed (block mask)
   auto keep = [&](int qt) { return !MASKED || mask_keep(p, qt >> 1, kt); };
-  // (query head, computed query tile) iterations; every warp counts them itself
-  const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
   // extents for the debug build's index checks: rows of q / dq / lse /
   // delta, of dk / dv, and of the k / v buffers (pitch kv_pitch per head)
@@ -154,6 +149,16 @@ __global__ void __launch_bounds__(Dkv2Geom<D>::NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // Launched behind the delta kernel as a programmatic dependent, this grid
+  // may start while that kernel finishes: it reads nothing in global memory
+  // (lse, delta, the inputs, the block mask) before every earlier kernel on
+  // the stream has completed.  Only then may a dQ kernel launched behind this
+  // one start filling the SMs this grid frees (it reads lse and delta, but
+  // none of this grid's outputs, without waiting itself).
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  // (query head, computed query tile) iterations; every warp counts them itself
+  const int n_iter = p.G * count_kept<MASKED>(keep, qt_start, p.n_qtiles);
 
   if (warp == Gm::PRODUCER_WARP) {
     // ---------------- producer (whole warp) ----------------

@@ -30,7 +30,11 @@
 // indices to the other warps through a four-slot ring in shared memory.
 // While a CTA works on item i, its producer warp prefetches item i+1's Q and
 // dO tiles into shared memory with TMA, so starting the next item costs a
-// shared-to-tensor-memory copy instead of a global-memory round trip.
+// shared-to-tensor-memory copy instead of a global-memory round trip.  Once
+// the row threads have copied it out, the same buffer stages the finished
+// item's dQ (16-bit, in the swizzled layout of the output's tensor map), and
+// the producer writes it out with TMA stores before it loads the next Q and
+// dO there: the row threads never wait on a global store.
 // Barrier phases count key tiles and items over the CTA's whole life.
 //
 // Warp roles (352 threads): warps 0-7 row threads -- warp w owns TMEM lanes
@@ -116,13 +120,13 @@ template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     attn_bwd_dq3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const BwdParams p) {
+                        const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
   using Gm = Dq3Geom<D>;
   using E = Elem<BF16>;
   constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES, NDP = Gm::NDP;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_qbfull, bar_qbfree, bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_sfree,
+  __shared__ uint64_t bar_qbfull, bar_qbfree, bar_qread, bar_qready, bar_kvfull[ST], bar_kvempty[ST], bar_sfull, bar_sfree,
       bar_dpfull[NDP], bar_dsready[NDP], bar_dqdone, bar_mfin[2];
   __shared__ uint64_t bar_item[kDq3ItemRing];
   __shared__ volatile int item_ring[kDq3ItemRing];  // work item of round r in slot r % 4 (-1: no more)
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQb = sbase;                // prefetched Q tile
+  const uint32_t sQb = sbase;                // prefetched Q tile; an item's dQ on its way out
   const uint32_t sDOb = sQb + Gm::QB_BYTES;  // prefetched dO tile
   const uint32_t sK0 = sDOb + Gm::QB_BYTES;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
 
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     abort_flag = 0;
     mbar_init(smem_u32(&bar_qbfull), 1);
     mbar_init(smem_u32(&bar_qbfree), Gm::NCT);
+    mbar_init(smem_u32(&bar_qread), Gm::NCT);  // every row thread has read the Q / dO buffer
     mbar_init(smem_u32(&bar_qready), Gm::NCT);
     for (int s = 0; s < ST; ++s) {
       mbar_init(smem_u32(&bar_kvfull[s]), 1);
@@ -197,9 +202,26 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       tma_prefetch_desc(&tmdO);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdQ);
     }
     __syncwarp();
     int nqb = 0;  // Q / dO prefetches issued
+    // dQ of item d, which the row threads staged in the Q prefetch buffer
+    // (32-row tiles in the map's swizzled layout: 64-column chunk h of rows
+    // 32 * qd .. +31 at sQb + h * BQ * 128 + qd * 32 * 128), written out with
+    // one TMA store per tile; the buffer may take the next Q once they have
+    // read it.  Rows past Lq are outside the map and are not written.
+    auto store_dq = [&](const Dq3Item& d) {
+      if (lane == 0) {
+        for (int h = 0; h < NCH; ++h)
+          for (int qd = 0; qd < 4; ++qd)
+            if (d.qt * BQ + qd * 32 < p.Lq)
+              tma_store_3d(&tmdQ, sQb + h * (BQ * 128) + qd * (32 * 128), h * 64, d.qt * BQ + qd * 32, d.bh);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      __syncwarp();
+    };
     auto load_q = [&](int w) {
       const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
       ++nqb;
@@ -226,6 +248,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     RingPos<ST> kv;  // stage of the next key tile
     bool wrapped = false;  // the ring has been filled once: stages must be freed first
     int r = 0;
+    Dq3Item prev{};  // the item of the previous round
     int w = take_item();
     publish(0, w);
     if (w >= 0) load_q(w);
@@ -252,14 +275,25 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       }
       // The row threads copied this item's Q / dO out of the buffer when the
       // item started (after every MMA of round r - 1 had completed, so every
-      // warp has read round r - 1's slot): round r + 1 may take the slot of
-      // round r - 3, and the buffer the next item's Q / dO.
+      // warp has read round r - 1's slot) and staged round r - 1's dQ in it:
+      // round r + 1 may take the slot of round r - 3, and once that dQ is
+      // out, the buffer the next item's Q / dO.
       w = take_item();
       mbar_wait(smem_u32(&bar_qbfree), r & 1, g, wait_code<72>());
       __syncwarp();
+      if (r > 0 && !abort_flag) store_dq(prev);
+      prev = it;
       publish(r + 1, w);
       if (w >= 0 && !abort_flag) load_q(w);
     }
+    // the last item's dQ, staged after its last MMA
+    if (r > 0 && !abort_flag) {
+      mbar_wait(smem_u32(&bar_qbfree), r & 1, g, wait_code<74>());
+      __syncwarp();
+      if (!abort_flag) store_dq(prev);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     // the last Q / dO prefetch and the last ST issued stages (fewer if the
     // ring never wrapped; a stage is refilled only after its release, so each
     // holds at most one copy in flight)
@@ -376,8 +410,9 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
     // row % 8; zeros past Lq and past D) into tensor memory: this warp copies
     // elements [half*D/2, (half+1)*D/2) of its 32 rows as 16-bit pairs.  No
     // MMA of the previous item reads them any more (its final commit has
-    // completed).
-    auto copy_q = [&](int rn) {
+    // completed).  The first item hands the buffer back at once; later ones
+    // after the epilogue has staged the previous item's dQ in it.
+    auto copy_q = [&](int rn, bool release) {
       mbar_wait(smem_u32(&bar_qbfull), rn & 1, g, wait_code<73>());
       uint32_t qa[HALF / 2], oa[HALF / 2];
 #pragma unroll
@@ -389,8 +424,10 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
         oa[4 * v + 0] = y.x, oa[4 * v + 1] = y.y, oa[4 * v + 2] = y.z, oa[4 * v + 3] = y.w;
       }
       // the producer may refill the buffer once every row thread has read it
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bar_qbfree));
+      if (release) {
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bar_qbfree));
+      }
       // HALF / 2 packed columns: 16, 24 or 32 (D = 64, 96, 128)
 #pragma unroll
       for (int c = 0; c + 16 <= HALF / 2; c += 16) {
@@ -416,7 +453,7 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(smem_u32(&bar_qready));
     };
-    if (round_item(0) >= 0) copy_q(0);
+    if (round_item(0) >= 0) copy_q(0, true);
     for (int r = 0, w = round_item(0); w >= 0; w = round_item(++r)) {
       const Dq3Item it = dq3_item(w, BH, p.n_qtiles);
       const int q0 = it.qt * BQ;
@@ -494,22 +531,36 @@ __global__ void __launch_bounds__(Dq3Geom<D>::NUM_THREADS, 1)
       __syncwarp();
       tc_fence_after_sync();
       // the next item's Q and dO first, so that its first S and dP products
-      // run while this item's dQ is read out and stored
-      if (round_item(r + 1) >= 0) copy_q(r + 1);
-      typename E::T* dqrow = reinterpret_cast<typename E::T*>(p.dq) + row * D;
+      // run while this item's dQ is read out and stored (copying them right
+      // after the item's last dS instead measured 32% slower at D = 96 and no
+      // faster at D = 128)
+      if (round_item(r + 1) >= 0) copy_q(r + 1, false);
+      // Every row thread has read the prefetch buffer: it now stages this
+      // item's dQ, warp (quad, half) writing 64-column chunk `half` of its 32
+      // rows, for the producer's TMA stores.  Staging through shared memory
+      // keeps the stores off the load/store unit (a store per row from every
+      // thread touches 32 rows' lines per instruction).
+      mbar_arrive(smem_u32(&bar_qread));
+      mbar_wait(smem_u32(&bar_qread), r & 1, g, wait_code<75>());
+      if (half < NCH) {
+        const uint32_t stg = sQb + half * (BQ * 128) + quad * (32 * 128) + lane * 128;
 #pragma unroll 1
-      for (int c = half; c < D / 32; c += 2) {
-        uint32_t rr[32];
-        if (nk > 0) {
-          tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
-          tmem_ld_wait(rr);
-        } else {
+        for (int c = 2 * half; c < 2 * half + 2 && c < D / 32; ++c) {
+          uint32_t rr[32];
+          if (nk > 0) {  // same for the whole CTA: tcgen05.ld is warp-collective
+            tmem_ld32(tmem + lrow + Gm::DQ_COL + c * 32, rr);
+            tmem_ld_wait(rr);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept key tile: dQ = 0
+            for (int i = 0; i < 32; ++i) rr[i] = 0u;  // no kept key tile: dQ = 0
+          }
+          uint32_t pk[16];
+          pack_row32<BF16>(rr, p.scale, pk);
+          stage_row16_sw128(stg, lane, (c & 1) * 4, pk);
         }
-        if (qi < p.Lq && dbg_in_range(row * D + c * 32, 32, n_qrows * D, p.status, 9))
-          store_row32<BF16>(dqrow + c * 32, rr, p.scale);
       }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bar_qbfree));
       // The next item's first dQ MMA overwrites these columns; it is issued
       // after this thread's next dS arrival, which follows these loads.
       tc_fence_before_sync();

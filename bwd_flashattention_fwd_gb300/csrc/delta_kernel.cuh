@@ -64,6 +64,11 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const void* __restrict_
   using Gm = DeltaGeom<D>;
   using V = VecT<Gm::VEC>;
   using E = Elem<BF16>;
+  // Launched behind the forward as a programmatic dependent: O is read only
+  // once every earlier kernel on the stream has completed, and a dK/dV kernel
+  // launched behind this one may start once every CTA of it has got here.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int sub = lane % Gm::LPR;        // lane within the row group
   const int grp = lane / Gm::LPR;        // row group within the warp

@@ -34,11 +34,20 @@
 // share of the issue slots of the sub-partitions the MMA warps run on, low.
 //
 // Persistent: one CTA per SM walks a list of (256-row query pair, head) work
-// items, heaviest first, dealt to the CTAs in alternating (snake) order.  As
-// soon as an item's last S MMAs have completed, the producer loads the next
+// items, heaviest first: each CTA starts with the item of its own index and
+// takes the next from a global counter when its producer has issued the
+// current one's copies, and hands the index to the other warps through a
+// four-slot ring in shared memory (a static deal left the busiest CTA ~10%
+// above the mean).  As soon as an item's last S MMAs have completed, the producer loads the next
 // item's Q into the (then unused) Q buffer, and the MMA warps compute the next
 // item's first S tiles while the softmax warps write out the current item's O
 // and lse.  Barrier phases count key tiles and items over the CTA's life.
+// O goes out through shared memory: each softmax warp converts its 32 rows
+// into a 4 KB staging tile (64 columns at a time, in the swizzled layout of
+// the output's tensor map) and one lane issues a TMA store, so the tensor
+// pipe idles only briefly between items (a 16-byte store per row from every
+// thread kept the load/store unit busy for ~3 us per item).  The staging
+// costs one K/V ring stage, which measured free.
 //
 // MASKED: block-sparse variant ("feat(attention): complete Flash Attention
 // VJP implementation", section "Sparse Block Masks"; the forward applies the
@@ -53,6 +62,8 @@
 
 namespace gbattn {
 
+constexpr int kFwdItemRing = 4;  // rounds whose item index a CTA keeps in shared memory
+
 template <int D>
 struct Fwd2Geom {
   static constexpr int BQ = 128;  // rows per query tile; the CTA owns 2 tiles
@@ -60,9 +71,11 @@ struct Fwd2Geom {
   static constexpr int NCH = n_chunks(D);
   static constexpr int Q_BYTES = NCH * BQ * 128;
   static constexpr int KV_BYTES = NCH * BK * 128;
-  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * Q_BYTES;
+  // O staging: each softmax warp's 32 rows x 64 columns (16-bit), swizzled
+  static constexpr int O_STG_BYTES = 32 * 128;
+  static constexpr int AVAIL = kMaxDynSmem - 512 - 1024 - 2 * Q_BYTES - 8 * O_STG_BYTES;
   static constexpr int STAGES = AVAIL / (2 * KV_BYTES) > 6 ? 6 : AVAIL / (2 * KV_BYTES);  // K_j + V_j each
-  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + STAGES * 2 * KV_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + STAGES * 2 * KV_BYTES + 8 * O_STG_BYTES;
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_THREADS = 352;
   static constexpr float TAU = 8.0f;
@@ -76,7 +89,8 @@ struct Fwd2Geom {
 template <int D, bool BF16, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const FwdParams p) {
   using Gm = Fwd2Geom<D>;
   using E = Elem<BF16>;
   constexpr int BQ = Gm::BQ, BK = Gm::BK, NCH = Gm::NCH, ST = Gm::STAGES;
@@ -84,13 +98,22 @@ __global__ void __launch_bounds__(352, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qfree, bar_kvfull[ST], bar_kvempty[ST], bar_sfull[2][2], bar_pready[2][2],
       bar_odone[2], bar_done, bar_mfin[2];
+  // work item of round r in slot r % 4 (-1: no more); bar_itemfree: every
+  // consumer warp (the MMA and softmax warps) has read the slot
+  __shared__ uint64_t bar_item[kFwdItemRing], bar_itemfree[kFwdItemRing];
+  __shared__ volatile int item_ring[kFwdItemRing];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
+  // A kernel launched behind this one as a programmatic dependent (the delta
+  // kernel) may take the SMs this grid frees; it waits for this grid to
+  // complete before it reads anything.
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;  // tile t at sQ + t * Q_BYTES
   const uint32_t sK0 = sQ + 2 * Gm::Q_BYTES;  // stage s: K at sK0 + 2s * KV_BYTES, V right after
+  const uint32_t sO = sK0 + ST * 2 * Gm::KV_BYTES;  // softmax warp w's O staging at sO + w * O_STG_BYTES
 
   // work items: w -> (query pair pt, head bh), heaviest query pairs first;
   // n_qtiles counts 256-row pairs
@@ -98,12 +121,6 @@ __global__ void __launch_bounds__(352, 1)
   const int n_items = p.n_qtiles * BH;
   auto item_pt = [&](int w) { return p.n_qtiles - 1 - w / BH; };
   auto item_bh = [&](int w) { return w - (w / BH) * BH; };
-  // item of this CTA's round r (snake order over the CTAs), or -1
-  auto round_item = [&](int r) {
-    const int nc = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int w = r * nc + ((r & 1) ? nc - 1 - c : c);
-    return w < n_items ? w : -1;
-  };
   auto n_kv_of = [&](int pt) {
     const int q_hi = min(pt * 2 * BQ + 2 * BQ, p.Lq);
     const int kv_end = CAUSAL ? min(p.Lk, q_hi + p.off) : p.Lk;
@@ -120,6 +137,17 @@ __global__ void __launch_bounds__(352, 1)
   // computed key tiles of pair pt (warp-collective)
   auto n_kept = [&](int pt) { return count_kept<MASKED>([&](int j) { return keep(pt, j); }, 0, n_kv_of(pt)); };
   const WaitGuard g{&abort_flag, p.status, p.limit_ns};
+  // The work item of round r, as the producer published it (warp-collective);
+  // -1 ends the loop (also once a wait has run out, so no loop outlives an
+  // abort).  The warp hands the slot back once every lane has read it.
+  auto round_item = [&](int r) {
+    const int slot = r % kFwdItemRing;
+    mbar_wait(smem_u32(&bar_item[slot]), (r / kFwdItemRing) & 1, g, wait_code<36>());
+    const int w = abort_flag ? -1 : item_ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bar_itemfree[slot]));
+    return w;
+  };
   // extents for the debug build's index checks: rows of q / o / lse
   [[maybe_unused]] const size_t n_qrows = static_cast<size_t>(p.B) * p.Hq * p.Lq;
 
@@ -142,6 +170,10 @@ __global__ void __launch_bounds__(352, 1)
     }
     mbar_init(smem_u32(&bar_done), 2);
     for (int t = 0; t < 2; ++t) mbar_init(smem_u32(&bar_mfin[t]), 1);
+    for (int i = 0; i < kFwdItemRing; ++i) {
+      mbar_init(smem_u32(&bar_item[i]), 1);
+      mbar_init(smem_u32(&bar_itemfree[i]), 10);  // warps 0-7 and 9-10
+    }
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -159,14 +191,39 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
     }
     __syncwarp();
     RingPos<ST> st;  // stage of the next key tile
     int issued = 0;  // key tiles issued (all items)
     int nq = 0;      // items whose Q was loaded
+    // The next item from the global counter (warp-collective), -1 past the
+    // end; each CTA's first item is its own index (the grid has at most one
+    // CTA per item), so the counter starts behind them.
+    auto take_item = [&]() {
+      int t = 0;
+      if (lane == 0) t = atomicAdd(p.sched, 1);
+      t = __shfl_sync(0xffffffffu, t, 0) + static_cast<int>(gridDim.x);
+      return t < n_items ? t : -1;
+    };
+    // round r's item into its ring slot, once every consumer warp has read
+    // the round that used the slot before
+    auto publish = [&](int r, int w) {
+      const int slot = r % kFwdItemRing;
+      if (r >= kFwdItemRing)
+        mbar_wait(smem_u32(&bar_itemfree[slot]), ((r / kFwdItemRing) - 1) & 1, g, wait_code<95>());
+      __syncwarp();
+      if (lane == 0) {
+        item_ring[slot] = abort_flag ? -1 : w;
+        mbar_arrive(smem_u32(&bar_item[slot]));
+      }
+      __syncwarp();
+    };
+    int w = static_cast<int>(blockIdx.x);
+    publish(0, w);
     // After an abort (a wait ran out) no further copy is issued, so the
     // drains below cover every copy still in flight.
-    for (int r = 0, w = round_item(0); w >= 0 && !abort_flag; w = round_item(++r)) {
+    for (int r = 0; w >= 0 && !abort_flag; ++r) {
       const int pt = item_pt(w), bh = item_bh(w);
       const int b = bh / p.Hq, hq = bh - b * p.Hq;
       const int zkv = b * p.Hkv + hq / p.G;
@@ -197,6 +254,9 @@ __global__ void __launch_bounds__(352, 1)
         st.next();
         ++issued;
       }
+      // the next item, published while the MMA warps still work on this one
+      w = take_item();
+      publish(r + 1, w);
     }
     // the last ST issued stages (each slot holds at most one copy in
     // flight: a stage is refilled only after its release), and the last Q
@@ -393,20 +453,40 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_after_sync();
       const bool empty = MASKED && !(l > 0.f);  // the row saw no key: O = 0, lse = +inf
       const float inv_l = empty ? 0.f : 1.f / l;
-      typename E::T* orow = reinterpret_cast<typename E::T*>(p.o) + (static_cast<size_t>(bh) * p.Lq + qi) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
+      // O leaves through this warp's staging tile (its 32 rows x 64 columns
+      // in the tensor map's swizzled layout) and one TMA store per 64
+      // columns, which keeps the stores off the load/store unit: a store per
+      // row from every thread would touch 32 rows' lines per instruction.
+      // Rows past Lq are outside the map and are not written.
+      const uint32_t stg = sO + warp * Gm::O_STG_BYTES;
+#pragma unroll
+      for (int h = 0; h < NCH; ++h) {
+        // columns 64h .. 64h+63 (the second chunk exists unless D = 96, h = 1),
+        // read and rounded while the tile's previous store still reads it
+        const bool two = 2 * h + 1 < D / 32;
+        uint32_t ra[32], rb[32], pa[16], pb[16];
         if (!MASKED || nk > 0) {  // same for the whole CTA: tcgen05.ld is warp-collective
-          tmem_ld32(o_col + c * 32, rr);
-          tmem_ld_wait(rr);
+          tmem_ld32(o_col + 2 * h * 32, ra);
+          if (two) tmem_ld32(o_col + (2 * h + 1) * 32, rb);
+          tmem_ld_wait(ra);  // waits for both loads
+          if (two) reg_fence(rb);
         }
         if (MASKED && (nk == 0 || empty)) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+          for (int i = 0; i < 32; ++i) ra[i] = rb[i] = 0u;
         }
-        if (qi < p.Lq && dbg_in_range((static_cast<size_t>(bh) * p.Lq + qi) * D + c * 32, 32, n_qrows * D, p.status, 1))
-          store_row32<BF16>(orow + c * 32, rr, inv_l);
+        pack_row32<BF16>(ra, inv_l, pa);
+        if (two) pack_row32<BF16>(rb, inv_l, pb);
+        if (lane == 0) bulk_wait_read_all();  // the tile's previous store has read it
+        __syncwarp();
+        stage_row16_sw128(stg + lane * 128, lane, 0, pa);
+        if (two) stage_row16_sw128(stg + lane * 128, lane, 4, pb);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmO, stg, h * 64, q0t + quad * 32, bh);
+          bulk_commit_group();
+        }
       }
       if (qi < p.Lq && dbg_in_range(static_cast<size_t>(bh) * p.Lq + qi, 1, n_qrows, p.status, 2))
         p.lse[static_cast<size_t>(bh) * p.Lq + qi] = empty ? INFINITY : m + log2f(l);
@@ -414,6 +494,9 @@ __global__ void __launch_bounds__(352, 1)
       // P arrival, which follows these loads
       tc_fence_before_sync();
     }
+    // the O stores have read their staging tiles and written global memory
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -421,6 +504,16 @@ __global__ void __launch_bounds__(352, 1)
   if (warp == 9) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    // The last CTA to finish puts the work counter back to zero: every CTA
+    // has taken its last item by now.
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      p.sched[0] = 0;
+      p.sched[1] = 0;
+      __threadfence();
+    }
   }
 }
 

@@ -64,14 +64,35 @@ int launch(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, con
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
+// Launch as a programmatic dependent of the previous kernel on the stream:
+// its CTAs may start while that kernel finishes, so the kernel waits for it
+// (griddepcontrol.wait) before reading anything in global memory.
+template <typename Kern, typename... Args>
+int launch_dependent(Kern kern, dim3 grid, int threads, int smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return kLaunchCudaError;
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+}
+
 // D <= 128: two 128-row query tiles per work item, persistent CTAs (fwd2_kernel.cuh).
 template <bool BF16, bool CAUSAL, bool MASKED>
 int fwd2_impl(const AttnArgs& a) {
   using Gm = Fwd2Geom<(kD <= 128 ? kD : 128)>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
+  // O is written by TMA stores of one softmax warp's 32 rows
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) ||
       !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &to, a.o_out, a.Lq, a.B * a.Hq, 32))
     return kLaunchBadMap;
   FwdParams p{};
   p.o = a.o_out;
@@ -84,12 +105,16 @@ int fwd2_impl(const AttnArgs& a) {
   p.nkb = (a.Lk + kMaskBlock - 1) / kMaskBlock;
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.limit_ns = a.limit_ns;
+  p.sched = a.sched;
   // persistent: one CTA per SM (fewer when there are fewer work items)
   const long long n_items = static_cast<long long>(p.n_qtiles) * a.B * a.Hq;
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  return launch(attn_fwd2_kernel<(kD <= 128 ? kD : 128), BF16, CAUSAL, MASKED>, grid, Gm::NUM_THREADS,
-                Gm::SMEM_BYTES, a.stream, tq, tk, tv, p);
+  auto kern = attn_fwd2_kernel<(kD <= 128 ? kD : 128), BF16, CAUSAL, MASKED>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
+    return kLaunchCudaError;
+  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tk, tv, to, p);
+  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
 template <bool BF16, bool CAUSAL>
@@ -180,8 +205,8 @@ int dkv2_impl(const AttnArgs& a) {
   auto kern = attn_bwd_dkv2_kernel<DD, BF16, CAUSAL, MASKED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES) != cudaSuccess)
     return kLaunchCudaError;
-  kern<<<grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream>>>(tq, tv, tdo, a.k, p);
-  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+  // behind the delta kernel: its CTAs start as that kernel's retire
+  return launch_dependent(kern, grid, Gm::NUM_THREADS, Gm::SMEM_BYTES, a.stream, tq, tv, tdo, a.k, p);
 }
 
 // D <= 128: Q and dO held in tensor memory as MMA A operands (bwd_dq3_kernel.cuh).
@@ -192,10 +217,12 @@ template <bool BF16, bool CAUSAL, bool MASKED>
 int dq3_impl(const AttnArgs& a, bool behind_dkv) {
   constexpr int DD = kD <= 128 ? kD : 128;
   using Gm = Dq3Geom<DD>;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdq;
+  // dQ is written by TMA stores of 32-row tiles
   if (!make_map(a, &tq, a.q, a.Lq, a.B * a.Hq, Gm::BQ) || !make_map(a, &tdo, a.dO, a.Lq, a.B * a.Hq, Gm::BQ) ||
       !make_map(a, &tk, a.k, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
-      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch))
+      !make_map(a, &tv, a.v, a.Lk, a.B * a.Hkv, Gm::BK, a.kv_pitch) ||
+      !make_map(a, &tdq, a.dq, a.Lq, a.B * a.Hq, 32))
     return kLaunchBadMap;
   BwdParams p = bwd_params(a);
   p.n_qtiles = (a.Lq + Gm::BQ - 1) / Gm::BQ;
@@ -218,7 +245,7 @@ int dq3_impl(const AttnArgs& a, bool behind_dkv) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = behind_dkv ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kern, tq, tdo, tk, tv, p) != cudaSuccess) return kLaunchCudaError;
+  if (cudaLaunchKernelEx(&cfg, kern, tq, tdo, tk, tv, tdq, p) != cudaSuccess) return kLaunchCudaError;
   return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
 }
 
@@ -393,9 +420,9 @@ int delta_impl(const AttnArgs& a) {
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = static_cast<long long>(a.num_sms > 0 ? a.num_sms : 152) * 8;
   if (blocks > cap) blocks = cap;
-  attn_delta_kernel<kD, BF16><<<static_cast<unsigned>(blocks), Gm::THREADS, 0, a.stream>>>(a.o, a.dO, a.delta_out,
-                                                                                            rows);
-  return cudaPeekAtLastError() == cudaSuccess ? kLaunchOk : kLaunchCudaError;
+  // behind the forward: its CTAs take the SMs the forward's last CTAs free
+  return launch_dependent(attn_delta_kernel<kD, BF16>, dim3(static_cast<unsigned>(blocks)), Gm::THREADS, 0, a.stream,
+                          static_cast<const void*>(a.o), static_cast<const void*>(a.dO), a.delta_out, rows);
 }
 
 }  // namespace inst_d<D>

@@ -75,6 +75,9 @@ struct FwdParams {
   int qmod, split_tiles;
   float* ws;
   float* ws_lse;
+  // persistent forward: its work counter and the count of CTAs that have
+  // finished (two ints, zero at launch; the last CTA puts them back to zero)
+  int* sched;
 };
 
 struct BwdParams {
@@ -222,6 +225,26 @@ __device__ __forceinline__ void store_row32(void* dst, const uint32_t (&r)[32], 
     w.w = Elem<BF16>::pack(__uint_as_float(r[q * 8 + 6]) * mul, __uint_as_float(r[q * 8 + 7]) * mul);
     d[q] = w;
   }
+}
+
+// Scale 32 fp32 values and round them to 16-bit pairs.
+template <bool BF16>
+__device__ __forceinline__ void pack_row32(const uint32_t (&v)[32], float mul, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    pk[i] = Elem<BF16>::pack(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+}
+
+// Write 16 packed pairs (64 bytes) as the 16-byte pieces p0..p0+3 of row r of
+// a shared-memory tile of 128-byte rows in the 128-byte-swizzled layout that
+// a TMA store with that swizzle reads (piece p of row r sits (p ^ (r mod 8))
+// * 16 bytes into the row; the tile starts on a 1024-byte boundary).  One
+// warp writing one row per lane touches every bank group once per eight rows,
+// so the four stores are free of conflicts.
+__device__ __forceinline__ void stage_row16_sw128(uint32_t row_addr, int r, int p0, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(row_addr + ((((p0 + q) ^ r) & 7) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
 // Position in a ring of N slots whose barriers flip phase once per lap:
