@@ -37,8 +37,8 @@
 // items, heaviest first: each CTA starts with the item of its own index and
 // takes the next from a global counter when its producer has issued the
 // current one's copies, and hands the index to the other warps through a
-// four-slot ring in shared memory (a static deal left the busiest CTA ~10%
-// above the mean).  As soon as an item's last S MMAs have completed, the producer loads the next
+// four-slot ring in shared memory (a static deal left the busiest CTA's
+// key-tile loops ~8% above the median at L = 2048).  As soon as an item's last S MMAs have completed, the producer loads the next
 // item's Q into the (then unused) Q buffer, and the MMA warps compute the next
 // item's first S tiles while the softmax warps write out the current item's O
 // and lse.  Barrier phases count key tiles and items over the CTA's life.

@@ -80,6 +80,11 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * computed once, before the two gradient kernels).
  *   o, dO [B,Hq,Lq,D]: inputs (dtype); o is the forward's stored output.
  *   delta [B,Hq,Lq]: output, float32.
+ * Launched as a programmatic dependent of the work before it on the stream:
+ * its CTAs may start while the previous kernel finishes, but it reads
+ * nothing before all earlier work on the stream has completed, so stream
+ * order holds for the caller as with a plain launch.  (The D <= 128 dK/dV
+ * kernel of attn_bwd / attn_bwd_dkv is launched the same way.)
  */
 attn_status_t attn_bwd_delta(const void* o, const void* dO, float* delta, int B, int Hq, int Lq,
                              int D, attn_dtype_t dtype, cudaStream_t stream);
